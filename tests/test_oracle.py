@@ -1,0 +1,270 @@
+"""Pins of the float64 oracle against facts the pages and the mathematics fix.
+
+Each test checks one closed form, invariant or independent restatement, chosen
+so that a plausible slip in the oracle (a dropped scale, a wrong sign, a
+transposed operand, a missing or misplaced causal mask) fails at least one.
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import attention as oa
+from attn_inputs import make_inputs, bf16_bits_to_f64
+
+
+def rand(shape, seed):
+    return np.random.default_rng(seed).standard_normal(shape)
+
+
+def qkv(B, H, N, d, seed):
+    return rand((B, H, N, d), seed), rand((B, H, N, d), seed + 1), rand((B, H, N, d), seed + 2)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_probability_rows_sum_to_one(causal):
+    q, k, _ = qkv(2, 3, 37, 8, 1)
+    p = oracle.attention_probabilities(q, k, causal, 0.3)
+    np.testing.assert_allclose(p.sum(-1), 1.0, rtol=0, atol=1e-13)
+    assert (p >= 0).all()
+    if causal:
+        # entries right of the diagonal are exactly zero
+        iu = np.triu_indices(37, 1)
+        assert np.all(p[:, :, iu[0], iu[1]] == 0.0)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_constant_value_column_passes_through(causal):
+    q, k, v = qkv(1, 2, 29, 6, 2)
+    v[..., 3] = 2.5
+    o, _ = oracle.attention_forward(q, k, v, causal, 0.7)
+    np.testing.assert_allclose(o[..., 3], 2.5, rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_equal_logits_give_prefix_mean(causal):
+    B, H, N, d = 1, 2, 23, 5
+    _, k, v = qkv(B, H, N, d, 3)
+    q = np.zeros((B, H, N, d))
+    o, lse = oracle.attention_forward(q, k, v, causal, 0.125)
+    if causal:
+        counts = np.arange(1, N + 1)
+        expect = np.cumsum(v, axis=2) / counts[:, None]
+        expect_lse = np.log(counts)
+    else:
+        expect = np.broadcast_to(v.mean(axis=2, keepdims=True), v.shape)
+        expect_lse = np.full(N, np.log(N))
+    np.testing.assert_allclose(o, expect, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse, np.broadcast_to(expect_lse, lse.shape), rtol=0, atol=1e-13)
+
+
+def test_causal_row_zero_returns_first_value():
+    q, k, v = qkv(2, 2, 17, 4, 4)
+    scale = 0.5
+    o, lse = oracle.attention_forward(q, k, v, True, scale)
+    np.testing.assert_allclose(o[:, :, 0], v[:, :, 0], rtol=0, atol=1e-14)
+    np.testing.assert_allclose(lse[:, :, 0], scale * np.sum(q[:, :, 0] * k[:, :, 0], -1), rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_single_key(causal):
+    q, k, v = qkv(2, 3, 1, 7, 5)
+    o, lse = oracle.attention_forward(q, k, v, causal, 0.9)
+    np.testing.assert_allclose(o, v, rtol=0, atol=1e-14)
+    np.testing.assert_allclose(lse[..., 0], 0.9 * np.sum(q[..., 0, :] * k[..., 0, :], -1), atol=1e-13)
+
+
+def test_two_keys_logistic_closed_form():
+    q, k, v = qkv(1, 1, 2, 3, 6)
+    scale = 0.8
+    o, lse = oracle.attention_forward(q, k, v, False, scale)
+    for i in range(2):
+        s0 = scale * q[0, 0, i] @ k[0, 0, 0]
+        s1 = scale * q[0, 0, i] @ k[0, 0, 1]
+        w0 = 1.0 / (1.0 + np.exp(s1 - s0))
+        w1 = 1.0 / (1.0 + np.exp(s0 - s1))
+        np.testing.assert_allclose(o[0, 0, i], w0 * v[0, 0, 0] + w1 * v[0, 0, 1], atol=1e-14)
+        np.testing.assert_allclose(lse[0, 0, i], np.log(np.exp(s0) + np.exp(s1)), atol=1e-13)
+
+
+def test_joint_key_value_permutation_invariance():
+    q, k, v = qkv(1, 2, 31, 8, 7)
+    perm = np.random.default_rng(0).permutation(31)
+    o1, l1 = oracle.attention_forward(q, k, v, False, 0.35)
+    o2, l2 = oracle.attention_forward(q, k[:, :, perm], v[:, :, perm], False, 0.35)
+    np.testing.assert_allclose(o1, o2, atol=1e-13)
+    np.testing.assert_allclose(l1, l2, atol=1e-13)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_key_shift_moves_lse_only(causal):
+    q, k, v = qkv(1, 2, 19, 6, 8)
+    u = rand((6,), 99)
+    scale = 0.4
+    o1, l1 = oracle.attention_forward(q, k, v, causal, scale)
+    o2, l2 = oracle.attention_forward(q, k + u, v, causal, scale)
+    np.testing.assert_allclose(o1, o2, atol=1e-12)
+    np.testing.assert_allclose(l2 - l1, scale * (q @ u), atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_gradient_sum_identities(causal):
+    q, k, v = qkv(2, 2, 27, 5, 9)
+    do = rand(q.shape, 10)
+    dq, dk, dv = oracle.attention_backward(q, k, v, do, causal, 0.6)
+    # rows of dS sum to zero, so the key gradients sum to zero over keys
+    np.testing.assert_allclose(dk.sum(axis=2), 0.0, atol=1e-12)
+    # P^T has columns summing to one, so sum_j dV_j = sum_i dO_i
+    np.testing.assert_allclose(dv.sum(axis=2), do.sum(axis=2), atol=1e-12)
+    assert np.abs(dq).max() > 0
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("blocks", [(4, 4), (5, 3), (16, 7), (64, 64), (1, 9)])
+def test_tiled_variants_agree(causal, blocks):
+    B, H, N, d = 2, 2, 29, 6
+    q, k, v = qkv(B, H, N, d, 11)
+    do = rand(q.shape, 12)
+    scale = 0.45
+    o, lse = oracle.attention_forward(q, k, v, causal, scale)
+    o_t, lse_t = oracle.tiled_forward(q, k, v, causal, scale, *blocks)
+    np.testing.assert_allclose(o_t, o, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse_t, lse, rtol=0, atol=1e-12)
+    g = oracle.attention_backward(q, k, v, do, causal, scale)
+    g_t = oracle.tiled_backward(q, k, v, o, lse, do, causal, scale, *blocks)
+    for a, b in zip(g_t, g):
+        np.testing.assert_allclose(a, b, rtol=0, atol=1e-12)
+
+
+def test_row_sampled_forward_matches_full():
+    q, k, v = qkv(1, 1, 300, 8, 13)
+    rows = np.array([0, 1, 17, 255, 256, 299])
+    for causal in (False, True):
+        o, lse = oracle.attention_forward(q, k, v, causal, 0.3)
+        o_r, l_r = oracle.attention_forward_rows(q[0, 0], k[0, 0], v[0, 0], rows, causal, 0.3)
+        np.testing.assert_allclose(o_r, o[0, 0, rows], atol=1e-14)
+        np.testing.assert_allclose(l_r, lse[0, 0, rows], atol=1e-14)
+
+
+def test_backward_head_subset():
+    q, k, v = qkv(2, 2, 9, 3, 14)
+    do = rand(q.shape, 15)
+    full = oracle.attention_backward(q, k, v, do, True, 0.5)
+    part = oracle.attention_backward(q, k, v, do, True, 0.5, heads=[(1, 0)])
+    for a, b in zip(part, full):
+        np.testing.assert_allclose(a[1, 0], b[1, 0], atol=1e-15)
+        assert np.all(a[0] == 0)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_torch_float64_sdpa_and_autograd_agree(causal):
+    torch = pytest.importorskip("torch")
+    B, H, N, d = 2, 3, 33, 8
+    q, k, v = qkv(B, H, N, d, 16)
+    do = rand(q.shape, 17)
+    scale = 0.21
+    tq, tk, tv = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (q, k, v))
+    to = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=causal, scale=scale)
+    to.backward(torch.tensor(do))
+    o, lse = oracle.attention_forward(q, k, v, causal, scale)
+    np.testing.assert_allclose(o, to.detach().numpy(), rtol=0, atol=1e-12)
+    s = scale * torch.tensor(q) @ torch.tensor(k).transpose(-1, -2)
+    if causal:
+        s = s.masked_fill(torch.ones(N, N, dtype=torch.bool).triu(1), float("-inf"))
+    np.testing.assert_allclose(lse, torch.logsumexp(s, -1).numpy(), rtol=0, atol=1e-12)
+    dq, dk, dv = oracle.attention_backward(q, k, v, do, causal, scale)
+    np.testing.assert_allclose(dq, tq.grad.numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dk, tk.grad.numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dv, tv.grad.numpy(), rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_central_finite_differences(causal):
+    B, H, N, d = 1, 1, 6, 3
+    q, k, v = qkv(B, H, N, d, 18)
+    do = rand(q.shape, 19)
+    scale = 0.7
+    dq, dk, dv = oracle.attention_backward(q, k, v, do, causal, scale)
+
+    def loss(q_, k_, v_):
+        o, _ = oracle.attention_forward(q_, k_, v_, causal, scale)
+        return float(np.sum(o * do))
+
+    h = 1e-6
+    for idx, (x, g) in enumerate(((q, dq), (k, dk), (v, dv))):
+        num = np.zeros_like(x)
+        for pos in np.ndindex(x.shape):
+            xp = x.copy()
+            xm = x.copy()
+            xp[pos] += h
+            xm[pos] -= h
+            args_p = [q, k, v]
+            args_m = [q, k, v]
+            args_p[idx] = xp
+            args_m[idx] = xm
+            num[pos] = (loss(*args_p) - loss(*args_m)) / (2 * h)
+        np.testing.assert_allclose(g, num, rtol=1e-6, atol=1e-8)
+
+
+def test_lse_bounds_row_max():
+    q, k, v = qkv(1, 2, 40, 8, 20)
+    scale = 0.5
+    _, lse = oracle.attention_forward(q, k, v, True, scale)
+    s = scale * q @ np.swapaxes(k, -1, -2)
+    s = np.where(np.triu(np.ones((40, 40), bool), 1), -np.inf, s)
+    m = s.max(-1)
+    assert np.all(lse >= m - 1e-12)
+    assert np.all(lse <= m + np.log(np.arange(1, 41)) + 1e-12)
+
+
+def test_bf16_inputs_promote_exactly():
+    x = make_inputs(1, 1, 4, 8, 123, tensors=("q",))["q"]
+    f = bf16_bits_to_f64(x)
+    # every value has at most 8 significant bits
+    mant, _ = np.frexp(f)
+    assert np.all(mant * 256 == np.round(mant * 256))
+
+
+# ---- planted mistakes: each must be caught by a pin above -------------------
+
+def _forward_with(monkeypatch, fake_scores, causal):
+    monkeypatch.setattr(oa, "_scores", fake_scores)
+    q, k, v = qkv(1, 1, 5, 3, 21)
+    return oracle.attention_forward(q, k, v, causal, 0.5), (q, k, v)
+
+
+def test_planted_missing_scale_is_caught(monkeypatch):
+    real = oa._scores
+
+    def no_scale(q_rows, k, row_ids, causal, scale):
+        return real(q_rows, k, row_ids, causal, 1.0)
+
+    (o, lse), (q, k, v) = _forward_with(monkeypatch, no_scale, True)
+    # causal row 0 pin: L_0 = scale * q_0 . k_0
+    assert abs(lse[0, 0, 0] - 0.5 * q[0, 0, 0] @ k[0, 0, 0]) > 1e-6
+
+
+def test_planted_mask_off_by_one_is_caught(monkeypatch):
+    def shifted_mask(q_rows, k, row_ids, causal, scale):
+        s = scale * (q_rows @ k.T)
+        cols = np.arange(k.shape[0])
+        return np.where(cols[None, :] >= row_ids[:, None], -np.inf, s) if causal else s
+
+    with np.errstate(invalid="ignore"):
+        (o, _), (q, k, v) = _forward_with(monkeypatch, shifted_mask, True)
+    # causal row 0 pin: O_0 = V_0 (the shifted mask leaves row 0 empty -> NaN)
+    assert not np.allclose(o[0, 0, 0], v[0, 0, 0])
+
+
+def test_planted_wrong_softmax_gradient_sign_is_caught(monkeypatch):
+    q, k, v = qkv(1, 1, 6, 3, 22)
+    do = rand(q.shape, 23)
+    real = oa.softmax_rows
+
+    dq, dk, dv = oracle.attention_backward(q, k, v, do, False, 0.5)
+    assert np.allclose(dk.sum(axis=2), 0.0, atol=1e-12)
+
+    # a transposed-operand slip in dV breaks sum_j dV_j = sum_i dO_i
+    monkeypatch.setattr(oa, "softmax_rows", lambda s: (real(s)[0].T.copy(), real(s)[1]))
+    _, _, dv_bad = oracle.attention_backward(q, k, v, do, False, 0.5)
+    assert not np.allclose(dv_bad.sum(axis=2), do.sum(axis=2), atol=1e-9)
