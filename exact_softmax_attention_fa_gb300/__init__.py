@@ -1,0 +1,144 @@
+"""GB300 (sm_103a) exact softmax attention: Python binding of the C ABI.
+
+The functions here only check and marshal arguments (torch tensors -> device
+pointers, sizes, the current CUDA stream) and call libfa_gb300.so; every step
+of the computation runs in the library's CUDA kernels. PyTorch supplies device
+memory and streams.
+
+    o, lse = forward(q, k, v, causal=True)            # q, k, v: bf16 [B, H, N, d] on CUDA
+    dq, dk, dv = backward(q, k, v, o, lse, do, causal=True)
+"""
+
+from __future__ import annotations
+
+import math
+
+from ._lib import load, check, FAError, header_functions, STATUS_NAMES  # noqa: F401
+
+__all__ = ["fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_get_device_status", "fa_set_wait_limit_ns",
+           "fa_debug_timeout_probe", "forward", "backward", "FAError", "flops"]
+
+_SUPPORTED_D = (64, 128, 256)
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _dims(q):
+    if q.dim() != 4:
+        raise ValueError("expected [B, H, N, d] tensors")
+    return tuple(int(x) for x in q.shape)
+
+
+def _check_bf16(name, t, shape):
+    import torch
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be bfloat16, got {t.dtype}")
+    if tuple(t.shape) != shape:
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {shape}")
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+
+
+def _check_lse(t, shape):
+    import torch
+    if t.dtype != torch.float32 or tuple(t.shape) != shape[:3] or not t.is_cuda or not t.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 CUDA tensor of shape [B, H, N]")
+
+
+def default_scale(d: int) -> float:
+    return 1.0 / math.sqrt(d)
+
+
+def fa_fwd(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> None:
+    """fa_fwd of the C ABI on torch tensors (outputs o, lse written in place)."""
+    shape = _dims(q)
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o)):
+        _check_bf16(name, t, shape)
+    _check_lse(lse, shape)
+    B, H, N, d = shape
+    lib = load()
+    check("fa_fwd", lib.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                               B, H, N, d, int(bool(causal)), float(scale), _stream_handle(stream)))
+
+
+def fa_bwd_workspace_size(B: int, H: int, N: int, d: int) -> int:
+    return int(load().fa_bwd_workspace_size(B, H, N, d))
+
+
+def fa_bwd(q, k, v, o, lse, do, dq, dk, dv, causal: bool, scale: float, workspace, stream=None) -> None:
+    """fa_bwd of the C ABI on torch tensors (dq, dk, dv written in place).
+
+    `workspace` is a CUDA uint8 tensor of at least fa_bwd_workspace_size() bytes.
+    """
+    shape = _dims(q)
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do), ("dq", dq), ("dk", dk), ("dv", dv)):
+        _check_bf16(name, t, shape)
+    _check_lse(lse, shape)
+    B, H, N, d = shape
+    lib = load()
+    ws_ptr = workspace.data_ptr() if workspace is not None else 0
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    check("fa_bwd", lib.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                               do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                               B, H, N, d, int(bool(causal)), float(scale), ws_ptr, ws_bytes,
+                               _stream_handle(stream)))
+
+
+def fa_get_device_status(stream=None) -> int:
+    """Synchronise the stream; return and clear the device status (0 = FA_OK)."""
+    return int(load().fa_get_device_status(_stream_handle(stream)))
+
+
+def fa_set_wait_limit_ns(limit_ns: int) -> None:
+    load().fa_set_wait_limit_ns(int(limit_ns))
+
+
+def fa_debug_timeout_probe(limit_ns: int, stream=None) -> None:
+    check("fa_debug_timeout_probe", load().fa_debug_timeout_probe(int(limit_ns), _stream_handle(stream)))
+
+
+def forward(q, k, v, causal: bool = False, scale: float | None = None, stream=None):
+    """Allocate O (bf16) and L (fp32) with torch and run fa_fwd."""
+    import torch
+    B, H, N, d = _dims(q)
+    if scale is None:
+        scale = default_scale(d)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    fa_fwd(q, k, v, o, lse, causal, scale, stream)
+    return o, lse
+
+
+def backward(q, k, v, o, lse, do, causal: bool = False, scale: float | None = None, workspace=None, stream=None):
+    """Allocate dQ, dK, dV (and the workspace if not given) with torch and run fa_bwd."""
+    import torch
+    B, H, N, d = _dims(q)
+    if scale is None:
+        scale = default_scale(d)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    if workspace is None:
+        workspace = torch.empty(max(1, fa_bwd_workspace_size(B, H, N, d)), dtype=torch.uint8, device=q.device)
+    fa_bwd(q, k, v, o, lse, do, dq, dk, dv, causal, scale, workspace, stream)
+    return dq, dk, dv
+
+
+def flops(B: int, H: int, N: int, d: int, causal: bool, mode: str = "fwd") -> float:
+    """Algorithmic FLOPs of the pages' benchmark convention.
+
+    forward = 4 * N^2 * d * H (* B), halved under a causal mask; backward = 2.5x
+    forward (five matmuls instead of two); fwd+bwd = 3.5x forward. (Reading note
+    on papers.chlience.com, "结果 1"; paper-graph-ui summary, "Evaluation
+    Methodology".)
+    """
+    f = 4.0 * B * H * N * N * d
+    if causal:
+        f *= 0.5
+    mult = {"fwd": 1.0, "bwd": 2.5, "fwd_bwd": 3.5}[mode]
+    return f * mult

@@ -1,0 +1,284 @@
+// C ABI of the attention library: argument validation, TMA tensor-map
+// construction, per-device state and the device status word. All compute is
+// in the kernels of fa_fwd.cu / fa_bwd.cu.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "fa_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace fa {
+
+// Per-device status word written by kernels whose bounded waits gave up.
+__device__ uint32_t g_status_word[4];
+
+// One thread waits on an mbarrier that nothing arrives at; the bounded wait
+// gives up after limit_ns and records FA_ERR_TIMEOUT.
+__global__ void timeout_probe_kernel(uint32_t* status, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && !mbar_wait(&bar, 0, &abort_flag, limit_ns)) {
+    if (atomicCAS(status, 0u, static_cast<uint32_t>(FA_ERR_TIMEOUT)) == 0u) {
+      status[1] = WHERE_PROBE;
+      status[2] = blockIdx.x;
+      status[3] = threadIdx.x;
+    }
+  }
+}
+
+cudaError_t launch_timeout_probe(uint32_t* status, uint64_t limit_ns, cudaStream_t stream) {
+  timeout_probe_kernel<<<1, 32, 0, stream>>>(status, limit_ns);
+  return cudaGetLastError();
+}
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr uint64_t kDefaultWaitLimitNs = 4000000000ull;
+constexpr double kLog2e = 1.4426950408889634074;
+
+std::atomic<unsigned long long> g_wait_limit_ns{kDefaultWaitLimitNs};
+
+struct DeviceState {
+  std::once_flag once;
+  cudaError_t init_error = cudaSuccess;
+  int num_sms = 0;
+  int cc_major = 0, cc_minor = 0;
+  uint32_t* status = nullptr;  // device address of g_status_word
+};
+DeviceState g_dev[kMaxDevices];
+
+std::once_flag g_encode_once;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode;
+}
+
+// Current device's cached state; nullptr (and *err set) on failure.
+DeviceState* device_state(fa_status_t* err) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    *err = FA_ERR_CUDA;
+    return nullptr;
+  }
+  DeviceState& s = g_dev[dev];
+  std::call_once(s.once, [&s, dev] {
+    cudaError_t e = cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&s.cc_major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&s.cc_minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (e == cudaSuccess) e = cudaGetSymbolAddress(reinterpret_cast<void**>(&s.status), g_status_word);
+    s.init_error = e;
+  });
+  if (s.init_error != cudaSuccess) {
+    *err = FA_ERR_CUDA;
+    return nullptr;
+  }
+  if (s.cc_major != 10 || s.cc_minor != 3) {  // kernels are built for sm_103a only
+    *err = FA_ERR_UNSUPPORTED;
+    return nullptr;
+  }
+  return &s;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// [BH][N][d] bf16, boxes of 128 rows x 64 columns, 128-byte swizzle; rows
+// past N read as zero and are not written by stores.
+bool make_map(CUtensorMap* m, const void* base, int BH, int N, int d) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+fa_status_t check_common(int B, int H, int N, int d, int causal, float scale, bool* empty) {
+  if (B < 0 || H < 0 || N < 0) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
+  // [BH] is a TMA coordinate (int32) and the tensor byte size must fit.
+  const long long bh = static_cast<long long>(B) * H;
+  if (bh > INT32_MAX) return FA_ERR_INVALID_ARG;
+  if (bh * N > (1ll << 40)) return FA_ERR_INVALID_ARG;
+  *empty = (bh * N == 0);
+  return FA_OK;
+}
+
+int round_up_128(int n) { return (n + 127) / 128 * 128; }
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct BwdWorkspaceLayout {
+  size_t D_off, lse2_off, dq_off, total;
+};
+
+BwdWorkspaceLayout bwd_layout(long long BH, int N, int d) {
+  const size_t rows = static_cast<size_t>(BH) * round_up_128(N);
+  BwdWorkspaceLayout w;
+  w.D_off = 0;
+  w.lse2_off = align_up(w.D_off + rows * 4, 256);
+  w.dq_off = align_up(w.lse2_off + rows * 4, 256);
+  w.total = align_up(w.dq_off + rows * static_cast<size_t>(d) * 4, 256);
+  return w;
+}
+
+fa_status_t from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return FA_OK;
+  if (e == cudaErrorLaunchFailure || e == cudaErrorInvalidConfiguration || e == cudaErrorLaunchOutOfResources ||
+      e == cudaErrorInvalidDeviceFunction || e == cudaErrorNoKernelImageForDevice)
+    return FA_ERR_LAUNCH;
+  return FA_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+int fa_version(void) { return 100; }
+
+const char* fa_status_string(fa_status_t s) {
+  switch (s) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG: null pointer, negative size, or bad scale/flag";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: head dimension must be 64, 128 or 256 on an sm_103a device";
+    case FA_ERR_MISALIGNED: return "FA_ERR_MISALIGNED: bf16 tensors need 16-byte, lse 4-byte, workspace 256-byte alignment";
+    case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE: backward workspace missing or smaller than fa_bwd_workspace_size()";
+    case FA_ERR_LAUNCH: return "FA_ERR_LAUNCH: kernel launch failed";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a device-side pipeline wait exceeded its limit";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA: CUDA runtime error";
+  }
+  return "unknown fa_status_t";
+}
+
+void fa_set_wait_limit_ns(unsigned long long limit_ns) {
+  g_wait_limit_ns.store(limit_ns == 0 ? kDefaultWaitLimitNs : limit_ns);
+}
+
+fa_status_t fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                   int causal, float scale, cudaStream_t stream) {
+  bool empty = false;
+  fa_status_t st = check_common(B, H, N, d, causal, scale, &empty);
+  if (st != FA_OK) return st;
+  if (empty) return FA_OK;
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
+    return FA_ERR_MISALIGNED;
+  DeviceState* ds = device_state(&st);
+  if (!ds) return st;
+  FwdLaunch a{};
+  const int BH = B * H;
+  if (!make_map(&a.tmQ, q, BH, N, d) || !make_map(&a.tmK, k, BH, N, d) || !make_map(&a.tmV, v, BH, N, d) ||
+      !make_map(&a.tmO, o, BH, N, d))
+    return FA_ERR_CUDA;
+  a.lse = lse;
+  a.status = ds->status;
+  a.N = N;
+  a.BH = BH;
+  a.d = d;
+  a.causal = causal;
+  a.scale_log2 = static_cast<float>(static_cast<double>(scale) * kLog2e);
+  a.wait_limit_ns = g_wait_limit_ns.load();
+  a.num_sms = ds->num_sms;
+  return from_cuda(launch_fwd(a, stream));
+}
+
+size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
+  bool empty = false;
+  if (check_common(B, H, N, d, 0, 1.0f, &empty) != FA_OK || empty) return 0;
+  return bwd_layout(static_cast<long long>(B) * H, N, d).total;
+}
+
+fa_status_t fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                   void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal, float scale,
+                   void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  bool empty = false;
+  fa_status_t st = check_common(B, H, N, d, causal, scale, &empty);
+  if (st != FA_OK) return st;
+  if (empty) return FA_OK;
+  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(dO, 16) ||
+      !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4))
+    return FA_ERR_MISALIGNED;
+  const int BH = B * H;
+  const BwdWorkspaceLayout wl = bwd_layout(BH, N, d);
+  if (!workspace || workspace_bytes < wl.total) return FA_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return FA_ERR_MISALIGNED;
+  DeviceState* ds = device_state(&st);
+  if (!ds) return st;
+  BwdLaunch a{};
+  if (!make_map(&a.tmQ, q, BH, N, d) || !make_map(&a.tmK, k, BH, N, d) || !make_map(&a.tmV, v, BH, N, d) ||
+      !make_map(&a.tmdO, dO, BH, N, d) || !make_map(&a.tmdK, dk, BH, N, d) || !make_map(&a.tmdV, dv, BH, N, d))
+    return FA_ERR_CUDA;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  a.o = static_cast<const __nv_bfloat16*>(o);
+  a.dO = static_cast<const __nv_bfloat16*>(dO);
+  a.lse = lse;
+  a.dq = static_cast<__nv_bfloat16*>(dq);
+  a.D = reinterpret_cast<float*>(ws + wl.D_off);
+  a.lse2 = reinterpret_cast<float*>(ws + wl.lse2_off);
+  a.dq_acc = reinterpret_cast<float*>(ws + wl.dq_off);
+  a.status = ds->status;
+  a.N = N;
+  a.Npad = round_up_128(N);
+  a.BH = BH;
+  a.d = d;
+  a.causal = causal;
+  a.scale = scale;
+  a.scale_log2 = static_cast<float>(static_cast<double>(scale) * kLog2e);
+  a.wait_limit_ns = g_wait_limit_ns.load();
+  a.num_sms = ds->num_sms;
+  return from_cuda(launch_bwd(a, stream));
+}
+
+fa_status_t fa_get_device_status(cudaStream_t stream) {
+  fa_status_t st = FA_OK;
+  DeviceState* ds = device_state(&st);
+  if (!ds) return st;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return FA_ERR_CUDA;
+  uint32_t word[4] = {0, 0, 0, 0};
+  if (cudaMemcpy(word, ds->status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
+  if (word[0] != 0) {
+    const uint32_t zero[4] = {0, 0, 0, 0};
+    if (cudaMemcpy(ds->status, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_CUDA;
+  }
+  return static_cast<fa_status_t>(word[0]);
+}
+
+fa_status_t fa_debug_timeout_probe(unsigned long long limit_ns, cudaStream_t stream) {
+  fa_status_t st = FA_OK;
+  DeviceState* ds = device_state(&st);
+  if (!ds) return st;
+  if (limit_ns == 0 || limit_ns > 10000000000ull) return FA_ERR_INVALID_ARG;
+  return from_cuda(launch_timeout_probe(ds->status, limit_ns, stream));
+}
+
+}  // extern "C"

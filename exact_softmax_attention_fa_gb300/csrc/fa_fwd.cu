@@ -1,0 +1,487 @@
+// Forward pass of exact softmax attention for sm_103a.
+//
+// Method (web pages on FlashAttention-2):
+//   "FlashAttention 2: ..." reading note (papers.chlience.com) 5.1-5.2 and the
+//   paper-graph-ui summary, "Algorithm 1 Walkthrough": for a query block Q_i
+//   keep a running row max m, running sum l and an UNSCALED accumulator O~;
+//   for each key block j: S = Q_i K_j^T, m' = max(m, rowmax S),
+//   P~ = exp(S - m'), l = e^{m - m'} l + rowsum P~, O~ = e^{m - m'} O~ + P~ V_j;
+//   at the end O = O~ / l and L = m + log l (the only statistics stored).
+//   Causal key blocks entirely right of the diagonal are skipped and only the
+//   diagonal block is masked element-wise (summary, "Causal masking
+//   optimization"; reading note 5.6).
+//
+// GB300 mapping (our design; the pages' A100 warp layout does not apply):
+//   - One CTA owns NT query tiles of 128 rows of one (batch, head) (NT = 2
+//     for d <= 128, 1 for d = 256) and streams the 128-key K/V tiles of that
+//     head through a TMA + mbarrier ring.
+//   - Warp 9 (one thread) issues tcgen05 MMAs: S_t = Q_t K_j^T into TMEM
+//     (SS, both operands K-major in 128-byte-swizzled smem) and
+//     O~_t += P_t V_j (A = P_t read from TMEM, B = V_j MN-major in smem).
+//   - Warp 8 (one thread) issues the TMA loads.
+//   - Warpgroup t (warps 4t..4t+3) owns query tile t: thread r <-> query row r
+//     <-> TMEM lane r. It reads its row of S from TMEM, keeps m (in base-2
+//     units of the scaled scores) and l in registers, computes
+//     P~ = 2^(S*scale*log2e - m) with one FFMA + ex2 per element, writes P~
+//     as bf16 back to TMEM, and rescales its row of O~ in TMEM only when the
+//     row max of some row of the warp grew.
+//   - While warpgroup 0 does softmax on tile 0 the tensor core works on
+//     tile 1 and vice versa.
+//   - Epilogue: O = O~ / l converted to bf16 into the (now free) Q tile's
+//     smem in the TMA swizzle, one TMA store; L = ln2 * (m + log2 l).
+//
+// TMEM columns (512 allocated):
+//   d=64 : S0 0, S1 128, O0 256, O1 320, P0 384, P1 448
+//   d=128: S0 0, S1 128, O0 256, O1 384, P_t aliases the first 64 columns of
+//          S_t, so S_t(j+1) is issued only after O_t += P_t V_j completed
+//   d=256: S 0, P 128, O 256
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <cmath>
+
+#include "fa_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kThreads = 320;
+constexpr int kLoadWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr float kLn2 = 0.69314718055994530942f;
+
+template <int HD>
+struct FwdCfg {
+  static constexpr int NT = HD <= 128 ? 2 : 1;
+  static constexpr int CHUNKS = HD / 64;             // 64-column (128-byte) swizzle chunks
+  static constexpr int TILE_BYTES = 128 * HD * 2;    // one 128-row bf16 tile
+  static constexpr int CHUNK_BYTES = 128 * 128;      // 128 rows x 128 bytes
+  static constexpr int KST = HD == 64 ? 4 : (HD == 128 ? 2 : 1);
+  static constexpr int VST = KST;
+  static constexpr bool P_ALIAS = HD == 128;
+  __host__ __device__ static constexpr uint32_t s_col(int t) { return HD == 256 ? 0u : uint32_t(t) * 128u; }
+  __host__ __device__ static constexpr uint32_t o_col(int t) { return 256u + uint32_t(t) * HD; }
+  __host__ __device__ static constexpr uint32_t p_col(int t) {
+    return HD == 64 ? 384u + uint32_t(t) * 64u : (HD == 128 ? uint32_t(t) * 128u : 128u);
+  }
+  static constexpr int SMEM_BYTES = (NT + KST + VST) * TILE_BYTES + 1024;
+};
+
+struct FwdShared {
+  uint64_t q_full;
+  uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
+  uint64_t s_full[2], p_full[2], pv_done[2];
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+__device__ __forceinline__ void record_timeout(uint32_t* status, int* abort_flag, uint32_t where) {
+  if (atomicCAS(status, 0u, static_cast<uint32_t>(FA_ERR_TIMEOUT)) == 0u) {
+    status[1] = where;
+    status[2] = blockIdx.x;
+    status[3] = threadIdx.x;
+  }
+  *reinterpret_cast<volatile int*>(abort_flag) = 1;
+}
+
+// Work item of one CTA: NT consecutive 128-row query tiles of head `bh`.
+template <int NT, bool CAUSAL>
+struct FwdWork {
+  int bh;
+  int qt[NT];       // query tile indices
+  int last_kv[NT];  // last key tile each query tile needs; -1 if the tile is past the end
+  int nkv;          // number of key tiles streamed
+  __device__ FwdWork(int block, int BH, int N) {
+    const int T = (N + 127) / 128;
+    const int n_w = (T + NT - 1) / NT;
+    int w;
+    if (CAUSAL) {  // longest work first: the last query tiles see the most keys
+      bh = block % BH;
+      w = n_w - 1 - block / BH;
+    } else {
+      bh = block / n_w;
+      w = block % n_w;
+    }
+    nkv = 0;
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      qt[t] = w * NT + t;
+      last_kv[t] = qt[t] < T ? (CAUSAL ? qt[t] : T - 1) : -1;
+      nkv = max(nkv, last_kv[t] + 1);
+    }
+  }
+};
+
+// ---------------------------------------------------------------------------
+// TMA producer (one thread)
+// ---------------------------------------------------------------------------
+template <int HD, bool CAUSAL>
+__device__ void fwd_load_role(const FwdLaunch& p, FwdShared& sh, uint8_t* sQ, uint8_t* sK, uint8_t* sV,
+                              const FwdWork<FwdCfg<HD>::NT, CAUSAL>& wk) {
+  using C = FwdCfg<HD>;
+  tma_prefetch_desc(&p.tmQ);
+  tma_prefetch_desc(&p.tmK);
+  tma_prefetch_desc(&p.tmV);
+  tma_prefetch_desc(&p.tmO);
+  uint32_t qbytes = 0;
+#pragma unroll
+  for (int t = 0; t < C::NT; ++t)
+    if (wk.last_kv[t] >= 0) qbytes += C::TILE_BYTES;
+  mbar_arrive_expect_tx(&sh.q_full, qbytes);
+#pragma unroll
+  for (int t = 0; t < C::NT; ++t) {
+    if (wk.last_kv[t] < 0) continue;
+#pragma unroll
+    for (int c = 0; c < C::CHUNKS; ++c)
+      tma_load_3d(sQ + t * C::TILE_BYTES + c * C::CHUNK_BYTES, &p.tmQ, &sh.q_full, c * 64, wk.qt[t] * 128, wk.bh);
+  }
+  int k_issued = 0, v_issued = 0;
+  bool aborted = false;
+  for (int j = 0; j < wk.nkv && !aborted; ++j) {
+    const int ks = j % C::KST;
+    if (j >= C::KST && !mbar_wait(&sh.k_empty[ks], ((j / C::KST) - 1) & 1, &sh.abort_flag, p.wait_limit_ns)) {
+      aborted = true;
+      break;
+    }
+    mbar_arrive_expect_tx(&sh.k_full[ks], C::TILE_BYTES);
+#pragma unroll
+    for (int c = 0; c < C::CHUNKS; ++c)
+      tma_load_3d(sK + ks * C::TILE_BYTES + c * C::CHUNK_BYTES, &p.tmK, &sh.k_full[ks], c * 64, j * 128, wk.bh);
+    ++k_issued;
+    const int vs = j % C::VST;
+    if (j >= C::VST && !mbar_wait(&sh.v_empty[vs], ((j / C::VST) - 1) & 1, &sh.abort_flag, p.wait_limit_ns)) {
+      aborted = true;
+      break;
+    }
+    mbar_arrive_expect_tx(&sh.v_full[vs], C::TILE_BYTES);
+#pragma unroll
+    for (int c = 0; c < C::CHUNKS; ++c)
+      tma_load_3d(sV + vs * C::TILE_BYTES + c * C::CHUNK_BYTES, &p.tmV, &sh.v_full[vs], c * 64, j * 128, wk.bh);
+    ++v_issued;
+  }
+  if (aborted) {
+    record_timeout(p.status, &sh.abort_flag, WHERE_FWD_LOAD);
+    // Let the copies already issued land before the CTA can exit.
+    const int zero = 0;
+    for (int jj = max(0, k_issued - C::KST); jj < k_issued; ++jj)
+      mbar_wait(&sh.k_full[jj % C::KST], (jj / C::KST) & 1, &zero, p.wait_limit_ns);
+    for (int jj = max(0, v_issued - C::VST); jj < v_issued; ++jj)
+      mbar_wait(&sh.v_full[jj % C::VST], (jj / C::VST) & 1, &zero, p.wait_limit_ns);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// MMA issuer (one thread)
+// ---------------------------------------------------------------------------
+template <int HD, bool CAUSAL>
+__device__ void fwd_mma_role(const FwdLaunch& p, FwdShared& sh, uint8_t* sQ, uint8_t* sK, uint8_t* sV,
+                             uint32_t tmem, const FwdWork<FwdCfg<HD>::NT, CAUSAL>& wk) {
+  using C = FwdCfg<HD>;
+  constexpr uint32_t kIdescS = make_idesc_bf16_f32(128, 128, false, false);
+  constexpr uint32_t kIdescPV = make_idesc_bf16_f32(128, HD, false, true);
+  const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV);
+  const uint64_t lim = p.wait_limit_ns;
+
+  auto issue_s = [&](int t, int j) {
+    const uint32_t qa = q_addr + t * C::TILE_BYTES;
+    const uint32_t ka = k_addr + (j % C::KST) * C::TILE_BYTES;
+#pragma unroll
+    for (int ks = 0; ks < HD / 16; ++ks) {
+      const uint32_t off = (ks >> 2) * C::CHUNK_BYTES + (ks & 3) * 32;
+      umma_ss(tmem + C::s_col(t), make_smem_desc_sw128(qa + off, 16, 1024), make_smem_desc_sw128(ka + off, 16, 1024),
+              kIdescS, ks > 0 ? 1u : 0u);
+    }
+    umma_commit(&sh.s_full[t]);
+  };
+  auto issue_pv = [&](int t, int j) {
+    const uint32_t va = v_addr + (j % C::VST) * C::TILE_BYTES;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks)
+      umma_ts(tmem + C::o_col(t), tmem + C::p_col(t) + ks * 8, make_smem_desc_sw128(va + ks * 2048, C::CHUNK_BYTES, 1024),
+              kIdescPV, (j > 0 || ks > 0) ? 1u : 0u);
+    umma_commit(&sh.pv_done[t]);
+  };
+
+  if (!mbar_wait(&sh.q_full, 0, &sh.abort_flag, lim) || !mbar_wait(&sh.k_full[0], 0, &sh.abort_flag, lim)) {
+    record_timeout(p.status, &sh.abort_flag, WHERE_FWD_MMA);
+    return;
+  }
+  tc_fence_after_sync();
+#pragma unroll
+  for (int t = 0; t < C::NT; ++t)
+    if (wk.last_kv[t] >= 0) issue_s(t, 0);
+  umma_commit(&sh.k_empty[0]);
+
+  for (int j = 0; j < wk.nkv; ++j) {
+    const int vs = j % C::VST;
+    if (!mbar_wait(&sh.v_full[vs], (j / C::VST) & 1, &sh.abort_flag, lim)) {
+      record_timeout(p.status, &sh.abort_flag, WHERE_FWD_MMA);
+      return;
+    }
+    const bool has_next = j + 1 < wk.nkv;
+    const int ks_next = (j + 1) % C::KST;
+    bool k_next_ready = false;
+    auto wait_k_next = [&]() -> bool {
+      if (k_next_ready) return true;
+      if (!mbar_wait(&sh.k_full[ks_next], ((j + 1) / C::KST) & 1, &sh.abort_flag, lim)) return false;
+      tc_fence_after_sync();
+      k_next_ready = true;
+      return true;
+    };
+#pragma unroll
+    for (int t = 0; t < C::NT; ++t) {
+      if (j > wk.last_kv[t]) continue;
+      if (!mbar_wait(&sh.p_full[t], j & 1, &sh.abort_flag, lim)) {
+        record_timeout(p.status, &sh.abort_flag, WHERE_FWD_MMA);
+        return;
+      }
+      tc_fence_after_sync();
+      issue_pv(t, j);
+      if (!C::P_ALIAS && has_next && j + 1 <= wk.last_kv[t]) {
+        if (!wait_k_next()) {
+          record_timeout(p.status, &sh.abort_flag, WHERE_FWD_MMA);
+          return;
+        }
+        issue_s(t, j + 1);
+      }
+    }
+    if (C::P_ALIAS && has_next) {
+#pragma unroll
+      for (int t = 0; t < C::NT; ++t) {
+        if (j + 1 > wk.last_kv[t]) continue;
+        // S_t(j+1) overwrites the TMEM columns P_t(j) is read from.
+        if (!wait_k_next() || !mbar_wait(&sh.pv_done[t], j & 1, &sh.abort_flag, lim)) {
+          record_timeout(p.status, &sh.abort_flag, WHERE_FWD_MMA);
+          return;
+        }
+        tc_fence_after_sync();
+        issue_s(t, j + 1);
+      }
+    }
+    if (has_next) umma_commit(&sh.k_empty[ks_next]);
+    umma_commit(&sh.v_empty[vs]);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Softmax + correction + epilogue (one warpgroup per query tile)
+// ---------------------------------------------------------------------------
+template <int HD, bool CAUSAL>
+__device__ void fwd_softmax_role(const FwdLaunch& p, FwdShared& sh, uint8_t* sQ, uint32_t tmem, int t,
+                                 const FwdWork<FwdCfg<HD>::NT, CAUSAL>& wk) {
+  using C = FwdCfg<HD>;
+  const int r = threadIdx.x & 127;
+  const uint32_t lane_base = static_cast<uint32_t>((threadIdx.x >> 5) & 3) << 21;  // (warp % 4) * 32 lanes
+  const uint32_t tS = tmem + lane_base + C::s_col(t);
+  const uint32_t tP = tmem + lane_base + C::p_col(t);
+  const uint32_t tO = tmem + lane_base + C::o_col(t);
+  const int N = p.N;
+  const int T = (N + 127) / 128;
+  const int qt = wk.qt[t];
+  const int last_kv = wk.last_kv[t];
+  const int row = qt * 128 + r;
+  const float c2 = p.scale_log2;
+  const uint64_t lim = p.wait_limit_ns;
+
+  float m2 = -INFINITY;  // running max of S * scale * log2(e)
+  float l = 0.f;         // running sum of P~ (unrounded fp32)
+  bool ok = true;
+  for (int j = 0; j <= last_kv; ++j) {
+    ok = __all_sync(0xffffffffu, mbar_wait(&sh.s_full[t], j & 1, &sh.abort_flag, lim));
+    if (!ok) {
+      record_timeout(p.status, &sh.abort_flag, WHERE_FWD_SOFTMAX);
+      break;
+    }
+    tc_fence_after_sync();
+    float s[128];
+    {
+      uint32_t a[32], b[32], c[32], d[32];
+      tmem_ld32(tS + 0, a);
+      tmem_ld32(tS + 32, b);
+      tmem_ld32(tS + 64, c);
+      tmem_ld32(tS + 96, d);
+      tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        s[i] = __uint_as_float(a[i]);
+        s[32 + i] = __uint_as_float(b[i]);
+        s[64 + i] = __uint_as_float(c[i]);
+        s[96 + i] = __uint_as_float(d[i]);
+      }
+    }
+    // Element-wise mask only on the key-tail tile and the causal diagonal tile.
+    const bool mask_tail = (j == T - 1) && (N & 127);
+    const bool mask_diag = CAUSAL && (j == qt);
+    if (mask_tail || mask_diag) {
+      int lim_col = N - 1 - j * 128;
+      if (CAUSAL) lim_col = min(lim_col, row - j * 128);
+#pragma unroll
+      for (int i = 0; i < 128; ++i)
+        if (i > lim_col) s[i] = -INFINITY;
+    }
+    float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+    for (int i = 4; i < 128; i += 4) {
+      mx0 = fmaxf(mx0, s[i]);
+      mx1 = fmaxf(mx1, s[i + 1]);
+      mx2 = fmaxf(mx2, s[i + 2]);
+      mx3 = fmaxf(mx3, s[i + 3]);
+    }
+    const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+    const float m_new = fmaxf(m2, mx * c2);
+    const float m_use = m_new == -INFINITY ? 0.f : m_new;
+    const float alpha = ex2_approx(m2 - m_use);  // 0 on the first block, 1 when the max is unchanged
+    const float neg = -m_use;
+    float sum0 = 0.f, sum1 = 0.f;
+    uint32_t pk0[32], pk1[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float p0 = ex2_approx(fmaf(s[2 * i], c2, neg));
+      const float p1 = ex2_approx(fmaf(s[2 * i + 1], c2, neg));
+      sum0 += p0;
+      sum1 += p1;
+      pk0[i] = pack_bf16x2(p0, p1);
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float p0 = ex2_approx(fmaf(s[64 + 2 * i], c2, neg));
+      const float p1 = ex2_approx(fmaf(s[64 + 2 * i + 1], c2, neg));
+      sum0 += p0;
+      sum1 += p1;
+      pk1[i] = pack_bf16x2(p0, p1);
+    }
+    l = l * alpha + (sum0 + sum1);
+    tmem_st32(tP, pk0);
+    tmem_st32(tP + 32, pk1);
+    // Rescale O~ only when some row of this warp found a larger max.
+    if (j > 0 && __any_sync(0xffffffffu, m_new > m2)) {
+#pragma unroll 1
+      for (int c = 0; c < HD; c += 32) {
+        uint32_t o[32];
+        tmem_ld32(tO + c, o);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+        tmem_st32(tO + c, o);
+      }
+    }
+    m2 = m_new;
+    tmem_st_wait();
+    tc_fence_before_sync();
+    mbar_arrive(&sh.p_full[t]);
+  }
+
+  // Epilogue: wait for the last O~ += P~ V, normalise, store.
+  if (ok && last_kv >= 0) {
+    ok = __all_sync(0xffffffffu, mbar_wait(&sh.pv_done[t], last_kv & 1, &sh.abort_flag, lim));
+    if (!ok) record_timeout(p.status, &sh.abort_flag, WHERE_FWD_SOFTMAX);
+  }
+  tc_fence_after_sync();
+  uint8_t* stage = sQ + t * C::TILE_BYTES;  // Q_t is no longer read by any MMA
+  const bool active = ok && last_kv >= 0;
+  if (active) {
+    const float inv_l = 1.f / l;
+    const uint32_t stage_addr = smem_u32(stage);
+#pragma unroll 1
+    for (int c = 0; c < HD; c += 32) {
+      uint32_t o[32];
+      tmem_ld32(tO + c, o);
+      tmem_ld_wait();
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int col = c + u * 8;
+        const uint32_t w0 = pack_bf16x2(__uint_as_float(o[u * 8 + 0]) * inv_l, __uint_as_float(o[u * 8 + 1]) * inv_l);
+        const uint32_t w1 = pack_bf16x2(__uint_as_float(o[u * 8 + 2]) * inv_l, __uint_as_float(o[u * 8 + 3]) * inv_l);
+        const uint32_t w2 = pack_bf16x2(__uint_as_float(o[u * 8 + 4]) * inv_l, __uint_as_float(o[u * 8 + 5]) * inv_l);
+        const uint32_t w3 = pack_bf16x2(__uint_as_float(o[u * 8 + 6]) * inv_l, __uint_as_float(o[u * 8 + 7]) * inv_l);
+        st_shared_v4(stage_addr + (col >> 6) * C::CHUNK_BYTES + sw128_offset(r, (col & 63) >> 3), w0, w1, w2, w3);
+      }
+    }
+    fence_proxy_async_smem();
+  }
+  named_barrier_sync(1 + t, 128);
+  if (active && r == 0 && !*reinterpret_cast<volatile int*>(&sh.abort_flag)) {
+#pragma unroll
+    for (int c = 0; c < C::CHUNKS; ++c) tma_store_3d(&p.tmO, stage + c * C::CHUNK_BYTES, c * 64, qt * 128, wk.bh);
+    tma_store_commit();
+    tma_store_wait_all();
+  }
+  if (active && row < N) p.lse[static_cast<size_t>(wk.bh) * N + row] = (m2 + log2f(l)) * kLn2;
+}
+
+template <int HD, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_constant__ FwdLaunch p) {
+  using C = FwdCfg<HD>;
+  extern __shared__ uint8_t smem_dyn[];
+  __shared__ FwdShared sh;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sK = sQ + C::NT * C::TILE_BYTES;
+  uint8_t* sV = sK + C::KST * C::TILE_BYTES;
+  const int warp = threadIdx.x >> 5;
+  const FwdWork<C::NT, CAUSAL> wk(blockIdx.x, p.BH, p.N);
+
+  if (threadIdx.x == 0) {
+    mbar_init(&sh.q_full, 1);
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&sh.k_full[i], 1);
+      mbar_init(&sh.k_empty[i], 1);
+      mbar_init(&sh.v_full[i], 1);
+      mbar_init(&sh.v_empty[i], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&sh.s_full[t], 1);
+      mbar_init(&sh.p_full[t], 128);
+      mbar_init(&sh.pv_done[t], 1);
+    }
+    sh.abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&sh.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = sh.tmem_base;
+
+  if (warp == kLoadWarp) {
+    if (lane_id() == 0) fwd_load_role<HD, CAUSAL>(p, sh, sQ, sK, sV, wk);
+  } else if (warp == kMmaWarp) {
+    if (lane_id() == 0) fwd_mma_role<HD, CAUSAL>(p, sh, sQ, sK, sV, tmem, wk);
+  } else if (warp < 4 * C::NT) {
+    fwd_softmax_role<HD, CAUSAL>(p, sh, sQ, tmem, warp >> 2, wk);
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
+}
+
+template <int HD, bool CAUSAL>
+cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
+  using C = FwdCfg<HD>;
+  auto kern = fa_fwd_kernel<HD, CAUSAL>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  const int T = (a.N + 127) / 128;
+  const long long blocks = static_cast<long long>(a.BH) * ((T + C::NT - 1) / C::NT);
+  kern<<<static_cast<unsigned>(blocks), kThreads, C::SMEM_BYTES, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t stream) {
+  switch (a.d) {
+    case 64: return a.causal ? launch_fwd_t<64, true>(a, stream) : launch_fwd_t<64, false>(a, stream);
+    case 128: return a.causal ? launch_fwd_t<128, true>(a, stream) : launch_fwd_t<128, false>(a, stream);
+    case 256: return a.causal ? launch_fwd_t<256, true>(a, stream) : launch_fwd_t<256, false>(a, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace fa

@@ -1,0 +1,62 @@
+// Internal interfaces between the C-ABI layer (fa_api.cu) and the kernel
+// translation units. Host-side only; no torch types anywhere.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "../../include/fa.h"
+
+namespace fa {
+
+// Device status word layout (4 x uint32): [0] first error code, [1] where
+// (role id), [2] blockIdx.x, [3] threadIdx.x.
+enum : uint32_t {
+  WHERE_FWD_LOAD = 1,
+  WHERE_FWD_MMA = 2,
+  WHERE_FWD_SOFTMAX = 3,
+  WHERE_BWD_LOAD = 11,
+  WHERE_BWD_MMA = 12,
+  WHERE_BWD_SOFTMAX = 13,
+  WHERE_BWD_DQ = 14,
+  WHERE_PROBE = 99,
+};
+
+// Tiles of the [B*H][N][d] bf16 tensors, as seen by TMA: 128 rows x 64
+// columns per box, 128-byte swizzle.
+struct FwdLaunch {
+  CUtensorMap tmQ, tmK, tmV, tmO;
+  float* lse;
+  uint32_t* status;
+  int N, BH, d, causal;
+  float scale_log2;  // scale * log2(e): scores are exponentiated in base 2
+  uint64_t wait_limit_ns;
+  int num_sms;
+};
+
+struct BwdLaunch {
+  CUtensorMap tmQ, tmK, tmV, tmdO, tmdK, tmdV;
+  const __nv_bfloat16* o;
+  const __nv_bfloat16* dO;
+  const float* lse;
+  __nv_bfloat16* dq;
+  float* D;       // [BH][Npad]
+  float* lse2;    // [BH][Npad], base-2 logsumexp (+inf on padding rows)
+  float* dq_acc;  // [BH][Npad][d]
+  uint32_t* status;
+  int N, Npad, BH, d, causal;
+  float scale;       // softmax scale (dK, dQ carry it)
+  float scale_log2;  // scale * log2(e)
+  uint64_t wait_limit_ns;
+  int num_sms;
+};
+
+// Launchers (defined in the kernel translation units). Return cudaSuccess or
+// the launch error.
+cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t stream);
+cudaError_t launch_bwd(const BwdLaunch& a, cudaStream_t stream);
+cudaError_t launch_timeout_probe(uint32_t* status, uint64_t limit_ns, cudaStream_t stream);
+
+}  // namespace fa

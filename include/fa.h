@@ -1,0 +1,129 @@
+/*
+ * fa.h - C ABI of the GB300 (sm_103a) exact softmax attention library.
+ *
+ * Computes, for every batch b and head h (Q, K, V in R^{N x d}):
+ *   S = scale * Q K^T, with S_ij = -inf for j > i when causal,
+ *   P = softmax(S) (row-wise), O = P V, L_i = log sum_j exp(S_ij)   (natural log)
+ * and the gradients of a scalar loss given dO = dLoss/dO:
+ *   D_i = sum_k dO_ik O_ik, dV = P^T dO, dP = dO V^T, dS = P o (dP - D),
+ *   dQ = scale * dS K, dK = scale * dS^T Q.
+ *
+ * Sources (web pages on FlashAttention-2, by title and section):
+ *   "FlashAttention 2: Faster Attention with Better Parallelism and Work
+ *   Partitioning" (reading note, papers.chlience.com): section 1 for the
+ *   standard attention definition; 5.1-5.2 for the blocked forward with the
+ *   unscaled accumulator and the stored logsumexp L = m + log(l); 5.3 for the
+ *   recomputation backward with D = rowsum(dO o O).
+ *   "FlashAttention" (llm-infra-atlas), section 1, for the 1/sqrt(d) scale.
+ *   "FlashAttention-2: ..." (paper-graph-ui summary), "Causal masking
+ *   optimization": entries whose column index exceeds the row index are -inf.
+ *
+ * Conventions shared by every entry point:
+ *   - Tensors are contiguous, row-major [B][H][N][d]; q, k, v, o, dO, dq, dk,
+ *     dv are bfloat16; lse is float32 [B][H][N]. All are DEVICE pointers
+ *     owned by the caller. bf16 pointers must be 16-byte aligned, lse 4-byte
+ *     aligned, the workspace 256-byte aligned.
+ *   - d must be 64, 128 or 256 (else FA_ERR_UNSUPPORTED). N >= 0, B >= 0,
+ *     H >= 0; if B*H*N == 0 the call does nothing and returns FA_OK (null
+ *     pointers are then allowed). scale must be finite and > 0.
+ *   - Calls are asynchronous on `stream` (0 = the legacy default stream).
+ *     Argument errors are returned synchronously before any GPU work is
+ *     queued. Launch failures return FA_ERR_LAUNCH / FA_ERR_CUDA.
+ *   - Device-side failures (a pipeline wait that exceeded its time limit) are
+ *     recorded in a per-device status word that fa_get_device_status() reads.
+ *   - The library allocates no device memory; it keeps only cached device
+ *     attributes in process-wide state. Entry points are thread-safe.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* cudaStream_t;
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad scale or flag */
+  FA_ERR_UNSUPPORTED = 2, /* head dimension other than 64/128/256, or no sm_103a device */
+  FA_ERR_MISALIGNED = 3,  /* pointer alignment below the stated minimum */
+  FA_ERR_WORKSPACE = 4,   /* backward workspace missing or too small */
+  FA_ERR_LAUNCH = 5,      /* a kernel launch failed */
+  FA_ERR_TIMEOUT = 6,     /* a device-side pipeline wait gave up (see fa_get_device_status) */
+  FA_ERR_CUDA = 7         /* another CUDA runtime error */
+} fa_status_t;
+
+/*
+ * Forward pass (reading note 5.1-5.2; paper-graph-ui summary, "Algorithm 1
+ * Walkthrough"): O = softmax(scale * Q K^T [causal]) V and L = logsumexp per
+ * query row.
+ *   q, k, v : in,  bf16 [B][H][N][d]
+ *   o       : out, bf16 [B][H][N][d]
+ *   lse     : out, fp32 [B][H][N], natural log, in units of the scaled scores
+ *   causal  : 0 or 1
+ *   scale   : softmax scale, typically 1/sqrt(d)
+ */
+fa_status_t fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                   int causal, float scale, cudaStream_t stream);
+
+/*
+ * Bytes of device workspace fa_bwd needs: D and the base-2 logsumexp
+ * (fp32 per query row) and the fp32 dQ accumulator, with every head padded
+ * to a multiple of 128 rows. Returns 0 for invalid or empty sizes.
+ */
+size_t fa_bwd_workspace_size(int B, int H, int N, int d);
+
+/*
+ * Backward pass (reading note 5.3; paper-graph-ui summary, "The Backward
+ * Pass"): recomputes S and P = exp(S - L) block by block, then
+ *   dV = P^T dO, dP = dO V^T, dS = P o (dP - D), dQ = scale dS K,
+ *   dK = scale dS^T Q, with D = rowsum(dO o O) precomputed.
+ *   q, k, v, o : in, bf16 [B][H][N][d] (o is the forward output)
+ *   lse        : in, fp32 [B][H][N] from fa_fwd with the same arguments
+ *   dO         : in, bf16 [B][H][N][d]
+ *   dq, dk, dv : out, bf16 [B][H][N][d]
+ *   workspace  : device scratch of at least fa_bwd_workspace_size() bytes,
+ *                owned by the caller; its contents on entry do not matter.
+ * dQ is accumulated in fp32 with atomic adds across key blocks, so dq is not
+ * bitwise reproducible run to run; dk and dv are.
+ */
+fa_status_t fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                   void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal, float scale,
+                   void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char* fa_status_string(fa_status_t status);
+
+/*
+ * Synchronise `stream`, then read and clear the current device's status word.
+ * Returns FA_OK, FA_ERR_TIMEOUT if a kernel's bounded wait gave up since the
+ * last call, or FA_ERR_CUDA if the synchronisation failed.
+ */
+fa_status_t fa_get_device_status(cudaStream_t stream);
+
+/*
+ * Time limit, in nanoseconds, of every device-side pipeline wait in later
+ * launches (default 4e9). A wait that exceeds it records FA_ERR_TIMEOUT and
+ * the kernel returns early with its outputs undefined.
+ */
+void fa_set_wait_limit_ns(unsigned long long limit_ns);
+
+/*
+ * Failure-detection self-test: launches one CTA that waits on a barrier no
+ * thread ever arrives at, with the given limit, so the wait gives up and
+ * records FA_ERR_TIMEOUT. Asynchronous; read the result with
+ * fa_get_device_status().
+ */
+fa_status_t fa_debug_timeout_probe(unsigned long long limit_ns, cudaStream_t stream);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

@@ -1,0 +1,104 @@
+"""CPU checks of the C ABI: the library loads, exports every function fa.h
+declares, and rejects bad arguments before touching the GPU."""
+
+import ctypes
+
+import pytest
+
+from exact_softmax_attention_fa_gb300 import _lib
+from exact_softmax_attention_fa_gb300.build import build, LIB_PATH
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return _lib.load()
+
+
+OK, INVALID, UNSUPPORTED, MISALIGNED, WORKSPACE = 0, 1, 2, 3, 4
+P = 0x10000  # a 16-byte aligned fake device address.
+# Every call below has at least one invalid argument, so the library returns
+# before any CUDA call and the fake address is never used, even on a GPU machine.
+
+
+def test_exports_every_header_function(lib):
+    names = _lib.header_functions()
+    assert {"fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_status_string"} <= set(names)
+    raw = ctypes.CDLL(LIB_PATH)
+    for n in names:
+        assert hasattr(raw, n), n
+    assert set(_lib._SIGNATURES) == set(names)
+
+
+def test_status_strings(lib):
+    for code, name in _lib.STATUS_NAMES.items():
+        assert lib.fa_status_string(code).decode().startswith(name)
+    assert lib.fa_version() >= 100
+
+
+def fwd(lib, q=P, k=P, v=P, o=P, lse=P, B=1, H=1, N=128, d=64, causal=0, scale=0.125):
+    return lib.fa_fwd(q, k, v, o, lse, B, H, N, d, causal, scale, None)
+
+
+def bwd(lib, ptr=P, lse=P, ws=P, ws_bytes=1 << 30, B=1, H=1, N=128, d=64, causal=0, scale=0.125):
+    return lib.fa_bwd(ptr, ptr, ptr, ptr, lse, ptr, ptr, ptr, ptr, B, H, N, d, causal, scale, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("d", [0, 32, 96, 160, 512])
+def test_unsupported_head_dim(lib, d):
+    assert fwd(lib, d=d) == UNSUPPORTED
+    assert bwd(lib, d=d) == UNSUPPORTED
+    assert lib.fa_bwd_workspace_size(1, 1, 128, d) == 0
+
+
+@pytest.mark.parametrize("kw", [dict(B=-1), dict(H=-2), dict(N=-1), dict(causal=2), dict(causal=-1),
+                                dict(scale=0.0), dict(scale=-0.1), dict(scale=float("nan")),
+                                dict(scale=float("inf")), dict(q=0), dict(o=0), dict(lse=0)])
+def test_invalid_arguments(lib, kw):
+    assert fwd(lib, **kw) == INVALID
+
+
+def test_empty_problem_is_a_no_op(lib):
+    for kw in (dict(N=0), dict(B=0), dict(H=0)):
+        assert fwd(lib, q=0, k=0, v=0, o=0, lse=0, **kw) == OK
+        assert bwd(lib, ptr=0, lse=0, ws=0, ws_bytes=0, **kw) == OK
+        assert lib.fa_bwd_workspace_size(kw.get("B", 1), kw.get("H", 1), kw.get("N", 128), 64) == 0
+
+
+@pytest.mark.parametrize("which", ["q", "k", "v", "o"])
+def test_misaligned_bf16(lib, which):
+    assert fwd(lib, **{which: P + 8}) == MISALIGNED
+
+
+def test_misaligned_lse(lib):
+    assert fwd(lib, lse=P + 2) == MISALIGNED
+
+
+def test_backward_workspace_checks(lib):
+    need = lib.fa_bwd_workspace_size(1, 1, 128, 64)
+    assert need > 0
+    assert bwd(lib, ws=0) == WORKSPACE
+    assert bwd(lib, ws_bytes=need - 1) == WORKSPACE
+    assert bwd(lib, ws=P + 16, ws_bytes=need) == MISALIGNED
+    assert bwd(lib, ptr=P + 8) == MISALIGNED
+
+
+def test_workspace_size_formula(lib):
+    # D and base-2 L (fp32 per padded row) + fp32 dQ accumulator, heads padded to 128 rows
+    for B, H, N, d in ((2, 4, 1024, 64), (1, 16, 1000, 128), (1, 2, 1, 256)):
+        rows = B * H * ((N + 127) // 128 * 128)
+        expect = 0
+        for nbytes in (rows * 4, rows * 4, rows * d * 4):
+            expect = (expect + 255) // 256 * 256 + nbytes
+        expect = (expect + 255) // 256 * 256
+        assert lib.fa_bwd_workspace_size(B, H, N, d) == expect
+
+
+def test_python_binding_rejects_cpu_tensors():
+    torch = pytest.importorskip("torch")
+    import exact_softmax_attention_fa_gb300 as fa
+    q = torch.zeros(1, 1, 128, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fa.fa_fwd(q, q, q, q.clone(), torch.zeros(1, 1, 128), False, 0.125)
+    with pytest.raises(TypeError):
+        fa.fa_fwd(q.float(), q, q, q, torch.zeros(1, 1, 128), False, 0.125)
