@@ -228,6 +228,7 @@ fa_status_t fa_bwd(const void* q, const void* k, const void* v, const void* o, c
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(dO, 16) ||
       !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4))
     return FA_ERR_MISALIGNED;
+  if (d == 256) return FA_ERR_UNSUPPORTED;  // d = 256 backward kernel not built yet
   const int BH = B * H;
   const BwdWorkspaceLayout wl = bwd_layout(BH, N, d);
   if (!workspace || workspace_bytes < wl.total) return FA_ERR_WORKSPACE;

@@ -1,6 +1,547 @@
-// Backward pass (placeholder until the kernels land).
+// Backward pass of exact softmax attention for sm_103a.
+//
+// Method (web pages on FlashAttention-2):
+//   "FlashAttention 2: ..." reading note (papers.chlience.com) 5.3 and the
+//   paper-graph-ui summary, "The Backward Pass": precompute
+//   D_i = sum_k dO_ik O_ik; then, with key blocks OUTER (dK_j, dV_j stay on
+//   chip) and query blocks inner: S = Q_i K_j^T, P = exp(S - L_i),
+//   dV_j += P^T dO_i, dP = dO_i V_j^T, dS = P o (dP - D_i),
+//   dQ_i += dS K_j (accumulated across key blocks with atomic adds, reading
+//   note 5.4), dK_j += dS^T Q_i.
+//
+// GB300 mapping (our design):
+//   Three kernels on the caller's stream:
+//   1. bwd_pre_kernel (HBM-bound): D from the stored bf16 O and dO, the
+//      base-2 logsumexp L*log2(e), and zeroes the fp32 dQ accumulator. Every
+//      head is padded to a multiple of 128 rows; padding rows get D = 0 and
+//      L = +inf so their probabilities are exactly 0.
+//   2. fa_bwd_kernel: one CTA per (head, 128-key tile j). Everything is
+//      computed transposed, with keys on the 128 TMEM lanes:
+//        S^T = K_j Q_i^T and dP^T = V_j dO_i^T   (SS MMAs into TMEM)
+//        warpgroup 0, thread r = key r: P^T = 2^(S^T scale log2e - L log2e),
+//          dS^T = P^T o (dP^T - D) * scale; P^T (bf16) goes back to TMEM,
+//          dS^T (bf16) to a 128-byte-swizzled smem tile
+//        dV += P^T dO_i      (A = P^T from TMEM, B = dO_i MN-major)
+//        dK += dS^T Q_i      (A = dS^T smem, K-major; B = Q_i MN-major)
+//        dQ_i = dS K_j       (A = the same smem tile read MN-major,
+//                             B = K_j MN-major), into TMEM, queries on lanes
+//        warpgroup 1, thread q = query q: reads its dQ_i row from TMEM and
+//          adds it into the fp32 accumulator with 16-byte vector reductions.
+//      Two 128-column TMEM regions alternate: S^T(i) and later dQ_i use one,
+//      dP^T(i) and then P^T(i) the other; S^T(i+1) reuses the P^T region once
+//      dV(i) is done and dP^T(i+1) reuses the dQ region once it was drained.
+//      dK, dV (fp32, TMEM) are written once at the end through TMA stores.
+//   3. bwd_post_kernel (HBM-bound): dQ = bf16(accumulator).
+//
+// TMEM columns (512 allocated): dK [0, d), dV [d, 2d), region 0 [256, 384),
+// region 1 [384, 512).
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <cmath>
+
 #include "fa_internal.h"
+#include "sm103_ptx.cuh"
 
 namespace fa {
-cudaError_t launch_bwd(const BwdLaunch&, cudaStream_t) { return cudaErrorNotSupported; }
+namespace {
+
+constexpr int kThreads = 320;
+constexpr int kLoadWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr float kLog2e = 1.44269504088896340736f;
+
+template <int HD>
+struct BwdCfg {
+  static constexpr int CHUNKS = HD / 64;
+  static constexpr int TILE_BYTES = 128 * HD * 2;
+  static constexpr int CHUNK_BYTES = 128 * 128;
+  static constexpr int QST = HD == 64 ? 3 : 2;  // Q_i / dO_i pipeline stages
+  static constexpr int DS_BYTES = 128 * 128 * 2;
+  static constexpr uint32_t DK_COL = 0;
+  static constexpr uint32_t DV_COL = HD;
+  __host__ __device__ static constexpr uint32_t region(int r) { return 256u + 128u * uint32_t(r); }
+  // smem: K_j, V_j, QST x (Q_i, dO_i), dS^T
+  static constexpr int SMEM_BYTES = (2 + 2 * QST) * TILE_BYTES + DS_BYTES + 1024;
+};
+
+struct BwdShared {
+  uint64_t kv_full;
+  uint64_t qdo_full[4], qdo_empty[4];
+  uint64_t sdp_full, ds_ready, pv_done, dq_full, dq_free, acc_done;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+__device__ __forceinline__ void record_timeout(uint32_t* status, int* abort_flag, uint32_t where) {
+  if (atomicCAS(status, 0u, static_cast<uint32_t>(FA_ERR_TIMEOUT)) == 0u) {
+    status[1] = where;
+    status[2] = blockIdx.x;
+    status[3] = threadIdx.x;
+  }
+  *reinterpret_cast<volatile int*>(abort_flag) = 1;
+}
+
+// Work item: key tile j of head bh; query tiles i0..T-1 (causal: i0 = j).
+template <bool CAUSAL>
+struct BwdWork {
+  int bh, j, i0, T;
+  __device__ BwdWork(int block, int BH, int N) {
+    T = (N + 127) / 128;
+    if (CAUSAL) {  // most work first: key tile j meets T - j query tiles
+      bh = block % BH;
+      j = block / BH;
+    } else {
+      bh = block / T;
+      j = block % T;
+    }
+    i0 = CAUSAL ? j : 0;
+  }
+  __device__ int n_iter() const { return T - i0; }
+};
+
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
+__device__ __forceinline__ float4 ldg_f4(const float* p) { return __ldg(reinterpret_cast<const float4*>(p)); }
+
+// ---------------------------------------------------------------------------
+// 1. preprocess
+// ---------------------------------------------------------------------------
+// One group of d/8 lanes per padded row: D = sum(dO * O) in fp32 from bf16,
+// lse2 = L * log2(e) (+inf on padding rows), dq_acc row = 0.
+template <int HD>
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
+                                                      const __nv_bfloat16* __restrict__ dO,
+                                                      const float* __restrict__ lse, float* __restrict__ D,
+                                                      float* __restrict__ lse2, float* __restrict__ dq_acc, int N,
+                                                      int Npad, long long total_rows) {
+  constexpr int LPR = HD / 8;  // lanes per row, 16 bytes of O and dO each
+  constexpr int RPW = 32 / LPR;
+  const long long row = (static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32) * RPW +
+                        (threadIdx.x % 32) / LPR;
+  const int sub = threadIdx.x % LPR;
+  float acc = 0.f;
+  const bool in_range = row < total_rows;
+  long long bh = 0;
+  int n = 0;
+  if (in_range) {
+    bh = row / Npad;
+    n = static_cast<int>(row - bh * Npad);
+    if (n < N) {
+      const size_t off = (static_cast<size_t>(bh) * N + n) * HD + sub * 8;
+      const uint4 a = __ldg(reinterpret_cast<const uint4*>(o + off));
+      const uint4 b = __ldg(reinterpret_cast<const uint4*>(dO + off));
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 fa = __bfloat1622float2(a2[k]);
+        const float2 fb = __bfloat1622float2(b2[k]);
+        acc = fmaf(fa.x, fb.x, acc);
+        acc = fmaf(fa.y, fb.y, acc);
+      }
+    }
+    float4* z = reinterpret_cast<float4*>(dq_acc + static_cast<size_t>(row) * HD + sub * 8);
+    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+#pragma unroll
+  for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (in_range && sub == 0) {
+    D[row] = acc;
+    lse2[row] = n < N ? lse[static_cast<size_t>(bh) * N + n] * kLog2e : INFINITY;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 3. postprocess: dq = bf16(dq_acc) on the real rows
+// ---------------------------------------------------------------------------
+template <int HD>
+__global__ void __launch_bounds__(256) bwd_post_kernel(const float* __restrict__ dq_acc,
+                                                       __nv_bfloat16* __restrict__ dq, int N, int Npad,
+                                                       long long total_vec) {
+  const long long v = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;  // 8 elements each
+  if (v >= total_vec) return;
+  constexpr int VPR = HD / 8;
+  const long long row = v / VPR;  // row of [BH][N]
+  const int sub = static_cast<int>(v - row * VPR);
+  const long long bh = row / N;
+  const int n = static_cast<int>(row - bh * N);
+  const float* src = dq_acc + (static_cast<size_t>(bh) * Npad + n) * HD + sub * 8;
+  const float4 a = ldg_f4(src), b = ldg_f4(src + 4);
+  uint4 out;
+  out.x = pack_bf16x2(a.x, a.y);
+  out.y = pack_bf16x2(a.z, a.w);
+  out.z = pack_bf16x2(b.x, b.y);
+  out.w = pack_bf16x2(b.z, b.w);
+  *reinterpret_cast<uint4*>(dq + static_cast<size_t>(row) * HD + sub * 8) = out;
+}
+
+// ---------------------------------------------------------------------------
+// 2. main kernel roles
+// ---------------------------------------------------------------------------
+template <int HD, bool CAUSAL>
+__device__ void bwd_load_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sK, uint8_t* sV, uint8_t* sQ,
+                              uint8_t* sdO, const BwdWork<CAUSAL>& wk) {
+  using C = BwdCfg<HD>;
+  tma_prefetch_desc(&p.tmQ);
+  tma_prefetch_desc(&p.tmK);
+  tma_prefetch_desc(&p.tmV);
+  tma_prefetch_desc(&p.tmdO);
+  mbar_arrive_expect_tx(&sh.kv_full, 2 * C::TILE_BYTES);
+#pragma unroll
+  for (int c = 0; c < C::CHUNKS; ++c) {
+    tma_load_3d(sK + c * C::CHUNK_BYTES, &p.tmK, &sh.kv_full, c * 64, wk.j * 128, wk.bh);
+    tma_load_3d(sV + c * C::CHUNK_BYTES, &p.tmV, &sh.kv_full, c * 64, wk.j * 128, wk.bh);
+  }
+  const int n_iter = wk.n_iter();
+  int issued = 0;
+  bool aborted = false;
+  for (int n = 0; n < n_iter; ++n) {
+    const int s = n % C::QST;
+    if (n >= C::QST && !mbar_wait(&sh.qdo_empty[s], ((n / C::QST) - 1) & 1, &sh.abort_flag, p.wait_limit_ns)) {
+      aborted = true;
+      break;
+    }
+    const int i = wk.i0 + n;
+    mbar_arrive_expect_tx(&sh.qdo_full[s], 2 * C::TILE_BYTES);
+#pragma unroll
+    for (int c = 0; c < C::CHUNKS; ++c) {
+      tma_load_3d(sQ + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &p.tmQ, &sh.qdo_full[s], c * 64, i * 128, wk.bh);
+      tma_load_3d(sdO + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &p.tmdO, &sh.qdo_full[s], c * 64, i * 128, wk.bh);
+    }
+    ++issued;
+  }
+  const int zero = 0;
+  if (aborted) {
+    record_timeout(p.status, &sh.abort_flag, WHERE_BWD_LOAD);
+    for (int n = max(0, issued - C::QST); n < issued; ++n)
+      mbar_wait(&sh.qdo_full[n % C::QST], (n / C::QST) & 1, &zero, p.wait_limit_ns);
+  }
+  mbar_wait(&sh.kv_full, 0, &zero, p.wait_limit_ns);
+}
+
+template <int HD, bool CAUSAL>
+__device__ void bwd_mma_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sK, uint8_t* sV, uint8_t* sQ,
+                             uint8_t* sdO, uint8_t* sDS, uint32_t tmem, const BwdWork<CAUSAL>& wk) {
+  using C = BwdCfg<HD>;
+  constexpr uint32_t kIdescSq = make_idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
+  constexpr uint32_t kIdescAcc = make_idesc_bf16_f32(128, HD, false, true);   // dV, dK
+  constexpr uint32_t kIdescDq = make_idesc_bf16_f32(128, HD, true, true);     // dQ
+  const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV), q_addr = smem_u32(sQ), do_addr = smem_u32(sdO),
+                 ds_addr = smem_u32(sDS);
+  const uint64_t lim = p.wait_limit_ns;
+  const int n_iter = wk.n_iter();
+
+  // D[tmem] = A (128 x HD, K-major) * B (128 x HD, K-major)^T
+  auto issue_sq = [&](uint32_t d_col, uint32_t a_addr, uint32_t b_addr) {
+#pragma unroll
+    for (int ks = 0; ks < HD / 16; ++ks) {
+      const uint32_t off = (ks >> 2) * C::CHUNK_BYTES + (ks & 3) * 32;
+      umma_ss(tmem + d_col, make_smem_desc_sw128(a_addr + off, 16, 1024), make_smem_desc_sw128(b_addr + off, 16, 1024),
+              kIdescSq, ks > 0 ? 1u : 0u);
+    }
+  };
+  auto fail = [&]() { record_timeout(p.status, &sh.abort_flag, WHERE_BWD_MMA); };
+
+  if (!mbar_wait(&sh.kv_full, 0, &sh.abort_flag, lim) || !mbar_wait(&sh.qdo_full[0], 0, &sh.abort_flag, lim)) {
+    fail();
+    return;
+  }
+  tc_fence_after_sync();
+  issue_sq(C::region(0), k_addr, q_addr);   // S^T(i0)
+  issue_sq(C::region(1), v_addr, do_addr);  // dP^T(i0)
+  umma_commit(&sh.sdp_full);
+
+  for (int n = 0; n < n_iter; ++n) {
+    const int s = n % C::QST;
+    const uint32_t sreg = C::region(n & 1), dpreg = C::region((n + 1) & 1);
+    const uint32_t qa = q_addr + s * C::TILE_BYTES, doa = do_addr + s * C::TILE_BYTES;
+    if (!mbar_wait(&sh.ds_ready, n & 1, &sh.abort_flag, lim)) return fail();
+    tc_fence_after_sync();
+    // dV += P^T dO_i  (P^T bf16 in TMEM at dpreg)
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks)
+      umma_ts(tmem + C::DV_COL, tmem + dpreg + ks * 8, make_smem_desc_sw128(doa + ks * 2048, C::CHUNK_BYTES, 1024),
+              kIdescAcc, (n > 0 || ks > 0) ? 1u : 0u);
+    umma_commit(&sh.pv_done);
+    // dQ_i = dS K_j into sreg (queries on lanes)
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks)
+      umma_ss(tmem + sreg, make_smem_desc_sw128(ds_addr + ks * 2048, C::CHUNK_BYTES, 1024),
+              make_smem_desc_sw128(k_addr + ks * 2048, C::CHUNK_BYTES, 1024), kIdescDq, ks > 0 ? 1u : 0u);
+    umma_commit(&sh.dq_full);
+    // dK += dS^T Q_i
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks)
+      umma_ss(tmem + C::DK_COL, make_smem_desc_sw128(ds_addr + (ks >> 2) * C::CHUNK_BYTES + (ks & 3) * 32, 16, 1024),
+              make_smem_desc_sw128(qa + ks * 2048, C::CHUNK_BYTES, 1024), kIdescAcc, (n > 0 || ks > 0) ? 1u : 0u);
+    umma_commit(&sh.qdo_empty[s]);
+    if (n + 1 < n_iter) {
+      const int s1 = (n + 1) % C::QST;
+      if (!mbar_wait(&sh.qdo_full[s1], ((n + 1) / C::QST) & 1, &sh.abort_flag, lim)) return fail();
+      if (!mbar_wait(&sh.pv_done, n & 1, &sh.abort_flag, lim)) return fail();
+      tc_fence_after_sync();
+      issue_sq(dpreg, k_addr, q_addr + s1 * C::TILE_BYTES);  // S^T(i+1) over the consumed P^T(i)
+      if (!mbar_wait(&sh.dq_free, n & 1, &sh.abort_flag, lim)) return fail();
+      tc_fence_after_sync();
+      issue_sq(sreg, v_addr, do_addr + s1 * C::TILE_BYTES);  // dP^T(i+1) over the drained dQ_i
+      umma_commit(&sh.sdp_full);
+    }
+  }
+  umma_commit(&sh.acc_done);
+}
+
+// Warpgroup 0: thread r owns key r of the tile.
+template <int HD, bool CAUSAL>
+__device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS, uint32_t tmem,
+                                 const BwdWork<CAUSAL>& wk) {
+  using C = BwdCfg<HD>;
+  const int r = threadIdx.x & 127;
+  const uint32_t lane_base = static_cast<uint32_t>((threadIdx.x >> 5) & 3) << 21;
+  const int key = wk.j * 128 + r;
+  const bool key_valid = key < p.N;
+  const float c2 = p.scale_log2;
+  const float sc = p.scale;
+  const uint64_t lim = p.wait_limit_ns;
+  const uint32_t ds_base = smem_u32(sDS);
+  const float* lse2_bh = p.lse2 + static_cast<size_t>(wk.bh) * p.Npad;
+  const float* D_bh = p.D + static_cast<size_t>(wk.bh) * p.Npad;
+  const int n_iter = wk.n_iter();
+  for (int n = 0; n < n_iter; ++n) {
+    const int i = wk.i0 + n;
+    const uint32_t tS = tmem + lane_base + C::region(n & 1);
+    const uint32_t tdP = tmem + lane_base + C::region((n + 1) & 1);
+    if (!__all_sync(0xffffffffu, mbar_wait(&sh.sdp_full, n & 1, &sh.abort_flag, lim))) {
+      record_timeout(p.status, &sh.abort_flag, WHERE_BWD_SOFTMAX);
+      return;
+    }
+    tc_fence_after_sync();
+    // Causal diagonal tile: query q sees key r only if q >= r.
+    const int q_lo = (CAUSAL && i == wk.j) ? r : 0;
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      uint32_t sv[32], dpv[32];
+      tmem_ld32(tS + c * 32, sv);
+      tmem_ld32(tdP + c * 32, dpv);
+      const float* l2p = lse2_bh + i * 128 + c * 32;
+      const float* dp_ = D_bh + i * 128 + c * 32;
+      float l2[32], dd[32];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float4 a = ldg_f4(l2p + 4 * k);
+        const float4 b = ldg_f4(dp_ + 4 * k);
+        l2[4 * k] = a.x, l2[4 * k + 1] = a.y, l2[4 * k + 2] = a.z, l2[4 * k + 3] = a.w;
+        dd[4 * k] = b.x * sc, dd[4 * k + 1] = b.y * sc, dd[4 * k + 2] = b.z * sc, dd[4 * k + 3] = b.w * sc;
+      }
+      tmem_ld_wait();
+      uint32_t ppk[16], dpk[16];
+#pragma unroll
+      for (int k = 0; k < 32; k += 2) {
+        const int q0 = c * 32 + k;
+        float p0 = ex2_approx(fmaf(__uint_as_float(sv[k]), c2, -l2[k]));
+        float p1 = ex2_approx(fmaf(__uint_as_float(sv[k + 1]), c2, -l2[k + 1]));
+        if (!key_valid || q0 < q_lo) p0 = 0.f;
+        if (!key_valid || q0 + 1 < q_lo) p1 = 0.f;
+        const float d0 = p0 * fmaf(__uint_as_float(dpv[k]), sc, -dd[k]);
+        const float d1 = p1 * fmaf(__uint_as_float(dpv[k + 1]), sc, -dd[k + 1]);
+        ppk[k / 2] = pack_bf16x2(p0, p1);
+        dpk[k / 2] = pack_bf16x2(d0, d1);
+      }
+      // P^T chunk -> TMEM columns [16c, 16c + 16) of the dP region (already read)
+      tmem_st16(tdP + c * 16, ppk);
+      // dS^T chunk -> smem row r, queries 32c .. 32c + 31 (4 swizzled 16-byte units)
+      const uint32_t chunk_base = ds_base + (c >> 1) * C::CHUNK_BYTES;
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        st_shared_v4(chunk_base + sw128_offset(r, (c & 1) * 4 + u), dpk[4 * u], dpk[4 * u + 1], dpk[4 * u + 2],
+                     dpk[4 * u + 3]);
+    }
+    tmem_st_wait();
+    fence_proxy_async_smem();
+    tc_fence_before_sync();
+    mbar_arrive(&sh.ds_ready);
+  }
+}
+
+// Warpgroup 1: thread q owns query row q of the current query tile.
+template <int HD, bool CAUSAL>
+__device__ void bwd_dq_role(const BwdLaunch& p, BwdShared& sh, uint32_t tmem, const BwdWork<CAUSAL>& wk) {
+  using C = BwdCfg<HD>;
+  const int q = threadIdx.x & 127;
+  const uint32_t lane_base = static_cast<uint32_t>((threadIdx.x >> 5) & 3) << 21;
+  const uint64_t lim = p.wait_limit_ns;
+  const int n_iter = wk.n_iter();
+  for (int n = 0; n < n_iter; ++n) {
+    const int i = wk.i0 + n;
+    if (!__all_sync(0xffffffffu, mbar_wait(&sh.dq_full, n & 1, &sh.abort_flag, lim))) {
+      record_timeout(p.status, &sh.abort_flag, WHERE_BWD_DQ);
+      return;
+    }
+    tc_fence_after_sync();
+    const uint32_t t = tmem + lane_base + C::region(n & 1);
+    float* dst = p.dq_acc + (static_cast<size_t>(wk.bh) * p.Npad + i * 128 + q) * HD;
+#pragma unroll
+    for (int c = 0; c < HD; c += 32) {
+      uint32_t v[32];
+      tmem_ld32(t + c, v);
+      tmem_ld_wait();
+      if (c + 32 >= HD) {  // last chunk read: the region can be reused
+        tc_fence_before_sync();
+        mbar_arrive(&sh.dq_free);
+      }
+#pragma unroll
+      for (int k = 0; k < 32; k += 4)
+        red_add_v4(dst + c + k, __uint_as_float(v[k]), __uint_as_float(v[k + 1]), __uint_as_float(v[k + 2]),
+                   __uint_as_float(v[k + 3]));
+    }
+  }
+}
+
+// Warpgroup 0 after the loop: dK, dV (fp32 TMEM) -> bf16 -> smem (over K_j,
+// V_j) -> TMA store.
+template <int HD, bool CAUSAL>
+__device__ void bwd_epilogue(const BwdLaunch& p, BwdShared& sh, uint8_t* sK, uint8_t* sV, uint32_t tmem,
+                             const BwdWork<CAUSAL>& wk) {
+  using C = BwdCfg<HD>;
+  const int r = threadIdx.x & 127;
+  const uint32_t lane_base = static_cast<uint32_t>((threadIdx.x >> 5) & 3) << 21;
+  bool ok = !*reinterpret_cast<volatile int*>(&sh.abort_flag);
+  if (ok) {
+    ok = __all_sync(0xffffffffu, mbar_wait(&sh.acc_done, 0, &sh.abort_flag, p.wait_limit_ns));
+    if (!ok) record_timeout(p.status, &sh.abort_flag, WHERE_BWD_SOFTMAX);
+  }
+  tc_fence_after_sync();
+  if (ok) {
+#pragma unroll
+    for (int which = 0; which < 2; ++which) {
+      const uint32_t t = tmem + lane_base + (which == 0 ? C::DK_COL : C::DV_COL);
+      const uint32_t stage = smem_u32(which == 0 ? sK : sV);
+#pragma unroll 1
+      for (int c = 0; c < HD; c += 32) {
+        uint32_t v[32];
+        tmem_ld32(t + c, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int col = c + u * 8;
+          st_shared_v4(stage + (col >> 6) * C::CHUNK_BYTES + sw128_offset(r, (col & 63) >> 3),
+                       pack_bf16x2(__uint_as_float(v[u * 8 + 0]), __uint_as_float(v[u * 8 + 1])),
+                       pack_bf16x2(__uint_as_float(v[u * 8 + 2]), __uint_as_float(v[u * 8 + 3])),
+                       pack_bf16x2(__uint_as_float(v[u * 8 + 4]), __uint_as_float(v[u * 8 + 5])),
+                       pack_bf16x2(__uint_as_float(v[u * 8 + 6]), __uint_as_float(v[u * 8 + 7])));
+        }
+      }
+    }
+    fence_proxy_async_smem();
+  }
+  named_barrier_sync(1, 128);
+  if (ok && r == 0 && !*reinterpret_cast<volatile int*>(&sh.abort_flag)) {
+#pragma unroll
+    for (int c = 0; c < C::CHUNKS; ++c) {
+      tma_store_3d(&p.tmdK, sK + c * C::CHUNK_BYTES, c * 64, wk.j * 128, wk.bh);
+      tma_store_3d(&p.tmdV, sV + c * C::CHUNK_BYTES, c * 64, wk.j * 128, wk.bh);
+    }
+    tma_store_commit();
+    tma_store_wait_all();
+  }
+}
+
+template <int HD, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_constant__ BwdLaunch p) {
+  using C = BwdCfg<HD>;
+  extern __shared__ uint8_t smem_dyn[];
+  __shared__ BwdShared sh;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+  uint8_t* sK = smem;
+  uint8_t* sV = sK + C::TILE_BYTES;
+  uint8_t* sQ = sV + C::TILE_BYTES;
+  uint8_t* sdO = sQ + C::QST * C::TILE_BYTES;
+  uint8_t* sDS = sdO + C::QST * C::TILE_BYTES;
+  const int warp = threadIdx.x >> 5;
+  const BwdWork<CAUSAL> wk(blockIdx.x, p.BH, p.N);
+
+  if (threadIdx.x == 0) {
+    mbar_init(&sh.kv_full, 1);
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(&sh.qdo_full[s], 1);
+      mbar_init(&sh.qdo_empty[s], 1);
+    }
+    mbar_init(&sh.sdp_full, 1);
+    mbar_init(&sh.ds_ready, 128);
+    mbar_init(&sh.pv_done, 1);
+    mbar_init(&sh.dq_full, 1);
+    mbar_init(&sh.dq_free, 128);
+    mbar_init(&sh.acc_done, 1);
+    sh.abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&sh.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = sh.tmem_base;
+
+  if (warp == kLoadWarp) {
+    if (lane_id() == 0) bwd_load_role<HD, CAUSAL>(p, sh, sK, sV, sQ, sdO, wk);
+  } else if (warp == kMmaWarp) {
+    if (lane_id() == 0) bwd_mma_role<HD, CAUSAL>(p, sh, sK, sV, sQ, sdO, sDS, tmem, wk);
+  } else if (warp < 4) {
+    bwd_softmax_role<HD, CAUSAL>(p, sh, sDS, tmem, wk);
+    bwd_epilogue<HD, CAUSAL>(p, sh, sK, sV, tmem, wk);
+  } else {
+    bwd_dq_role<HD, CAUSAL>(p, sh, tmem, wk);
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
+}
+
+template <int HD, bool CAUSAL>
+cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t stream) {
+  using C = BwdCfg<HD>;
+  const long long rows = static_cast<long long>(a.BH) * a.Npad;
+  {
+    constexpr int RPB = 8 * (32 / (HD / 8));  // rows per 256-thread block
+    const long long blocks = (rows + RPB - 1) / RPB;
+    bwd_pre_kernel<HD><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a.o, a.dO, a.lse, a.D, a.lse2, a.dq_acc,
+                                                                          a.N, a.Npad, rows);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  {
+    auto kern = fa_bwd_kernel<HD, CAUSAL>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const int T = (a.N + 127) / 128;
+    kern<<<static_cast<unsigned>(static_cast<long long>(a.BH) * T), kThreads, C::SMEM_BYTES, stream>>>(a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  {
+    const long long vec = static_cast<long long>(a.BH) * a.N * (HD / 8);
+    bwd_post_kernel<HD><<<static_cast<unsigned>((vec + 255) / 256), 256, 0, stream>>>(a.dq_acc, a.dq, a.N, a.Npad,
+                                                                                      vec);
+    return cudaGetLastError();
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(const BwdLaunch& a, cudaStream_t stream) {
+  switch (a.d) {
+    case 64: return a.causal ? launch_bwd_t<64, true>(a, stream) : launch_bwd_t<64, false>(a, stream);
+    case 128: return a.causal ? launch_bwd_t<128, true>(a, stream) : launch_bwd_t<128, false>(a, stream);
+    default: return cudaErrorNotSupported;
+  }
+}
+
 }  // namespace fa
