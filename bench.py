@@ -1,0 +1,441 @@
+#!/usr/bin/env python3
+"""Benchmark of exact softmax attention (forward + backward) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+One step is one pass of the whole hot path over one batch of synthetic input:
+fa_fwd, then the backward's three phases (preprocess, main, postprocess), all
+through the C ABI. The default workload is the pages' microbenchmark shape at
+hidden size 2048 with d = 128 and N = 8192 (B = 16384 / N = 2, H = 16),
+non-causal: the configuration the headline "fwd+bwd TFLOP/s" figures are
+quoted on. FLOPs follow the pages' convention: forward 4 B H N^2 d (halved
+when causal), backward 2.5x forward.
+
+Rank 0 prints one JSON line. `value` is fwd+bwd TFLOP/s over all ranks with
+inputs resident in HBM; `e2e` is the same metric with host->device copies of
+Q, K, V, dO and device->host copies of O, L, dQ, dK, dV inside the timed
+region; `roofline` is the dominant kernel (the backward main kernel) against
+the measured dense bf16 peak; `cpu_baseline` is the float64 CPU oracle timed on
+a bounded sample. `--impl reference` times that oracle alone as the reference
+arm (rank 0 only).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from attn_inputs import WORKLOADS, sweep_points, seed_for, make_inputs  # noqa: E402
+
+METRIC = "attention fwd and fwd+bwd TFLOP/s (bf16, 1 GB300) and % of dense BF16 peak"
+UNIT = "TFLOP/s"
+DEFAULT_WORKLOAD = "sweep_d128_N8192_full"
+# Pages' fwd+bwd number for this exact workload (A100 80GB, d=128, N=8k,
+# non-causal, 16k tokens, hidden 2048): context only, another machine.
+PAGES_FWD_BWD_TFLOPS = {"sweep_d128_N8192_full": 201.0}
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = {
+    "fa_bwd_main": ["exact_softmax_attention_fa_gb300/csrc/fa_bwd.cu",
+                    "exact_softmax_attention_fa_gb300/csrc/sm103_ptx.cuh"],
+    "fa_fwd": ["exact_softmax_attention_fa_gb300/csrc/fa_fwd.cu",
+               "exact_softmax_attention_fa_gb300/csrc/sm103_ptx.cuh"],
+}
+
+
+def all_workloads() -> dict:
+    w = {name: dict(p) for name, p in sweep_points()}
+    for name, p in WORKLOADS.items():
+        w[name] = dict(p)
+    return w
+
+
+def flops(p: dict, mode: str) -> float:
+    f = 4.0 * p["B"] * p["H"] * p["N"] * p["N"] * p["d"]
+    if p["causal"]:
+        f *= 0.5
+    return f * {"fwd": 1.0, "bwd": 2.5, "fwd_bwd": 3.5}[mode]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return pk, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_hash(kernel: str) -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it matches the current source."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m_bytes = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
+    m_hash = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
+    if not m_bytes or not m_hash or m_hash.group(1) != source_hash(kernel):
+        return None
+    return int(m_bytes.group(1))
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        try:
+            self.out = tempfile.NamedTemporaryFile(mode="w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.gpu_index)], stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.flush()
+        self.out.seek(0)
+        rows = [r.split(",") for r in self.out.read().strip().splitlines() if r.strip()]
+        self.out.close()
+        os.unlink(self.out.name)
+        sm, mx, reasons = [], [], set()
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for name, val in zip(self.REASONS, r[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# distributed helpers (one process per GPU; gloo works on CPU for tests)
+# ---------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(device=None):
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        if device is not None and getattr(device, "type", "cpu") == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def aggregate_value(per_rank_flops: float, world: int, max_time_s: float) -> float:
+    """Whole-job TFLOP/s: every rank processes its own copy of the workload."""
+    return per_rank_flops * world / max_time_s / 1e12
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle baseline (bounded sample)
+# ---------------------------------------------------------------------------
+def cpu_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n and n[0]:
+            return int(n[0])
+    except Exception:
+        pass
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_sample(p: dict, x: dict, rows_per_call: int, calls: int):
+    """Run the float64 oracle's row-block fwd+bwd `calls` times; return (seconds, flops)."""
+    import numpy as np
+    import oracle
+    from attn_inputs import bf16_bits_to_f64
+    scale = float(np.float32(1.0 / np.sqrt(p["d"])))
+    N = p["N"]
+    f64 = {k: bf16_bits_to_f64(v[0, 0]) for k, v in x.items()}
+    t0 = time.perf_counter()
+    fl = 0.0
+    for c in range(calls):
+        r0 = (c * rows_per_call) % max(1, N - rows_per_call + 1)
+        rows = np.arange(r0, min(N, r0 + rows_per_call))
+        oracle.attention_fwd_bwd_rows(f64["q"], f64["k"], f64["v"], f64["do"], rows, p["causal"], scale)
+        keys = (rows + 1).sum() if p["causal"] else len(rows) * N
+        fl += 3.5 * 4.0 * keys * p["d"]  # same convention: causal counts only unmasked entries
+    return time.perf_counter() - t0, fl
+
+
+def calibrate_rows(p: dict, x: dict, target_s: float) -> int:
+    rows = 64
+    t, _ = oracle_sample(p, x, rows, 1)
+    per_row = max(t / rows, 1e-7)
+    return int(max(16, min(p["N"], target_s / per_row)))
+
+
+# ---------------------------------------------------------------------------
+# arms
+# ---------------------------------------------------------------------------
+def host_inputs(p: dict, rank: int):
+    return make_inputs(p["B"], p["H"], p["N"], p["d"], seed_for(p) + rank)
+
+
+def run_reference(args, p: dict, name: str) -> dict:
+    """The float64 CPU oracle as the reference arm (rank 0 only)."""
+    x = make_inputs(1, 1, p["N"], p["d"], seed_for(p))
+    budget_s = 100.0
+    rows = calibrate_rows(p, x, budget_s / max(1, args.steps + args.warmup))
+    oracle_sample(p, x, rows, args.warmup)
+    t, fl = oracle_sample(p, x, rows, args.steps)
+    value = fl / t / 1e12
+    cores = cpu_threads()
+    sample = (f"per step: float64 oracle forward+backward of {rows} query rows x all {p['N']} keys of one head "
+              f"(d={p['d']}, causal={p['causal']}), i.e. {rows / p['N'] / (p['B'] * p['H']):.2e} of one "
+              f"workload step")
+    return {
+        "metric": METRIC, "value": value, "unit": UNIT, "impl": "reference", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": name, **{k: p[k] for k in ("B", "H", "N", "d", "causal")}},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def run_ours(args, p: dict, name: str, world: int, rank: int, local: int) -> dict | None:
+    import numpy as np
+    import torch
+    import exact_softmax_attention_fa_gb300 as fa
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    B, H, N, d, causal = p["B"], p["H"], p["N"], p["d"], p["causal"]
+    scale = float(np.float32(1.0 / np.sqrt(d)))
+    x = host_inputs(p, rank)
+    pinned = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).pin_memory() for k, v in x.items()}
+    dev = {k: v.to(device) for k, v in pinned.items()}
+    q, k, v, do = dev["q"], dev["k"], dev["v"], dev["do"]
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    ws = torch.empty(fa.fa_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        fa.fa_fwd(q, k, v, o, lse, causal, scale, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        fa.fa_bwd_preprocess(o, lse, do, ws, stream)
+        if ev is not None:
+            ev[2].record(stream)
+        fa.fa_bwd_main(q, k, v, do, dk, dv, causal, scale, ws, stream)
+        if ev is not None:
+            ev[3].record(stream)
+        fa.fa_bwd_postprocess(dq, ws, stream)
+        if ev is not None:
+            ev[4].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(device)
+    if fa.fa_get_device_status(stream) != 0:
+        raise RuntimeError("device status reports a timed-out pipeline wait during warm-up")
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    barrier(device)
+    torch.cuda.synchronize(device)
+    clocks.start()
+    for s in range(args.steps):
+        step(events[s])
+    torch.cuda.synchronize(device)
+    barrier(device)
+    clk = clocks.stop()
+    total_ms = events[0][0].elapsed_time(events[-1][4])
+    phase_ms = [sum(e[i].elapsed_time(e[i + 1]) for e in events) / args.steps for i in range(4)]
+    status = fa.fa_get_device_status(stream)
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed region")
+    max_s = max_over_ranks(total_ms / 1e3, device if world > 1 else None)
+
+    # end to end through the public API with host buffers
+    e2e_steps = max(1, min(args.steps, 20))
+    out_host = {kk: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                for kk, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
+
+    def e2e_step():
+        for kk in ("q", "k", "v", "do"):
+            dev[kk].copy_(pinned[kk], non_blocking=True)
+        step()
+        for kk, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
+            out_host[kk].copy_(t, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(device)
+    barrier(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3 / e2e_steps, device if world > 1 else None)
+    h2d = sum(t.numel() * t.element_size() for t in (q, k, v, do))
+    d2h = sum(t.numel() * t.element_size() for t in (o, lse, dq, dk, dv))
+
+    if rank != 0:
+        return None
+
+    peaks, peak_kind = load_peaks()
+    burst, sustained = peaks["bf16_tflops"], peaks["bf16_tflops_sustained"]
+    f_fwd, f_bwd, f_step = flops(p, "fwd"), flops(p, "bwd"), flops(p, "fwd_bwd")
+    value = aggregate_value(f_step * args.steps, world, max_s)
+    fwd_tf = f_fwd / (phase_ms[0] / 1e3) / 1e12
+    bwd_tf = f_bwd / (sum(phase_ms[1:]) / 1e3) / 1e12
+    main_tf = f_bwd / (phase_ms[2] / 1e3) / 1e12
+    fwd_bwd_tf = f_step / (sum(phase_ms) / 1e3) / 1e12
+    # The dominant kernel (largest share of the step) gets the roofline entry.
+    kernels = {"fa_fwd": (phase_ms[0], f_fwd), "fa_bwd_main": (phase_ms[2], f_bwd)}
+    dom = max(kernels, key=lambda kk: kernels[kk][0])
+    dom_ms, dom_flops = kernels[dom]
+    achieved = dom_flops / (dom_ms / 1e3) / 1e12
+    # Each kernel is timed inside a long back-to-back step: sustained peak.
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": sustained, "unit": UNIT,
+                "frac": achieved / sustained, "traffic": profiled_traffic(dom, name),
+                "peak_kind": f"{peak_kind} sustained dense bf16 (MEASURED_PEAKS.json)",
+                "avg_launch_ms": dom_ms}
+    other = "fa_fwd" if dom == "fa_bwd_main" else "fa_bwd_main"
+    o_ms, o_fl = kernels[other]
+    roofline_other = {"bound": "tensor", "kernel": other, "achieved": o_fl / (o_ms / 1e3) / 1e12,
+                      "peak": sustained, "unit": UNIT, "frac": o_fl / (o_ms / 1e3) / 1e12 / sustained,
+                      "traffic": profiled_traffic(other, name), "avg_launch_ms": o_ms}
+
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": (value / PAGES_FWD_BWD_TFLOPS[name]) if name in PAGES_FWD_BWD_TFLOPS else None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": name, "B": B, "H": H, "N": N, "d": d, "causal": causal,
+                   "l2": "inputs larger than L2 (Q, K, V, dO and outputs exceed 129 MB per step)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf, "bwd_main_tflops": main_tf, "fwd_bwd_tflops": fwd_bwd_tf,
+        "pct_of_peak": {"fwd": fwd_tf / burst, "fwd_bwd": fwd_bwd_tf / burst, "peak_tflops": burst,
+                        "peak_kind": f"{peak_kind} burst dense bf16 (MEASURED_PEAKS.json)"},
+        "phase_ms": {"fwd": phase_ms[0], "bwd_pre": phase_ms[1], "bwd_main": phase_ms[2], "bwd_post": phase_ms[3]},
+        "roofline": roofline, "roofline_secondary": roofline_other,
+        "e2e": {"value": aggregate_value(f_step, world, e2e_s), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clk,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        xs = make_inputs(1, 1, N, d, seed_for(p))
+        rows = calibrate_rows(p, xs, 4.0)
+        t1, _ = oracle_sample(p, xs, rows, 1)
+        calls = max(1, int(round(12.0 / max(t1, 1e-3))))  # about 12 s of CPU work
+        t, fl = oracle_sample(p, xs, rows, calls)
+        result["cpu_baseline"] = {
+            "value": fl / t / 1e12, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+            "sample": (f"{calls} x float64 oracle forward+backward of {rows} query rows x all {N} keys of one head "
+                       f"({t:.1f} s); FLOPs by the same convention as the GPU number")}
+    return result
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(all_workloads()))
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle sample (profiling runs)")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    p = all_workloads()[args.workload]
+    world, rank, local = dist_env()
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, p, args.workload)), flush=True)
+        return 0
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    try:
+        res = run_ours(args, p, args.workload, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+    if res is not None:
+        print(json.dumps(res), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

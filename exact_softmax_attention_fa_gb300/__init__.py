@@ -15,7 +15,7 @@ import math
 
 from ._lib import load, check, FAError, header_functions, STATUS_NAMES  # noqa: F401
 
-__all__ = ["fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_get_device_status", "fa_set_wait_limit_ns",
+__all__ = ["fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_postprocess", "fa_get_device_status", "fa_set_wait_limit_ns",
            "fa_debug_timeout_probe", "forward", "backward", "FAError", "flops"]
 
 _SUPPORTED_D = (64, 128, 256)
@@ -83,12 +83,47 @@ def fa_bwd(q, k, v, o, lse, do, dq, dk, dv, causal: bool, scale: float, workspac
     _check_lse(lse, shape)
     B, H, N, d = shape
     lib = load()
-    ws_ptr = workspace.data_ptr() if workspace is not None else 0
-    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     check("fa_bwd", lib.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
                                do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
-                               B, H, N, d, int(bool(causal)), float(scale), ws_ptr, ws_bytes,
+                               B, H, N, d, int(bool(causal)), float(scale), *_ws(workspace),
                                _stream_handle(stream)))
+
+
+def _ws(workspace):
+    if workspace is None:
+        return 0, 0
+    return workspace.data_ptr(), workspace.numel() * workspace.element_size()
+
+
+def fa_bwd_preprocess(o, lse, do, workspace, stream=None) -> None:
+    """First phase of fa_bwd: D, base-2 L and a zeroed dQ accumulator in `workspace`."""
+    shape = _dims(o)
+    _check_bf16("o", o, shape)
+    _check_bf16("do", do, shape)
+    _check_lse(lse, shape)
+    B, H, N, d = shape
+    check("fa_bwd_preprocess", load().fa_bwd_preprocess(o.data_ptr(), lse.data_ptr(), do.data_ptr(), B, H, N, d,
+                                                        *_ws(workspace), _stream_handle(stream)))
+
+
+def fa_bwd_main(q, k, v, do, dk, dv, causal: bool, scale: float, workspace, stream=None) -> None:
+    """Second phase of fa_bwd: dk, dv, and dQ accumulated into `workspace`."""
+    shape = _dims(q)
+    for name, t in (("q", q), ("k", k), ("v", v), ("do", do), ("dk", dk), ("dv", dv)):
+        _check_bf16(name, t, shape)
+    B, H, N, d = shape
+    check("fa_bwd_main", load().fa_bwd_main(q.data_ptr(), k.data_ptr(), v.data_ptr(), do.data_ptr(), dk.data_ptr(),
+                                            dv.data_ptr(), B, H, N, d, int(bool(causal)), float(scale),
+                                            *_ws(workspace), _stream_handle(stream)))
+
+
+def fa_bwd_postprocess(dq, workspace, stream=None) -> None:
+    """Last phase of fa_bwd: dq = bf16(dQ accumulator)."""
+    shape = _dims(dq)
+    _check_bf16("dq", dq, shape)
+    B, H, N, d = shape
+    check("fa_bwd_postprocess", load().fa_bwd_postprocess(dq.data_ptr(), B, H, N, d, *_ws(workspace),
+                                                          _stream_handle(stream)))
 
 
 def fa_get_device_status(stream=None) -> int:

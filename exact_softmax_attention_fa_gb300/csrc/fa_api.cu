@@ -217,6 +217,63 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
   return bwd_layout(static_cast<long long>(B) * H, N, d).total;
 }
 
+}  // extern "C"
+
+namespace {
+
+// Validation and launch-argument setup shared by fa_bwd and its phases. A
+// null entry in `need` means the phase does not use that tensor.
+struct BwdTensors {
+  const void *q, *k, *v, *o, *dO;
+  const float* lse;
+  void *dq, *dk, *dv;
+};
+
+fa_status_t prepare_bwd(const BwdTensors& t, int B, int H, int N, int d, int causal, float scale, void* workspace,
+                        size_t workspace_bytes, bool* empty, BwdLaunch* a) {
+  fa_status_t st = check_common(B, H, N, d, causal, scale, empty);
+  if (st != FA_OK || *empty) return st;
+  const void* bf16_ptrs[] = {t.q, t.k, t.v, t.o, t.dO, t.dq, t.dk, t.dv};
+  for (const void* p : bf16_ptrs)
+    if (p && !aligned(p, 16)) return FA_ERR_MISALIGNED;
+  if (t.lse && !aligned(t.lse, 4)) return FA_ERR_MISALIGNED;
+  const int BH = B * H;
+  const BwdWorkspaceLayout wl = bwd_layout(BH, N, d);
+  if (!workspace || workspace_bytes < wl.total) return FA_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return FA_ERR_MISALIGNED;
+  if (d == 256) return FA_ERR_UNSUPPORTED;  // d = 256 backward kernel not built yet
+  DeviceState* ds = device_state(&st);
+  if (!ds) return st;
+  *a = BwdLaunch{};
+  auto map = [&](CUtensorMap* m, const void* ptr) { return !ptr || make_map(m, ptr, BH, N, d); };
+  if (!map(&a->tmQ, t.q) || !map(&a->tmK, t.k) || !map(&a->tmV, t.v) || !map(&a->tmdO, t.dO) ||
+      !map(&a->tmdK, t.dk) || !map(&a->tmdV, t.dv))
+    return FA_ERR_CUDA;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  a->o = static_cast<const __nv_bfloat16*>(t.o);
+  a->dO = static_cast<const __nv_bfloat16*>(t.dO);
+  a->lse = t.lse;
+  a->dq = static_cast<__nv_bfloat16*>(t.dq);
+  a->D = reinterpret_cast<float*>(ws + wl.D_off);
+  a->lse2 = reinterpret_cast<float*>(ws + wl.lse2_off);
+  a->dq_acc = reinterpret_cast<float*>(ws + wl.dq_off);
+  a->status = ds->status;
+  a->N = N;
+  a->Npad = round_up_128(N);
+  a->BH = BH;
+  a->d = d;
+  a->causal = causal;
+  a->scale = scale;
+  a->scale_log2 = static_cast<float>(static_cast<double>(scale) * kLog2e);
+  a->wait_limit_ns = g_wait_limit_ns.load();
+  a->num_sms = ds->num_sms;
+  return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
 fa_status_t fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
                    void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal, float scale,
                    void* workspace, size_t workspace_bytes, cudaStream_t stream) {
@@ -225,39 +282,57 @@ fa_status_t fa_bwd(const void* q, const void* k, const void* v, const void* o, c
   if (st != FA_OK) return st;
   if (empty) return FA_OK;
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
-  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(dO, 16) ||
-      !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4))
-    return FA_ERR_MISALIGNED;
-  if (d == 256) return FA_ERR_UNSUPPORTED;  // d = 256 backward kernel not built yet
-  const int BH = B * H;
-  const BwdWorkspaceLayout wl = bwd_layout(BH, N, d);
-  if (!workspace || workspace_bytes < wl.total) return FA_ERR_WORKSPACE;
-  if (!aligned(workspace, 256)) return FA_ERR_MISALIGNED;
-  DeviceState* ds = device_state(&st);
-  if (!ds) return st;
-  BwdLaunch a{};
-  if (!make_map(&a.tmQ, q, BH, N, d) || !make_map(&a.tmK, k, BH, N, d) || !make_map(&a.tmV, v, BH, N, d) ||
-      !make_map(&a.tmdO, dO, BH, N, d) || !make_map(&a.tmdK, dk, BH, N, d) || !make_map(&a.tmdV, dv, BH, N, d))
-    return FA_ERR_CUDA;
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  a.o = static_cast<const __nv_bfloat16*>(o);
-  a.dO = static_cast<const __nv_bfloat16*>(dO);
-  a.lse = lse;
-  a.dq = static_cast<__nv_bfloat16*>(dq);
-  a.D = reinterpret_cast<float*>(ws + wl.D_off);
-  a.lse2 = reinterpret_cast<float*>(ws + wl.lse2_off);
-  a.dq_acc = reinterpret_cast<float*>(ws + wl.dq_off);
-  a.status = ds->status;
-  a.N = N;
-  a.Npad = round_up_128(N);
-  a.BH = BH;
-  a.d = d;
-  a.causal = causal;
-  a.scale = scale;
-  a.scale_log2 = static_cast<float>(static_cast<double>(scale) * kLog2e);
-  a.wait_limit_ns = g_wait_limit_ns.load();
-  a.num_sms = ds->num_sms;
-  return from_cuda(launch_bwd(a, stream));
+  BwdLaunch a;
+  st = prepare_bwd(BwdTensors{q, k, v, o, dO, lse, dq, dk, dv}, B, H, N, d, causal, scale, workspace,
+                   workspace_bytes, &empty, &a);
+  if (st != FA_OK || empty) return st;
+  cudaError_t e = launch_bwd_pre(a, stream);
+  if (e == cudaSuccess) e = launch_bwd_main(a, stream);
+  if (e == cudaSuccess) e = launch_bwd_post(a, stream);
+  return from_cuda(e);
+}
+
+fa_status_t fa_bwd_preprocess(const void* o, const float* lse, const void* dO, int B, int H, int N, int d,
+                              void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  bool empty = false;
+  fa_status_t st = check_common(B, H, N, d, 0, 1.0f, &empty);
+  if (st != FA_OK) return st;
+  if (empty) return FA_OK;
+  if (!o || !lse || !dO) return FA_ERR_INVALID_ARG;
+  BwdLaunch a;
+  st = prepare_bwd(BwdTensors{nullptr, nullptr, nullptr, o, dO, lse, nullptr, nullptr, nullptr}, B, H, N, d, 0, 1.0f,
+                   workspace, workspace_bytes, &empty, &a);
+  if (st != FA_OK || empty) return st;
+  return from_cuda(launch_bwd_pre(a, stream));
+}
+
+fa_status_t fa_bwd_main(const void* q, const void* k, const void* v, const void* dO, void* dk, void* dv, int B,
+                        int H, int N, int d, int causal, float scale, void* workspace, size_t workspace_bytes,
+                        cudaStream_t stream) {
+  bool empty = false;
+  fa_status_t st = check_common(B, H, N, d, causal, scale, &empty);
+  if (st != FA_OK) return st;
+  if (empty) return FA_OK;
+  if (!q || !k || !v || !dO || !dk || !dv) return FA_ERR_INVALID_ARG;
+  BwdLaunch a;
+  st = prepare_bwd(BwdTensors{q, k, v, nullptr, dO, nullptr, nullptr, dk, dv}, B, H, N, d, causal, scale, workspace,
+                   workspace_bytes, &empty, &a);
+  if (st != FA_OK || empty) return st;
+  return from_cuda(launch_bwd_main(a, stream));
+}
+
+fa_status_t fa_bwd_postprocess(void* dq, int B, int H, int N, int d, void* workspace, size_t workspace_bytes,
+                               cudaStream_t stream) {
+  bool empty = false;
+  fa_status_t st = check_common(B, H, N, d, 0, 1.0f, &empty);
+  if (st != FA_OK) return st;
+  if (empty) return FA_OK;
+  if (!dq) return FA_ERR_INVALID_ARG;
+  BwdLaunch a;
+  st = prepare_bwd(BwdTensors{nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, dq, nullptr, nullptr}, B, H, N,
+                   d, 0, 1.0f, workspace, workspace_bytes, &empty, &a);
+  if (st != FA_OK || empty) return st;
+  return from_cuda(launch_bwd_post(a, stream));
 }
 
 fa_status_t fa_get_device_status(cudaStream_t stream) {

@@ -505,41 +505,56 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
   if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
 }
 
-template <int HD, bool CAUSAL>
-cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t stream) {
-  using C = BwdCfg<HD>;
+template <int HD>
+cudaError_t launch_pre_t(const BwdLaunch& a, cudaStream_t stream) {
   const long long rows = static_cast<long long>(a.BH) * a.Npad;
-  {
-    constexpr int RPB = 8 * (32 / (HD / 8));  // rows per 256-thread block
-    const long long blocks = (rows + RPB - 1) / RPB;
-    bwd_pre_kernel<HD><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a.o, a.dO, a.lse, a.D, a.lse2, a.dq_acc,
-                                                                          a.N, a.Npad, rows);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
-  {
-    auto kern = fa_bwd_kernel<HD, CAUSAL>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    const int T = (a.N + 127) / 128;
-    kern<<<static_cast<unsigned>(static_cast<long long>(a.BH) * T), kThreads, C::SMEM_BYTES, stream>>>(a);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
-  {
-    const long long vec = static_cast<long long>(a.BH) * a.N * (HD / 8);
-    bwd_post_kernel<HD><<<static_cast<unsigned>((vec + 255) / 256), 256, 0, stream>>>(a.dq_acc, a.dq, a.N, a.Npad,
-                                                                                      vec);
-    return cudaGetLastError();
-  }
+  constexpr int RPB = 8 * (32 / (HD / 8));  // rows per 256-thread block
+  const long long blocks = (rows + RPB - 1) / RPB;
+  bwd_pre_kernel<HD><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a.o, a.dO, a.lse, a.D, a.lse2, a.dq_acc, a.N,
+                                                                        a.Npad, rows);
+  return cudaGetLastError();
+}
+
+template <int HD, bool CAUSAL>
+cudaError_t launch_main_t(const BwdLaunch& a, cudaStream_t stream) {
+  using C = BwdCfg<HD>;
+  auto kern = fa_bwd_kernel<HD, CAUSAL>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  const int T = (a.N + 127) / 128;
+  kern<<<static_cast<unsigned>(static_cast<long long>(a.BH) * T), kThreads, C::SMEM_BYTES, stream>>>(a);
+  return cudaGetLastError();
+}
+
+template <int HD>
+cudaError_t launch_post_t(const BwdLaunch& a, cudaStream_t stream) {
+  const long long vec = static_cast<long long>(a.BH) * a.N * (HD / 8);
+  bwd_post_kernel<HD><<<static_cast<unsigned>((vec + 255) / 256), 256, 0, stream>>>(a.dq_acc, a.dq, a.N, a.Npad, vec);
+  return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_bwd(const BwdLaunch& a, cudaStream_t stream) {
+cudaError_t launch_bwd_pre(const BwdLaunch& a, cudaStream_t stream) {
   switch (a.d) {
-    case 64: return a.causal ? launch_bwd_t<64, true>(a, stream) : launch_bwd_t<64, false>(a, stream);
-    case 128: return a.causal ? launch_bwd_t<128, true>(a, stream) : launch_bwd_t<128, false>(a, stream);
+    case 64: return launch_pre_t<64>(a, stream);
+    case 128: return launch_pre_t<128>(a, stream);
+    default: return cudaErrorNotSupported;
+  }
+}
+
+cudaError_t launch_bwd_main(const BwdLaunch& a, cudaStream_t stream) {
+  switch (a.d) {
+    case 64: return a.causal ? launch_main_t<64, true>(a, stream) : launch_main_t<64, false>(a, stream);
+    case 128: return a.causal ? launch_main_t<128, true>(a, stream) : launch_main_t<128, false>(a, stream);
+    default: return cudaErrorNotSupported;
+  }
+}
+
+cudaError_t launch_bwd_post(const BwdLaunch& a, cudaStream_t stream) {
+  switch (a.d) {
+    case 64: return launch_post_t<64>(a, stream);
+    case 128: return launch_post_t<128>(a, stream);
     default: return cudaErrorNotSupported;
   }
 }

@@ -94,6 +94,28 @@ fa_status_t fa_bwd(const void* q, const void* k, const void* v, const void* o, c
                    void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal, float scale,
                    void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * The three phases fa_bwd runs, in order, on one stream (each also callable on
+ * its own with the same sizes and workspace; fa_bwd == preprocess, main,
+ * postprocess). Arguments mean what they mean for fa_bwd.
+ *
+ * fa_bwd_preprocess: D_i = sum_k dO_ik O_ik (the row-wise correction that
+ *   reading note 5.3 precomputes before the block loops), the base-2 logsumexp
+ *   L_i * log2(e), and a zeroed fp32 dQ accumulator, all in the workspace.
+ *   Reads o, lse, dO. HBM-bound.
+ * fa_bwd_main: the block loops of reading note 5.3 (key blocks outer): writes
+ *   dk and dv, and adds every dS K_j into the workspace's dQ accumulator.
+ *   Reads q, k, v, dO and the preprocessed workspace.
+ * fa_bwd_postprocess: dq = bf16(dQ accumulator). HBM-bound.
+ */
+fa_status_t fa_bwd_preprocess(const void* o, const float* lse, const void* dO, int B, int H, int N, int d,
+                              void* workspace, size_t workspace_bytes, cudaStream_t stream);
+fa_status_t fa_bwd_main(const void* q, const void* k, const void* v, const void* dO, void* dk, void* dv, int B,
+                        int H, int N, int d, int causal, float scale, void* workspace, size_t workspace_bytes,
+                        cudaStream_t stream);
+fa_status_t fa_bwd_postprocess(void* dq, int B, int H, int N, int d, void* workspace, size_t workspace_bytes,
+                               cudaStream_t stream);
+
 /* Static, human-readable name of a status code. */
 const char* fa_status_string(fa_status_t status);
 

@@ -11,6 +11,7 @@ from .attention import (  # noqa: F401
     attention_forward,
     attention_forward_rows,
     attention_backward,
+    attention_fwd_bwd_rows,
     attention_probabilities,
     tiled_forward,
     tiled_backward,

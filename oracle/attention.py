@@ -25,6 +25,8 @@ What is computed, per (batch, head), for Q, K, V in R^{N x d}:
 
 attention_forward / attention_backward are the plain definitions: S and P are
 materialised (in chunks of query rows, which changes nothing but memory use).
+attention_fwd_bwd_rows restates both for a block of query rows of one head
+(pinned by summing blocks back to the full result).
 tiled_forward / tiled_backward are a second, separately written restatement of
 the blocked algorithm (unscaled accumulator with running max and sum, then the
 column-block-outer backward with D = rowsum(dO o O)); the tests use them to
@@ -148,6 +150,27 @@ def attention_backward(q, k, v, do, causal, scale, heads=None):
             dq[b, h, rows] = scale * (ds @ k[b, h])
             dk[b, h] += scale * (ds.T @ q[b, h, rows])
     return dq, dk, dv
+
+
+def attention_fwd_bwd_rows(q_bh, k_bh, v_bh, do_bh, rows, causal, scale):
+    """Forward and backward restricted to a block of query rows of ONE head.
+
+    Returns (O_rows, L_rows, dQ_rows, dK_part, dV_part): the outputs and dQ of
+    those rows, and their additive contributions to dK and dV. Summing the
+    parts over a partition of the rows gives attention_backward's dK and dV;
+    this is how a bounded CPU sample of a large workload is timed.
+    """
+    q_bh, k_bh, v_bh, do_bh = (np.asarray(a, dtype=np.float64) for a in (q_bh, k_bh, v_bh, do_bh))
+    rows = np.asarray(rows, dtype=np.int64)
+    p, lse = softmax_rows(_scores(q_bh[rows], k_bh, rows, causal, scale))
+    o = p @ v_bh
+    do_rows = do_bh[rows]
+    dv_part = p.T @ do_rows
+    dp = do_rows @ v_bh.T
+    ds = p * (dp - np.sum(p * dp, axis=1, keepdims=True))
+    dq = scale * (ds @ k_bh)
+    dk_part = scale * (ds.T @ q_bh[rows])
+    return o, lse, dq, dk_part, dv_part
 
 
 def tiled_forward(q, k, v, causal, scale, block_rows, block_cols):

@@ -146,6 +146,26 @@ def test_row_sampled_forward_matches_full():
         np.testing.assert_allclose(l_r, lse[0, 0, rows], atol=1e-14)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_row_block_parts_sum_to_full(causal):
+    q, k, v = qkv(1, 1, 70, 5, 24)
+    do = rand(q.shape, 25)
+    o, lse = oracle.attention_forward(q, k, v, causal, 0.3)
+    dq, dk, dv = oracle.attention_backward(q, k, v, do, causal, 0.3)
+    dk_sum = np.zeros_like(dk[0, 0])
+    dv_sum = np.zeros_like(dv[0, 0])
+    for rows in (np.arange(0, 23), np.arange(23, 64), np.arange(64, 70)):
+        o_r, l_r, dq_r, dk_p, dv_p = oracle.attention_fwd_bwd_rows(q[0, 0], k[0, 0], v[0, 0], do[0, 0], rows,
+                                                                   causal, 0.3)
+        np.testing.assert_allclose(o_r, o[0, 0, rows], atol=1e-14)
+        np.testing.assert_allclose(l_r, lse[0, 0, rows], atol=1e-14)
+        np.testing.assert_allclose(dq_r, dq[0, 0, rows], atol=1e-13)
+        dk_sum += dk_p
+        dv_sum += dv_p
+    np.testing.assert_allclose(dk_sum, dk[0, 0], atol=1e-13)
+    np.testing.assert_allclose(dv_sum, dv[0, 0], atol=1e-13)
+
+
 def test_backward_head_subset():
     q, k, v = qkv(2, 2, 9, 3, 14)
     do = rand(q.shape, 15)
