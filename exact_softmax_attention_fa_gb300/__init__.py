@@ -15,7 +15,7 @@ import math
 
 from ._lib import load, check, FAError, header_functions, STATUS_NAMES  # noqa: F401
 
-__all__ = ["fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_postprocess", "fa_get_device_status", "fa_set_wait_limit_ns",
+__all__ = ["fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_postprocess", "fa_bwd_noalloc", "fa_get_device_status", "fa_set_wait_limit_ns",
            "fa_debug_timeout_probe", "forward", "backward", "FAError", "flops"]
 
 _SUPPORTED_D = (64, 128, 256)
@@ -124,6 +124,29 @@ def fa_bwd_postprocess(dq, workspace, stream=None) -> None:
     B, H, N, d = shape
     check("fa_bwd_postprocess", load().fa_bwd_postprocess(dq.data_ptr(), B, H, N, d, *_ws(workspace),
                                                           _stream_handle(stream)))
+
+
+# Scratch size compiled into the library for fa_bwd_noalloc (include/fa.h).
+FA_BWD_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
+
+
+def fa_bwd_noalloc(q, k, v, o, lse, do, dq, dk, dv, causal: bool, scale: float, stream=None) -> None:
+    """fa_bwd without a caller workspace: the library's fixed scratch array is used.
+
+    For callers that are given only input and output buffers and cannot
+    allocate device memory. Sizes whose workspace exceeds
+    FA_BWD_NOALLOC_SCRATCH_BYTES raise FAError(FA_ERR_WORKSPACE). Calls that
+    overlap on the GPU share the array and race.
+    """
+    shape = _dims(q)
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do), ("dq", dq), ("dk", dk), ("dv", dv)):
+        _check_bf16(name, t, shape)
+    _check_lse(lse, shape)
+    B, H, N, d = shape
+    check("fa_bwd_noalloc", load().fa_bwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                                  lse.data_ptr(), do.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                                  dv.data_ptr(), B, H, N, d, int(bool(causal)), float(scale),
+                                                  _stream_handle(stream)))
 
 
 def fa_get_device_status(stream=None) -> int:

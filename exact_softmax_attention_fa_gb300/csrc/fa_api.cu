@@ -358,3 +358,45 @@ fa_status_t fa_debug_timeout_probe(unsigned long long limit_ns, cudaStream_t str
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free backward: a fixed scratch array compiled into the library
+// stands in for the caller's workspace.
+// ---------------------------------------------------------------------------
+namespace fa {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[FA_BWD_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+struct NoAllocState {
+  std::once_flag once;
+  cudaError_t error = cudaSuccess;
+  void* scratch = nullptr;  // device address of g_noalloc_scratch on this device
+};
+NoAllocState g_noalloc[kMaxDevices];
+
+}  // namespace
+}  // namespace fa
+
+extern "C" fa_status_t fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                                      const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                                      int causal, float scale, cudaStream_t stream) {
+  bool empty = false;
+  fa_status_t st = check_common(B, H, N, d, causal, scale, &empty);
+  if (st != FA_OK) return st;
+  if (empty) return FA_OK;
+  if (fa_bwd_workspace_size(B, H, N, d) > FA_BWD_NOALLOC_SCRATCH_BYTES) return FA_ERR_WORKSPACE;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+  NoAllocState& ns = g_noalloc[dev];
+  // Once per device, with that device current: the array's device address.
+  // In host code the symbol itself is only a host-side stand-in.
+  std::call_once(ns.once, [&ns] {
+    ns.error = cudaGetSymbolAddress(&ns.scratch, g_noalloc_scratch);
+  });
+  if (ns.error != cudaSuccess || ns.scratch == nullptr) return FA_ERR_CUDA;
+  return fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, causal, scale, ns.scratch,
+                FA_BWD_NOALLOC_SCRATCH_BYTES, stream);
+}
+

@@ -116,6 +116,39 @@ fa_status_t fa_bwd_main(const void* q, const void* k, const void* v, const void*
 fa_status_t fa_bwd_postprocess(void* dq, int B, int H, int N, int d, void* workspace, size_t workspace_bytes,
                                cudaStream_t stream);
 
+/*
+ * Backward pass for callers that cannot allocate device memory. This entry
+ * point has no counterpart in the paper; it is a convenience of this library.
+ *
+ * Some callers are handed only their input and output buffers and have no
+ * allocator of their own: plugin hooks of inference engines and runtimes that
+ * plan every device byte up front and forbid allocations afterwards, or code
+ * that must not call cudaMalloc because it can synchronise the device and
+ * stall other work. fa_bwd needs a caller-provided workspace; this variant
+ * instead uses a scratch array compiled into the library (a file-scope
+ * __device__ array of FA_BWD_NOALLOC_SCRATCH_BYTES, which every GPU that
+ * loads the library holds until the process exits).
+ *
+ *   Arguments and results are those of fa_bwd, minus the workspace.
+ *   Problems whose workspace (fa_bwd_workspace_size) exceeds
+ *   FA_BWD_NOALLOC_SCRATCH_BYTES are rejected with FA_ERR_WORKSPACE before
+ *   any GPU work; use fa_bwd with your own workspace for those.
+ *   The call allocates nothing: no cudaMalloc/cudaFree and no allocating
+ *   library routine.
+ *   The first call on a device looks up the scratch array's device address
+ *   (once per device, with that device current); make that first call
+ *   before any stream capture.
+ *   All calls share the one array per device. Each call re-initialises the
+ *   parts that must start at zero, so a call never sees the previous call's
+ *   values, but calls that overlap on the GPU (different streams or
+ *   threads without ordering between them) race on the array and give wrong
+ *   results.
+ */
+#define FA_BWD_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+fa_status_t fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                           const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal,
+                           float scale, cudaStream_t stream);
+
 /* Static, human-readable name of a status code. */
 const char* fa_status_string(fa_status_t status);
 

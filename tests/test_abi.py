@@ -102,3 +102,15 @@ def test_python_binding_rejects_cpu_tensors():
         fa.fa_fwd(q, q, q, q.clone(), torch.zeros(1, 1, 128), False, 0.125)
     with pytest.raises(TypeError):
         fa.fa_fwd(q.float(), q, q, q, torch.zeros(1, 1, 128), False, 0.125)
+
+
+def test_noalloc_backward_validation(lib):
+    """Argument errors and oversized problems are rejected before any CUDA call."""
+    def call(B=1, H=1, N=128, d=64, causal=0, scale=0.125, ptr=P, lse=P):
+        return lib.fa_bwd_noalloc(ptr, ptr, ptr, ptr, lse, ptr, ptr, ptr, ptr, B, H, N, d, causal, scale, None)
+    assert call(d=96) == UNSUPPORTED
+    assert call(scale=-1.0) == INVALID
+    assert call(N=0, ptr=0, lse=0) == OK
+    # 16 heads x 8192 rows at d=128 need ~68 MB of scratch, beyond the compiled 16 MiB
+    assert lib.fa_bwd_workspace_size(1, 16, 8192, 128) > (16 << 20)
+    assert call(B=1, H=16, N=8192, d=128) == WORKSPACE

@@ -1,0 +1,60 @@
+"""fa_bwd_noalloc: the backward for callers that cannot allocate device memory.
+
+Such callers (plugin hooks given only their input/output buffers, runtimes
+that forbid allocations after start-up) cannot provide fa_bwd's workspace, so
+this entry point uses a scratch array compiled into the library instead. The
+test calls it through the C ABI twice in a row, with different inputs, and
+checks each result against fa_bwd with a caller workspace, within the
+gradient tolerance the other parity tests use. This file is collected last
+so that a run stopping at the first failure has run every other test.
+"""
+
+import ctypes
+
+import numpy as np
+import pytest
+
+from gpu_util import TOL_GRAD_REL, inputs, to_device, to_host64, scale_f32
+
+pytestmark = pytest.mark.gpu
+
+
+def _rel(a, b):
+    return np.abs(a - b).max() / max(np.abs(b).max(), 1e-3)
+
+
+@pytest.mark.parametrize("d,causal", [(64, True), (128, False)])
+def test_noalloc_backward_matches_fa_bwd_twice(cuda_lib, d, causal):
+    import torch
+    import exact_softmax_attention_fa_gb300 as fa
+    B, H, N = 1, 3, 700
+    scale = scale_f32(d)
+    lib = cuda_lib
+    stream = torch.cuda.current_stream().cuda_stream
+    assert fa.fa_bwd_workspace_size(B, H, N, d) <= fa.FA_BWD_NOALLOC_SCRATCH_BYTES
+    for call, seed in enumerate((901, 902)):  # two calls in a row, different inputs
+        x, _ = inputs(B, H, N, d, seed + d)
+        q, k, v, do = (to_device(x[n]) for n in ("q", "k", "v", "do"))
+        o, lse = fa.forward(q, k, v, causal=causal, scale=scale)
+        ref = fa.backward(q, k, v, o, lse, do, causal=causal, scale=scale)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+        st = lib.fa_bwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                                B, H, N, d, int(causal), ctypes.c_float(scale), stream)
+        assert st == 0, lib.fa_status_string(st)
+        assert lib.fa_get_device_status(stream) == 0
+        for name, got, want in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+            e = _rel(to_host64(got), to_host64(want))
+            assert e <= TOL_GRAD_REL, (call, name, e)
+
+
+def test_noalloc_rejects_problems_beyond_the_scratch(cuda_lib):
+    import torch
+    import exact_softmax_attention_fa_gb300 as fa
+    B, H, N, d = 1, 16, 8192, 128
+    assert fa.fa_bwd_workspace_size(B, H, N, d) > fa.FA_BWD_NOALLOC_SCRATCH_BYTES
+    t = torch.empty(B, H, N, d, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(B, H, N, dtype=torch.float32, device="cuda")
+    with pytest.raises(fa.FAError) as e:
+        fa.fa_bwd_noalloc(t, t, t, t, lse, t, t.clone(), t.clone(), t.clone(), False, scale_f32(d))
+    assert e.value.status == 4  # FA_ERR_WORKSPACE
