@@ -60,15 +60,17 @@ struct BwdCfg {
   static constexpr int DS_BYTES = 128 * 128 * 2;
   static constexpr uint32_t DK_COL = 0;
   static constexpr uint32_t DV_COL = HD;
-  __host__ __device__ static constexpr uint32_t region(int r) { return 256u + 128u * uint32_t(r); }
-  // smem: K_j, V_j, QST x (Q_i, dO_i), dS^T
-  static constexpr int SMEM_BYTES = (2 + 2 * QST) * TILE_BYTES + DS_BYTES + 1024;
+  static constexpr uint32_t REG_A = 256;  // S^T, then P^T (bf16)
+  static constexpr uint32_t REG_B = 384;  // dP^T, then dQ_i
+  static constexpr int LD_BYTES = 2 * 128 * 4;  // per warpgroup: 64 base-2 L + 64 scaled D
+  // smem: K_j, V_j, QST x (Q_i, dO_i), dS^T, L/D staging
+  static constexpr int SMEM_BYTES = (2 + 2 * QST) * TILE_BYTES + DS_BYTES + LD_BYTES + 1024;
 };
 
 struct BwdShared {
   uint64_t kv_full;
   uint64_t qdo_full[4], qdo_empty[4];
-  uint64_t sdp_full, ds_ready, pv_done, dq_full, dq_free, acc_done;
+  uint64_t s_full, dp_full, pa_ready, ds_ready, pv_done, dq_full, dq_free, acc_done;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -224,6 +226,13 @@ __device__ void bwd_load_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sK, ui
   mbar_wait(&sh.kv_full, 0, &zero, p.wait_limit_ns);
 }
 
+// One thread issues every MMA. Per query tile n (regions A = S^T then P^T,
+// B = dP^T then dQ_i):
+//   dV += P^T dO_n       after phase A(n)           (overlaps phase B(n))
+//   dK += dS^T Q_n       after phase B(n)
+//   dQ_n = dS K_j -> B   after phase B(n)
+//   S^T(n+1) -> A        after dV(n) released P^T   (overlaps the dQ drain)
+//   dP^T(n+1) -> B       after the dQ drain         (overlaps phase A(n+1))
 template <int HD, bool CAUSAL>
 __device__ void bwd_mma_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sK, uint8_t* sV, uint8_t* sQ,
                              uint8_t* sdO, uint8_t* sDS, uint32_t tmem, const BwdWork<CAUSAL>& wk) {
@@ -252,53 +261,58 @@ __device__ void bwd_mma_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sK, uin
     return;
   }
   tc_fence_after_sync();
-  issue_sq(C::region(0), k_addr, q_addr);   // S^T(i0)
-  issue_sq(C::region(1), v_addr, do_addr);  // dP^T(i0)
-  umma_commit(&sh.sdp_full);
+  issue_sq(C::REG_A, k_addr, q_addr);  // S^T(i0)
+  umma_commit(&sh.s_full);
+  issue_sq(C::REG_B, v_addr, do_addr);  // dP^T(i0)
+  umma_commit(&sh.dp_full);
 
   for (int n = 0; n < n_iter; ++n) {
     const int s = n % C::QST;
-    const uint32_t sreg = C::region(n & 1), dpreg = C::region((n + 1) & 1);
     const uint32_t qa = q_addr + s * C::TILE_BYTES, doa = do_addr + s * C::TILE_BYTES;
+    if (!mbar_wait(&sh.pa_ready, n & 1, &sh.abort_flag, lim)) return fail();
+    tc_fence_after_sync();
+    // dV += P^T dO_n; P^T (bf16) sits in columns [0,32) and [64,96) of region A
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks)
+      umma_ts(tmem + C::DV_COL, tmem + C::REG_A + (ks >> 2) * 64 + (ks & 3) * 8,
+              make_smem_desc_sw128(doa + ks * 2048, C::CHUNK_BYTES, 1024), kIdescAcc, (n > 0 || ks > 0) ? 1u : 0u);
+    umma_commit(&sh.pv_done);
     if (!mbar_wait(&sh.ds_ready, n & 1, &sh.abort_flag, lim)) return fail();
     tc_fence_after_sync();
-    // dV += P^T dO_i  (P^T bf16 in TMEM at dpreg)
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks)
-      umma_ts(tmem + C::DV_COL, tmem + dpreg + ks * 8, make_smem_desc_sw128(doa + ks * 2048, C::CHUNK_BYTES, 1024),
-              kIdescAcc, (n > 0 || ks > 0) ? 1u : 0u);
-    umma_commit(&sh.pv_done);
-    // dQ_i = dS K_j into sreg (queries on lanes)
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks)
-      umma_ss(tmem + sreg, make_smem_desc_sw128(ds_addr + ks * 2048, C::CHUNK_BYTES, 1024),
-              make_smem_desc_sw128(k_addr + ks * 2048, C::CHUNK_BYTES, 1024), kIdescDq, ks > 0 ? 1u : 0u);
-    umma_commit(&sh.dq_full);
-    // dK += dS^T Q_i
+    // dK += dS^T Q_n
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks)
       umma_ss(tmem + C::DK_COL, make_smem_desc_sw128(ds_addr + (ks >> 2) * C::CHUNK_BYTES + (ks & 3) * 32, 16, 1024),
               make_smem_desc_sw128(qa + ks * 2048, C::CHUNK_BYTES, 1024), kIdescAcc, (n > 0 || ks > 0) ? 1u : 0u);
+    // dQ_n = dS K_j into region B (queries on lanes)
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks)
+      umma_ss(tmem + C::REG_B, make_smem_desc_sw128(ds_addr + ks * 2048, C::CHUNK_BYTES, 1024),
+              make_smem_desc_sw128(k_addr + ks * 2048, C::CHUNK_BYTES, 1024), kIdescDq, ks > 0 ? 1u : 0u);
+    umma_commit(&sh.dq_full);
     umma_commit(&sh.qdo_empty[s]);
     if (n + 1 < n_iter) {
       const int s1 = (n + 1) % C::QST;
       if (!mbar_wait(&sh.qdo_full[s1], ((n + 1) / C::QST) & 1, &sh.abort_flag, lim)) return fail();
       if (!mbar_wait(&sh.pv_done, n & 1, &sh.abort_flag, lim)) return fail();
       tc_fence_after_sync();
-      issue_sq(dpreg, k_addr, q_addr + s1 * C::TILE_BYTES);  // S^T(i+1) over the consumed P^T(i)
+      issue_sq(C::REG_A, k_addr, q_addr + s1 * C::TILE_BYTES);  // S^T(n+1) over the consumed P^T(n)
+      umma_commit(&sh.s_full);
       if (!mbar_wait(&sh.dq_free, n & 1, &sh.abort_flag, lim)) return fail();
       tc_fence_after_sync();
-      issue_sq(sreg, v_addr, do_addr + s1 * C::TILE_BYTES);  // dP^T(i+1) over the drained dQ_i
-      umma_commit(&sh.sdp_full);
+      issue_sq(C::REG_B, v_addr, do_addr + s1 * C::TILE_BYTES);  // dP^T(n+1) over the drained dQ_n
+      umma_commit(&sh.dp_full);
     }
   }
   umma_commit(&sh.acc_done);
 }
 
-// Warpgroup 0: thread r owns key r of the tile.
+// Warpgroup w (w = 0, 1) owns query columns [64w, 64w + 64) of every tile;
+// thread r owns key r (TMEM lane r) for phases A and B and query r for the
+// dQ drain.
 template <int HD, bool CAUSAL>
-__device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS, uint32_t tmem,
-                                 const BwdWork<CAUSAL>& wk) {
+__device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS, float* sLD, uint32_t tmem,
+                                 int w, const BwdWork<CAUSAL>& wk) {
   using C = BwdCfg<HD>;
   const int r = threadIdx.x & 127;
   const uint32_t lane_base = static_cast<uint32_t>((threadIdx.x >> 5) & 3) << 21;
@@ -307,104 +321,137 @@ __device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS
   const float c2 = p.scale_log2;
   const float sc = p.scale;
   const uint64_t lim = p.wait_limit_ns;
-  const uint32_t ds_base = smem_u32(sDS);
-  const float* lse2_bh = p.lse2 + static_cast<size_t>(wk.bh) * p.Npad;
-  const float* D_bh = p.D + static_cast<size_t>(wk.bh) * p.Npad;
+  const uint32_t ds_chunk = smem_u32(sDS) + w * C::CHUNK_BYTES;  // queries 64w .. 64w+63
+  float* ld_l2 = sLD + w * 128;  // 64 base-2 logsumexps, then 64 scaled D values
+  float* ld_d = ld_l2 + 64;
+  const float* lse2_bh = p.lse2 + static_cast<size_t>(wk.bh) * p.Npad + 64 * w;
+  const float* D_bh = p.D + static_cast<size_t>(wk.bh) * p.Npad + 64 * w;
   const int n_iter = wk.n_iter();
+  const uint32_t bar_id = 1 + w;
+  bool alive = true;
+
+  // L2 / D of query tile i for this warpgroup's 64 columns: thread r < 64
+  // loads L2[r], thread r >= 64 loads D[r - 64] * scale.
+  auto fetch_ld = [&](int i) -> float {
+    return r < 64 ? __ldg(lse2_bh + i * 128 + r) : __ldg(D_bh + i * 128 + (r - 64)) * sc;
+  };
+  {
+    const float v = fetch_ld(wk.i0);
+    sLD[w * 128 + r] = v;
+    named_barrier_sync(bar_id, 128);
+  }
+
   for (int n = 0; n < n_iter; ++n) {
     const int i = wk.i0 + n;
-    const uint32_t tS = tmem + lane_base + C::region(n & 1);
-    const uint32_t tdP = tmem + lane_base + C::region((n + 1) & 1);
-    if (!__all_sync(0xffffffffu, mbar_wait(&sh.sdp_full, n & 1, &sh.abort_flag, lim))) {
-      record_timeout(p.status, &sh.abort_flag, WHERE_BWD_SOFTMAX);
-      return;
-    }
+    const uint32_t tA = tmem + lane_base + C::REG_A + 64 * w;
+    const uint32_t tB = tmem + lane_base + C::REG_B + 64 * w;
+    // ---- phase A: P^T = 2^(S^T * scale * log2e - L2), written back to TMEM as bf16
+    // After a timed-out wait the warp stops working but still passes every
+    // named barrier below, so the warpgroup's barrier counts stay matched.
+    alive = alive && __all_sync(0xffffffffu, mbar_wait(&sh.s_full, n & 1, &sh.abort_flag, lim));
+    if (!alive) record_timeout(p.status, &sh.abort_flag, WHERE_BWD_SOFTMAX);
     tc_fence_after_sync();
-    // Causal diagonal tile: query q sees key r only if q >= r.
-    const int q_lo = (CAUSAL && i == wk.j) ? r : 0;
-#pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
-      uint32_t sv[32], dpv[32];
-      tmem_ld32(tS + c * 32, sv);
-      tmem_ld32(tdP + c * 32, dpv);
-      const float* l2p = lse2_bh + i * 128 + c * 32;
-      const float* dp_ = D_bh + i * 128 + c * 32;
-      float l2[32], dd[32];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const float4 a = ldg_f4(l2p + 4 * k);
-        const float4 b = ldg_f4(dp_ + 4 * k);
-        l2[4 * k] = a.x, l2[4 * k + 1] = a.y, l2[4 * k + 2] = a.z, l2[4 * k + 3] = a.w;
-        dd[4 * k] = b.x * sc, dd[4 * k + 1] = b.y * sc, dd[4 * k + 2] = b.z * sc, dd[4 * k + 3] = b.w * sc;
-      }
+    float pv[64];
+    if (alive) {
+      uint32_t a[32], b[32];
+      tmem_ld32(tA, a);
+      tmem_ld32(tA + 32, b);
       tmem_ld_wait();
-      uint32_t ppk[16], dpk[16];
 #pragma unroll
-      for (int k = 0; k < 32; k += 2) {
-        const int q0 = c * 32 + k;
-        float p0 = ex2_approx(fmaf(__uint_as_float(sv[k]), c2, -l2[k]));
-        float p1 = ex2_approx(fmaf(__uint_as_float(sv[k + 1]), c2, -l2[k + 1]));
-        if (!key_valid || q0 < q_lo) p0 = 0.f;
-        if (!key_valid || q0 + 1 < q_lo) p1 = 0.f;
-        const float d0 = p0 * fmaf(__uint_as_float(dpv[k]), sc, -dd[k]);
-        const float d1 = p1 * fmaf(__uint_as_float(dpv[k + 1]), sc, -dd[k + 1]);
-        ppk[k / 2] = pack_bf16x2(p0, p1);
-        dpk[k / 2] = pack_bf16x2(d0, d1);
+      for (int c = 0; c < 32; ++c) {
+        pv[c] = __uint_as_float(a[c]);
+        pv[32 + c] = __uint_as_float(b[c]);
       }
-      // P^T chunk -> TMEM columns [16c, 16c + 16) of the dP region (already read)
-      tmem_st16(tdP + c * 16, ppk);
-      // dS^T chunk -> smem row r, queries 32c .. 32c + 31 (4 swizzled 16-byte units)
-      const uint32_t chunk_base = ds_base + (c >> 1) * C::CHUNK_BYTES;
+    }
+    // causal diagonal tile: query (64w + c) sees key r only if 64w + c >= r
+    const int c_lo = (CAUSAL && i == wk.j) ? r - 64 * w : 0;
+    if (alive) {
+    uint32_t pk[32];
+#pragma unroll
+    for (int c4 = 0; c4 < 64; c4 += 4) {
+      const float4 l = *reinterpret_cast<const float4*>(ld_l2 + c4);
+      const float lv[4] = {l.x, l.y, l.z, l.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int c = c4 + u;
+        float e = ex2_approx(fmaf(pv[c], c2, -lv[u]));
+        if (!key_valid || c < c_lo) e = 0.f;
+        pv[c] = e;
+      }
+      pk[c4 / 2] = pack_bf16x2(pv[c4], pv[c4 + 1]);
+      pk[c4 / 2 + 1] = pack_bf16x2(pv[c4 + 2], pv[c4 + 3]);
+    }
+    tmem_st32(tA, pk);  // columns [64w, 64w + 32): already read
+    tmem_st_wait();
+    tc_fence_before_sync();
+    mbar_arrive(&sh.pa_ready);
+    }
+
+    // ---- phase B: dS^T = P^T o (dP^T - D) * scale -> smem (bf16, swizzled)
+    alive = alive && __all_sync(0xffffffffu, mbar_wait(&sh.dp_full, n & 1, &sh.abort_flag, lim));
+    if (!alive) record_timeout(p.status, &sh.abort_flag, WHERE_BWD_SOFTMAX);
+    tc_fence_after_sync();
+    if (alive) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t dpv[32];
+      tmem_ld32(tB + 32 * h, dpv);
+      tmem_ld_wait();
+      uint32_t dk[16];
+#pragma unroll
+      for (int c4 = 0; c4 < 32; c4 += 4) {
+        const float4 dd = *reinterpret_cast<const float4*>(ld_d + 32 * h + c4);
+        const float dv4[4] = {dd.x, dd.y, dd.z, dd.w};
+        float ds[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) ds[u] = pv[32 * h + c4 + u] * fmaf(__uint_as_float(dpv[c4 + u]), sc, -dv4[u]);
+        dk[c4 / 2] = pack_bf16x2(ds[0], ds[1]);
+        dk[c4 / 2 + 1] = pack_bf16x2(ds[2], ds[3]);
+      }
 #pragma unroll
       for (int u = 0; u < 4; ++u)
-        st_shared_v4(chunk_base + sw128_offset(r, (c & 1) * 4 + u), dpk[4 * u], dpk[4 * u + 1], dpk[4 * u + 2],
-                     dpk[4 * u + 3]);
+        st_shared_v4(ds_chunk + sw128_offset(r, 4 * h + u), dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
     }
-    tmem_st_wait();
     fence_proxy_async_smem();
     tc_fence_before_sync();
     mbar_arrive(&sh.ds_ready);
-  }
-}
-
-// Warpgroup 1: thread q owns query row q of the current query tile.
-template <int HD, bool CAUSAL>
-__device__ void bwd_dq_role(const BwdLaunch& p, BwdShared& sh, uint32_t tmem, const BwdWork<CAUSAL>& wk) {
-  using C = BwdCfg<HD>;
-  const int q = threadIdx.x & 127;
-  const uint32_t lane_base = static_cast<uint32_t>((threadIdx.x >> 5) & 3) << 21;
-  const uint64_t lim = p.wait_limit_ns;
-  const int n_iter = wk.n_iter();
-  for (int n = 0; n < n_iter; ++n) {
-    const int i = wk.i0 + n;
-    if (!__all_sync(0xffffffffu, mbar_wait(&sh.dq_full, n & 1, &sh.abort_flag, lim))) {
-      record_timeout(p.status, &sh.abort_flag, WHERE_BWD_DQ);
-      return;
     }
+
+    // ---- next tile's L2 / D (latency hidden behind the dQ wait)
+    const bool has_next = n + 1 < n_iter;
+    const float next_ld = has_next ? fetch_ld(i + 1) : 0.f;
+
+    // ---- dQ drain: columns [w*HD/2, (w+1)*HD/2) of region B, query r
+    alive = alive && __all_sync(0xffffffffu, mbar_wait(&sh.dq_full, n & 1, &sh.abort_flag, lim));
+    if (!alive) record_timeout(p.status, &sh.abort_flag, WHERE_BWD_DQ);
     tc_fence_after_sync();
-    const uint32_t t = tmem + lane_base + C::region(n & 1);
-    float* dst = p.dq_acc + (static_cast<size_t>(wk.bh) * p.Npad + i * 128 + q) * HD;
+    if (alive) {
+      constexpr int HALF = HD / 2;
+      float* dst = p.dq_acc + (static_cast<size_t>(wk.bh) * p.Npad + i * 128 + r) * HD + w * HALF;
+      uint32_t v[HALF];
+      const uint32_t tq = tmem + lane_base + C::REG_B + w * HALF;
 #pragma unroll
-    for (int c = 0; c < HD; c += 32) {
-      uint32_t v[32];
-      tmem_ld32(t + c, v);
+      for (int c = 0; c < HALF; c += 32) tmem_ld32(tq + c, *reinterpret_cast<uint32_t(*)[32]>(v + c));
       tmem_ld_wait();
-      if (c + 32 >= HD) {  // last chunk read: the region can be reused
-        tc_fence_before_sync();
-        mbar_arrive(&sh.dq_free);
-      }
+      tc_fence_before_sync();
+      mbar_arrive(&sh.dq_free);
 #pragma unroll
-      for (int k = 0; k < 32; k += 4)
-        red_add_v4(dst + c + k, __uint_as_float(v[k]), __uint_as_float(v[k + 1]), __uint_as_float(v[k + 2]),
+      for (int k = 0; k < HALF; k += 4)
+        red_add_v4(dst + k, __uint_as_float(v[k]), __uint_as_float(v[k + 1]), __uint_as_float(v[k + 2]),
                    __uint_as_float(v[k + 3]));
     }
+    if (has_next) {
+      named_barrier_sync(bar_id, 128);  // every thread is done reading this tile's L2 / D
+      sLD[w * 128 + r] = next_ld;
+      named_barrier_sync(bar_id, 128);
+    }
   }
 }
 
-// Warpgroup 0 after the loop: dK, dV (fp32 TMEM) -> bf16 -> smem (over K_j,
-// V_j) -> TMA store.
+// Warpgroup w after the loop: w = 0 stores dK, w = 1 stores dV
+// (fp32 TMEM -> bf16 -> smem over K_j / V_j -> TMA store).
 template <int HD, bool CAUSAL>
-__device__ void bwd_epilogue(const BwdLaunch& p, BwdShared& sh, uint8_t* sK, uint8_t* sV, uint32_t tmem,
+__device__ void bwd_epilogue(const BwdLaunch& p, BwdShared& sh, uint8_t* sK, uint8_t* sV, uint32_t tmem, int w,
                              const BwdWork<CAUSAL>& wk) {
   using C = BwdCfg<HD>;
   const int r = threadIdx.x & 127;
@@ -415,36 +462,32 @@ __device__ void bwd_epilogue(const BwdLaunch& p, BwdShared& sh, uint8_t* sK, uin
     if (!ok) record_timeout(p.status, &sh.abort_flag, WHERE_BWD_SOFTMAX);
   }
   tc_fence_after_sync();
+  uint8_t* stage = w == 0 ? sK : sV;
   if (ok) {
-#pragma unroll
-    for (int which = 0; which < 2; ++which) {
-      const uint32_t t = tmem + lane_base + (which == 0 ? C::DK_COL : C::DV_COL);
-      const uint32_t stage = smem_u32(which == 0 ? sK : sV);
+    const uint32_t t = tmem + lane_base + (w == 0 ? C::DK_COL : C::DV_COL);
+    const uint32_t st = smem_u32(stage);
 #pragma unroll 1
-      for (int c = 0; c < HD; c += 32) {
-        uint32_t v[32];
-        tmem_ld32(t + c, v);
-        tmem_ld_wait();
+    for (int c = 0; c < HD; c += 32) {
+      uint32_t v[32];
+      tmem_ld32(t + c, v);
+      tmem_ld_wait();
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int col = c + u * 8;
-          st_shared_v4(stage + (col >> 6) * C::CHUNK_BYTES + sw128_offset(r, (col & 63) >> 3),
-                       pack_bf16x2(__uint_as_float(v[u * 8 + 0]), __uint_as_float(v[u * 8 + 1])),
-                       pack_bf16x2(__uint_as_float(v[u * 8 + 2]), __uint_as_float(v[u * 8 + 3])),
-                       pack_bf16x2(__uint_as_float(v[u * 8 + 4]), __uint_as_float(v[u * 8 + 5])),
-                       pack_bf16x2(__uint_as_float(v[u * 8 + 6]), __uint_as_float(v[u * 8 + 7])));
-        }
+      for (int u = 0; u < 4; ++u) {
+        const int col = c + u * 8;
+        st_shared_v4(st + (col >> 6) * C::CHUNK_BYTES + sw128_offset(r, (col & 63) >> 3),
+                     pack_bf16x2(__uint_as_float(v[u * 8 + 0]), __uint_as_float(v[u * 8 + 1])),
+                     pack_bf16x2(__uint_as_float(v[u * 8 + 2]), __uint_as_float(v[u * 8 + 3])),
+                     pack_bf16x2(__uint_as_float(v[u * 8 + 4]), __uint_as_float(v[u * 8 + 5])),
+                     pack_bf16x2(__uint_as_float(v[u * 8 + 6]), __uint_as_float(v[u * 8 + 7])));
       }
     }
     fence_proxy_async_smem();
   }
-  named_barrier_sync(1, 128);
+  named_barrier_sync(1 + w, 128);
   if (ok && r == 0 && !*reinterpret_cast<volatile int*>(&sh.abort_flag)) {
+    const CUtensorMap* map = w == 0 ? &p.tmdK : &p.tmdV;
 #pragma unroll
-    for (int c = 0; c < C::CHUNKS; ++c) {
-      tma_store_3d(&p.tmdK, sK + c * C::CHUNK_BYTES, c * 64, wk.j * 128, wk.bh);
-      tma_store_3d(&p.tmdV, sV + c * C::CHUNK_BYTES, c * 64, wk.j * 128, wk.bh);
-    }
+    for (int c = 0; c < C::CHUNKS; ++c) tma_store_3d(map, stage + c * C::CHUNK_BYTES, c * 64, wk.j * 128, wk.bh);
     tma_store_commit();
     tma_store_wait_all();
   }
@@ -461,6 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
   uint8_t* sQ = sV + C::TILE_BYTES;
   uint8_t* sdO = sQ + C::QST * C::TILE_BYTES;
   uint8_t* sDS = sdO + C::QST * C::TILE_BYTES;
+  float* sLD = reinterpret_cast<float*>(sDS + C::DS_BYTES);
   const int warp = threadIdx.x >> 5;
   const BwdWork<CAUSAL> wk(blockIdx.x, p.BH, p.N);
 
@@ -470,11 +514,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
       mbar_init(&sh.qdo_full[s], 1);
       mbar_init(&sh.qdo_empty[s], 1);
     }
-    mbar_init(&sh.sdp_full, 1);
-    mbar_init(&sh.ds_ready, 128);
+    mbar_init(&sh.s_full, 1);
+    mbar_init(&sh.dp_full, 1);
+    mbar_init(&sh.pa_ready, 256);
+    mbar_init(&sh.ds_ready, 256);
     mbar_init(&sh.pv_done, 1);
     mbar_init(&sh.dq_full, 1);
-    mbar_init(&sh.dq_free, 128);
+    mbar_init(&sh.dq_free, 256);
     mbar_init(&sh.acc_done, 1);
     sh.abort_flag = 0;
     fence_mbarrier_init();
@@ -492,11 +538,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
     if (lane_id() == 0) bwd_load_role<HD, CAUSAL>(p, sh, sK, sV, sQ, sdO, wk);
   } else if (warp == kMmaWarp) {
     if (lane_id() == 0) bwd_mma_role<HD, CAUSAL>(p, sh, sK, sV, sQ, sdO, sDS, tmem, wk);
-  } else if (warp < 4) {
-    bwd_softmax_role<HD, CAUSAL>(p, sh, sDS, tmem, wk);
-    bwd_epilogue<HD, CAUSAL>(p, sh, sK, sV, tmem, wk);
   } else {
-    bwd_dq_role<HD, CAUSAL>(p, sh, tmem, wk);
+    const int w = warp >> 2;  // warpgroup 0 or 1
+    bwd_softmax_role<HD, CAUSAL>(p, sh, sDS, sLD, tmem, w, wk);
+    bwd_epilogue<HD, CAUSAL>(p, sh, sK, sV, tmem, w, wk);
   }
 
   tc_fence_before_sync();
