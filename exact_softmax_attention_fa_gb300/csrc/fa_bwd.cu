@@ -61,7 +61,8 @@ struct BwdCfg {
   static constexpr uint32_t DK_COL = 0;
   static constexpr uint32_t DV_COL = HD;
   static constexpr uint32_t REG_A = 256;  // S^T, then P^T (bf16)
-  static constexpr uint32_t REG_B = 384;  // dP^T, then dQ_i
+  static constexpr uint32_t REG_B = 384;  // dP^T, then dQ_i (d = 128: dQ_i^T)
+  static constexpr bool DQ_T = HD == 128;
   static constexpr int LD_BYTES = 2 * 128 * 4;  // per warpgroup: 64 base-2 L + 64 scaled D
   // smem: K_j, V_j, QST x (Q_i, dO_i), dS^T, L/D staging
   static constexpr int SMEM_BYTES = (2 + 2 * QST) * TILE_BYTES + DS_BYTES + LD_BYTES + 1024;
@@ -105,6 +106,10 @@ struct BwdWork {
 __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
                : "memory");
+}
+
+__device__ __forceinline__ void red_add_f32(float* addr, float a) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(a) : "memory");
 }
 
 __device__ __forceinline__ float4 ldg_f4(const float* p) { return __ldg(reinterpret_cast<const float4*>(p)); }
@@ -239,7 +244,7 @@ __device__ void bwd_mma_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sK, uin
   using C = BwdCfg<HD>;
   constexpr uint32_t kIdescSq = make_idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
   constexpr uint32_t kIdescAcc = make_idesc_bf16_f32(128, HD, false, true);   // dV, dK
-  constexpr uint32_t kIdescDq = make_idesc_bf16_f32(128, HD, true, true);     // dQ
+  constexpr uint32_t kIdescDq = make_idesc_bf16_f32(128, C::DQ_T ? 128 : HD, true, true);  // dQ (or dQ^T)
   const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV), q_addr = smem_u32(sQ), do_addr = smem_u32(sdO),
                  ds_addr = smem_u32(sDS);
   const uint64_t lim = p.wait_limit_ns;
@@ -284,11 +289,18 @@ __device__ void bwd_mma_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sK, uin
     for (int ks = 0; ks < 8; ++ks)
       umma_ss(tmem + C::DK_COL, make_smem_desc_sw128(ds_addr + (ks >> 2) * C::CHUNK_BYTES + (ks & 3) * 32, 16, 1024),
               make_smem_desc_sw128(qa + ks * 2048, C::CHUNK_BYTES, 1024), kIdescAcc, (n > 0 || ks > 0) ? 1u : 0u);
-    // dQ_n = dS K_j into region B (queries on lanes)
+    // dQ_n into region B. d = 128: dQ_n^T = K_j^T dS^T (head-dim columns on
+    // the lanes, queries along the columns), so the drain's reductions cover
+    // whole 128-byte lines. d = 64: dQ_n = dS K_j (queries on the lanes).
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks)
-      umma_ss(tmem + C::REG_B, make_smem_desc_sw128(ds_addr + ks * 2048, C::CHUNK_BYTES, 1024),
-              make_smem_desc_sw128(k_addr + ks * 2048, C::CHUNK_BYTES, 1024), kIdescDq, ks > 0 ? 1u : 0u);
+    for (int ks = 0; ks < 8; ++ks) {
+      const uint64_t ds_mn = make_smem_desc_sw128(ds_addr + ks * 2048, C::CHUNK_BYTES, 1024);
+      const uint64_t k_mn = make_smem_desc_sw128(k_addr + ks * 2048, C::CHUNK_BYTES, 1024);
+      if constexpr (C::DQ_T)
+        umma_ss(tmem + C::REG_B, k_mn, ds_mn, kIdescDq, ks > 0 ? 1u : 0u);
+      else
+        umma_ss(tmem + C::REG_B, ds_mn, k_mn, kIdescDq, ks > 0 ? 1u : 0u);
+    }
     umma_commit(&sh.dq_full);
     umma_commit(&sh.qdo_empty[s]);
     if (n + 1 < n_iter) {
@@ -425,7 +437,22 @@ __device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS
     alive = alive && __all_sync(0xffffffffu, mbar_wait(&sh.dq_full, n & 1, &sh.abort_flag, lim));
     if (!alive) record_timeout(p.status, &sh.abort_flag, WHERE_BWD_DQ);
     tc_fence_after_sync();
-    if (alive) {
+    if (alive && C::DQ_T) {
+      // lane r = head-dim column r; this warpgroup's 64 queries along the
+      // columns. For a fixed query the warp's 32 lanes add into 32
+      // consecutive floats: one full 128-byte line per reduction.
+      float* dst = p.dq_acc + (static_cast<size_t>(wk.bh) * p.Npad + i * 128 + 64 * w) * HD + r;
+      uint32_t v[64];
+      const uint32_t tq = tmem + lane_base + C::REG_B + 64 * w;
+      tmem_ld32(tq, *reinterpret_cast<uint32_t(*)[32]>(v));
+      tmem_ld32(tq + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+      tmem_ld_wait();
+      tc_fence_before_sync();
+      mbar_arrive(&sh.dq_free);
+#pragma unroll
+      for (int c = 0; c < 64; ++c) red_add_f32(dst + static_cast<size_t>(c) * HD, __uint_as_float(v[c]));
+    } else if (alive) {
+      // lane r = query r; columns [w*HD/2, (w+1)*HD/2) of the head dimension
       constexpr int HALF = HD / 2;
       float* dst = p.dq_acc + (static_cast<size_t>(wk.bh) * p.Npad + i * 128 + r) * HD + w * HALF;
       uint32_t v[HALF];

@@ -7,7 +7,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
-#include "../../include/fa.h"
+#include "fa.h"
 
 namespace fa {
 
