@@ -117,6 +117,20 @@ bool make_map(CUtensorMap* m, const void* base, int BH, int N, int d) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The fp32 dQ accumulator [BH][Npad][d]: boxes of 128 rows x 32 columns
+// (128 bytes), 128-byte swizzle, used by TMA reduce-adds.
+bool make_map_f32_acc(CUtensorMap* m, void* base, int BH, int Npad, int d) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(Npad), static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4, static_cast<cuuint64_t>(Npad) * d * 4};
+  cuuint32_t box[3] = {32, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 fa_status_t check_common(int B, int H, int N, int d, int causal, float scale, bool* empty) {
   if (B < 0 || H < 0 || N < 0) return FA_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
@@ -257,6 +271,7 @@ fa_status_t prepare_bwd(const BwdTensors& t, int B, int H, int N, int d, int cau
   a->D = reinterpret_cast<float*>(ws + wl.D_off);
   a->lse2 = reinterpret_cast<float*>(ws + wl.lse2_off);
   a->dq_acc = reinterpret_cast<float*>(ws + wl.dq_off);
+  if (!make_map_f32_acc(&a->tmdQacc, a->dq_acc, BH, round_up_128(N), d)) return FA_ERR_CUDA;
   a->status = ds->status;
   a->N = N;
   a->Npad = round_up_128(N);

@@ -63,9 +63,13 @@ struct BwdCfg {
   static constexpr uint32_t REG_A = 256;  // S^T, then P^T (bf16)
   static constexpr uint32_t REG_B = 384;  // dP^T, then dQ_i (d = 128: dQ_i^T)
   static constexpr bool DQ_T = HD == 128;
+  // d = 64: dQ_i is staged in smem (fp32, two 128 x 32 swizzled chunks, one
+  // per warpgroup) and added to the accumulator by TMA reduce-adds.
+  static constexpr bool DQ_TMA = HD == 64;
+  static constexpr int DQS_BYTES = DQ_TMA ? 128 * 64 * 4 : 0;
   static constexpr int LD_BYTES = 2 * 128 * 4;  // per warpgroup: 64 base-2 L + 64 scaled D
   // smem: K_j, V_j, QST x (Q_i, dO_i), dS^T, L/D staging
-  static constexpr int SMEM_BYTES = (2 + 2 * QST) * TILE_BYTES + DS_BYTES + LD_BYTES + 1024;
+  static constexpr int SMEM_BYTES = (2 + 2 * QST) * TILE_BYTES + DS_BYTES + LD_BYTES + DQS_BYTES + 1024;
 };
 
 struct BwdShared {
@@ -198,6 +202,7 @@ __device__ void bwd_load_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sK, ui
   tma_prefetch_desc(&p.tmK);
   tma_prefetch_desc(&p.tmV);
   tma_prefetch_desc(&p.tmdO);
+  tma_prefetch_desc(&p.tmdQacc);
   mbar_arrive_expect_tx(&sh.kv_full, 2 * C::TILE_BYTES);
 #pragma unroll
   for (int c = 0; c < C::CHUNKS; ++c) {
@@ -323,8 +328,8 @@ __device__ void bwd_mma_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sK, uin
 // thread r owns key r (TMEM lane r) for phases A and B and query r for the
 // dQ drain.
 template <int HD, bool CAUSAL>
-__device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS, float* sLD, uint32_t tmem,
-                                 int w, const BwdWork<CAUSAL>& wk) {
+__device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS, float* sLD, uint8_t* sDQ,
+                                 uint32_t tmem, int w, const BwdWork<CAUSAL>& wk) {
   using C = BwdCfg<HD>;
   const int r = threadIdx.x & 127;
   const uint32_t lane_base = static_cast<uint32_t>((threadIdx.x >> 5) & 3) << 21;
@@ -451,6 +456,31 @@ __device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS
       mbar_arrive(&sh.dq_free);
 #pragma unroll
       for (int c = 0; c < 64; ++c) red_add_f32(dst + static_cast<size_t>(c) * HD, __uint_as_float(v[c]));
+    } else if (C::DQ_TMA) {
+      // lane r = query r, head-dim columns [32w, 32w + 32): stage the row in
+      // this warpgroup's swizzled smem chunk, then one thread reduce-adds the
+      // 128 x 32 chunk into the accumulator through TMA.
+      uint32_t v[32];
+      if (alive) {
+        tmem_ld32(tmem + lane_base + C::REG_B + 32 * w, v);
+        tmem_ld_wait();
+        tc_fence_before_sync();
+        mbar_arrive(&sh.dq_free);
+      }
+      if (r == 0) tma_store_wait_read_all();  // the previous reduce has read the chunk
+      named_barrier_sync(bar_id, 128);
+      uint8_t* chunk = sDQ + w * 128 * 128;
+      if (alive) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          st_shared_v4(smem_u32(chunk) + sw128_offset(r, u), v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+        fence_proxy_async_smem();
+      }
+      named_barrier_sync(bar_id, 128);
+      if (alive && r == 0) {
+        tma_reduce_add_3d(&p.tmdQacc, chunk, 32 * w, i * 128, wk.bh);
+        tma_store_commit();
+      }
     } else if (alive) {
       // lane r = query r; columns [w*HD/2, (w+1)*HD/2) of the head dimension
       constexpr int HALF = HD / 2;
@@ -473,6 +503,7 @@ __device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS
       named_barrier_sync(bar_id, 128);
     }
   }
+  if (C::DQ_TMA && r == 0) tma_store_wait_all();  // reduce-adds complete before the CTA can exit
 }
 
 // Warpgroup w after the loop: w = 0 stores dK, w = 1 stores dV
@@ -532,6 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
   uint8_t* sdO = sQ + C::QST * C::TILE_BYTES;
   uint8_t* sDS = sdO + C::QST * C::TILE_BYTES;
   float* sLD = reinterpret_cast<float*>(sDS + C::DS_BYTES);
+  uint8_t* sDQ = sDS + C::DS_BYTES + C::LD_BYTES;  // 1024-aligned: DS and LD sizes are multiples of 1024
   const int warp = threadIdx.x >> 5;
   const BwdWork<CAUSAL> wk(blockIdx.x, p.BH, p.N);
 
@@ -567,7 +599,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
     if (lane_id() == 0) bwd_mma_role<HD, CAUSAL>(p, sh, sK, sV, sQ, sdO, sDS, tmem, wk);
   } else {
     const int w = warp >> 2;  // warpgroup 0 or 1
-    bwd_softmax_role<HD, CAUSAL>(p, sh, sDS, sLD, tmem, w, wk);
+    bwd_softmax_role<HD, CAUSAL>(p, sh, sDS, sLD, sDQ, tmem, w, wk);
     bwd_epilogue<HD, CAUSAL>(p, sh, sK, sV, tmem, w, wk);
   }
 

@@ -38,6 +38,7 @@ struct FwdLaunch {
 
 struct BwdLaunch {
   CUtensorMap tmQ, tmK, tmV, tmdO, tmdK, tmdV;
+  CUtensorMap tmdQacc;  // fp32 [BH][Npad][d] accumulator, 128 rows x 32 columns per box
   const __nv_bfloat16* o;
   const __nv_bfloat16* dO;
   const float* lse;
