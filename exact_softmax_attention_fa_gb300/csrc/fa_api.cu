@@ -105,12 +105,12 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 // [BH][N][d] bf16, boxes of 128 rows x 64 columns, 128-byte swizzle; rows
 // past N read as zero and are not written by stores.
-bool make_map(CUtensorMap* m, const void* base, int BH, int N, int d) {
+bool make_map(CUtensorMap* m, const void* base, int BH, int N, int d, unsigned box_rows = 128) {
   auto enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
-  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t box[3] = {64, box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -255,13 +255,15 @@ fa_status_t prepare_bwd(const BwdTensors& t, int B, int H, int N, int d, int cau
   const BwdWorkspaceLayout wl = bwd_layout(BH, N, d);
   if (!workspace || workspace_bytes < wl.total) return FA_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return FA_ERR_MISALIGNED;
-  if (d == 256) return FA_ERR_UNSUPPORTED;  // d = 256 backward kernel not built yet
   DeviceState* ds = device_state(&st);
   if (!ds) return st;
   *a = BwdLaunch{};
-  auto map = [&](CUtensorMap* m, const void* ptr) { return !ptr || make_map(m, ptr, BH, N, d); };
-  if (!map(&a->tmQ, t.q) || !map(&a->tmK, t.k) || !map(&a->tmV, t.v) || !map(&a->tmdO, t.dO) ||
-      !map(&a->tmdK, t.dk) || !map(&a->tmdV, t.dv))
+  auto map = [&](CUtensorMap* m, const void* ptr, unsigned rows) { return !ptr || make_map(m, ptr, BH, N, d, rows); };
+  // d = 256 streams Q and dO in 64-row query tiles (smem budget); all other
+  // tiles are 128 rows.
+  const unsigned q_rows = d == 256 ? 64 : 128;
+  if (!map(&a->tmQ, t.q, q_rows) || !map(&a->tmK, t.k, 128) || !map(&a->tmV, t.v, 128) ||
+      !map(&a->tmdO, t.dO, q_rows) || !map(&a->tmdK, t.dk, 128) || !map(&a->tmdV, t.dv, 128))
     return FA_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   a->o = static_cast<const __nv_bfloat16*>(t.o);

@@ -41,6 +41,7 @@
 #include <cmath>
 
 #include "fa_internal.h"
+#include "fa_kernel_common.cuh"
 #include "sm103_ptx.cuh"
 
 namespace fa {
@@ -80,15 +81,6 @@ struct BwdShared {
   int abort_flag;
 };
 
-__device__ __forceinline__ void record_timeout(uint32_t* status, int* abort_flag, uint32_t where) {
-  if (atomicCAS(status, 0u, static_cast<uint32_t>(FA_ERR_TIMEOUT)) == 0u) {
-    status[1] = where;
-    status[2] = blockIdx.x;
-    status[3] = threadIdx.x;
-  }
-  *reinterpret_cast<volatile int*>(abort_flag) = 1;
-}
-
 // Work item: key tile j of head bh; query tiles i0..T-1 (causal: i0 = j).
 template <bool CAUSAL>
 struct BwdWork {
@@ -106,17 +98,6 @@ struct BwdWork {
   }
   __device__ int n_iter() const { return T - i0; }
 };
-
-__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
-               : "memory");
-}
-
-__device__ __forceinline__ void red_add_f32(float* addr, float a) {
-  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(a) : "memory");
-}
-
-__device__ __forceinline__ float4 ldg_f4(const float* p) { return __ldg(reinterpret_cast<const float4*>(p)); }
 
 // ---------------------------------------------------------------------------
 // 1. preprocess
@@ -643,6 +624,7 @@ cudaError_t launch_bwd_pre(const BwdLaunch& a, cudaStream_t stream) {
   switch (a.d) {
     case 64: return launch_pre_t<64>(a, stream);
     case 128: return launch_pre_t<128>(a, stream);
+    case 256: return launch_pre_t<256>(a, stream);
     default: return cudaErrorNotSupported;
   }
 }
@@ -651,6 +633,7 @@ cudaError_t launch_bwd_main(const BwdLaunch& a, cudaStream_t stream) {
   switch (a.d) {
     case 64: return a.causal ? launch_main_t<64, true>(a, stream) : launch_main_t<64, false>(a, stream);
     case 128: return a.causal ? launch_main_t<128, true>(a, stream) : launch_main_t<128, false>(a, stream);
+    case 256: return launch_bwd_main_d256(a, stream);
     default: return cudaErrorNotSupported;
   }
 }
@@ -659,6 +642,7 @@ cudaError_t launch_bwd_post(const BwdLaunch& a, cudaStream_t stream) {
   switch (a.d) {
     case 64: return launch_post_t<64>(a, stream);
     case 128: return launch_post_t<128>(a, stream);
+    case 256: return launch_post_t<256>(a, stream);
     default: return cudaErrorNotSupported;
   }
 }

@@ -41,6 +41,7 @@
 #include <cmath>
 
 #include "fa_internal.h"
+#include "fa_kernel_common.cuh"
 #include "sm103_ptx.cuh"
 
 namespace fa {
@@ -75,15 +76,6 @@ struct FwdShared {
   uint32_t tmem_base;
   int abort_flag;
 };
-
-__device__ __forceinline__ void record_timeout(uint32_t* status, int* abort_flag, uint32_t where) {
-  if (atomicCAS(status, 0u, static_cast<uint32_t>(FA_ERR_TIMEOUT)) == 0u) {
-    status[1] = where;
-    status[2] = blockIdx.x;
-    status[3] = threadIdx.x;
-  }
-  *reinterpret_cast<volatile int*>(abort_flag) = 1;
-}
 
 // Work item of one CTA: NT consecutive 128-row query tiles of head `bh`.
 template <int NT, bool CAUSAL>

@@ -60,6 +60,7 @@ cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t stream);
 cudaError_t launch_bwd_pre(const BwdLaunch& a, cudaStream_t stream);   // D, base-2 L, zero dQ accumulator
 cudaError_t launch_bwd_main(const BwdLaunch& a, cudaStream_t stream);  // dK, dV; dQ into the accumulator
 cudaError_t launch_bwd_post(const BwdLaunch& a, cudaStream_t stream);  // dQ = bf16(accumulator)
+cudaError_t launch_bwd_main_d256(const BwdLaunch& a, cudaStream_t stream);  // fa_bwd256.cu
 cudaError_t launch_timeout_probe(uint32_t* status, uint64_t limit_ns, cudaStream_t stream);
 
 }  // namespace fa

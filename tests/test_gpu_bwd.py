@@ -44,14 +44,14 @@ def test_small_causal_fwd_bwd():
     check_full(w["B"], w["H"], w["N"], w["d"], w["causal"], seed_for(w))
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("N", [1, 7, 127, 128, 129, 200, 256, 383, 640])
+@pytest.mark.parametrize("N", [1, 7, 63, 64, 65, 127, 128, 129, 200, 256, 383, 640])
 def test_ragged_shapes(d, causal, N):
     check_full(1, 2, N, d, causal, BASE_SEED + 200 + N)
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("causal", [False, True])
 def test_several_tiles_with_tail(d, causal):
     check_full(2, 3, 1000, d, causal, BASE_SEED + 17)
@@ -95,3 +95,8 @@ def test_long_causal_peaked_sampled():
     w = WORKLOADS["long_causal_peaked"]
     check_sampled(w["B"], w["H"], w["N"], w["d"], w["causal"], seed_for(w), n_random=0,
                   peaked_frac=w["peaked_frac"])
+
+
+def test_wide_head_d256_sampled():
+    w = WORKLOADS["wide_head_d256"]
+    check_sampled(w["B"], w["H"], w["N"], w["d"], w["causal"], seed_for(w), n_random=0)
