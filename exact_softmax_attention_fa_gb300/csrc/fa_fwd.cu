@@ -24,7 +24,8 @@
 //     units of the scaled scores) and l in registers, computes
 //     P~ = 2^(S*scale*log2e - m) with one FFMA + ex2 per element, writes P~
 //     as bf16 back to TMEM, and rescales its row of O~ in TMEM only when the
-//     row max of some row of the warp grew.
+//     row max grew (by more than 8 in base-2 units for some row of the warp;
+//     smaller growth is absorbed with P~ <= 2^8).
 //   - While warpgroup 0 does softmax on tile 0 the tensor core works on
 //     tile 1 and vice versa.
 //   - Epilogue: O = O~ / l converted to bf16 into the (now free) Q tile's
@@ -51,6 +52,10 @@ constexpr int kThreads = 320;
 constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr float kLn2 = 0.69314718055994530942f;
+// Largest growth of a row max (in base-2 units of the scaled scores) absorbed
+// without rescaling: P~ <= 2^8 is exact in bf16's exponent range and l, O~
+// stay far from fp32 overflow.
+constexpr float kRescaleSlack = 8.0f;
 
 template <int HD>
 struct FwdCfg {
@@ -321,9 +326,16 @@ __device__ void fwd_softmax_role(const FwdLaunch& p, FwdShared& sh, uint8_t* sQ,
       mx3 = fmaxf(mx3, s[i + 3]);
     }
     const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
-    const float m_new = fmaxf(m2, mx * c2);
-    const float m_use = m_new == -INFINITY ? 0.f : m_new;
-    const float alpha = ex2_approx(m2 - m_use);  // 0 on the first block, 1 when the max is unchanged
+    // m2 is the reference max the exponentials and both accumulators are
+    // relative to. It moves to the running max only when some row of the
+    // warp has outgrown it by more than kRescaleSlack (then O~ and l are
+    // rescaled); otherwise P~ = 2^(S c - m2) <= 2^kRescaleSlack. Either way
+    // O~ / l is the same in exact arithmetic.
+    const float m_run = fmaxf(m2, mx * c2);
+    const bool move = __any_sync(0xffffffffu, m_run > m2 + kRescaleSlack);
+    const float m_ref = move ? m_run : m2;
+    const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+    const float alpha = ex2_approx(m2 - m_use);  // 0 on the first block, 1 when the reference is kept
     const float neg = -m_use;
     float sum0 = 0.f, sum1 = 0.f;
     uint32_t pk0[32], pk1[32];
@@ -346,8 +358,8 @@ __device__ void fwd_softmax_role(const FwdLaunch& p, FwdShared& sh, uint8_t* sQ,
     l = l * alpha + (sum0 + sum1);
     tmem_st32(tP, pk0);
     tmem_st32(tP + 32, pk1);
-    // Rescale O~ only when some row of this warp found a larger max.
-    if (j > 0 && __any_sync(0xffffffffu, m_new > m2)) {
+    // Rescale O~ only when the reference max moved.
+    if (j > 0 && move) {
 #pragma unroll 1
       for (int c = 0; c < HD; c += 32) {
         uint32_t o[32];
@@ -358,7 +370,7 @@ __device__ void fwd_softmax_role(const FwdLaunch& p, FwdShared& sh, uint8_t* sQ,
         tmem_st32(tO + c, o);
       }
     }
-    m2 = m_new;
+    m2 = m_ref;
     tmem_st_wait();
     tc_fence_before_sync();
     mbar_arrive(&sh.p_full[t]);
