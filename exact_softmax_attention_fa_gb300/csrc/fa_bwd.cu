@@ -47,6 +47,8 @@
 namespace fa {
 namespace {
 
+// Warps: 0-3 and 4-7 softmax + dQ drain (query columns 0-63 / 64-127),
+// 8 TMA loads, 9 MMA issue.
 constexpr int kThreads = 320;
 constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;
@@ -224,6 +226,13 @@ __device__ void bwd_load_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sK, ui
 //   dQ_n = dS K_j -> B   after phase B(n)
 //   S^T(n+1) -> A        after dV(n) released P^T   (overlaps the dQ drain)
 //   dP^T(n+1) -> B       after the dQ drain         (overlaps phase A(n+1))
+// One thread issues every MMA. Per query tile n (region A: S^T then P^T;
+// region B: dP^T then dQ_n):
+//   dV += P^T dO_n        after phase A(n)          (overlaps phase B(n))
+//   S^T(n+1) -> A         after dV(n) released P^T (overlaps phase B(n))
+//   dK += dS^T Q_n        after phase B(n)          (overlaps phase A(n+1))
+//   dQ_n -> B             after phase B(n)          (overlaps phase A(n+1))
+//   dP^T(n+1) -> B        after the drain warpgroup read dQ_n out of TMEM
 template <int HD, bool CAUSAL>
 __device__ void bwd_mma_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sK, uint8_t* sV, uint8_t* sQ,
                              uint8_t* sdO, uint8_t* sDS, uint32_t tmem, const BwdWork<CAUSAL>& wk) {
@@ -259,6 +268,8 @@ __device__ void bwd_mma_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sK, uin
 
   for (int n = 0; n < n_iter; ++n) {
     const int s = n % C::QST;
+    const bool has_next = n + 1 < n_iter;
+    const int s1 = (n + 1) % C::QST;
     const uint32_t qa = q_addr + s * C::TILE_BYTES, doa = do_addr + s * C::TILE_BYTES;
     if (!mbar_wait(&sh.pa_ready, n & 1, &sh.abort_flag, lim)) return fail();
     tc_fence_after_sync();
@@ -268,6 +279,14 @@ __device__ void bwd_mma_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sK, uin
       umma_ts(tmem + C::DV_COL, tmem + C::REG_A + (ks >> 2) * 64 + (ks & 3) * 8,
               make_smem_desc_sw128(doa + ks * 2048, C::CHUNK_BYTES, 1024), kIdescAcc, (n > 0 || ks > 0) ? 1u : 0u);
     umma_commit(&sh.pv_done);
+    if (has_next) {
+      // S^T(n+1) overwrites P^T(n): wait until dV(n) has read it.
+      if (!mbar_wait(&sh.qdo_full[s1], ((n + 1) / C::QST) & 1, &sh.abort_flag, lim)) return fail();
+      if (!mbar_wait(&sh.pv_done, n & 1, &sh.abort_flag, lim)) return fail();
+      tc_fence_after_sync();
+      issue_sq(C::REG_A, k_addr, q_addr + s1 * C::TILE_BYTES);
+      umma_commit(&sh.s_full);
+    }
     if (!mbar_wait(&sh.ds_ready, n & 1, &sh.abort_flag, lim)) return fail();
     tc_fence_after_sync();
     // dK += dS^T Q_n
@@ -289,13 +308,7 @@ __device__ void bwd_mma_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sK, uin
     }
     umma_commit(&sh.dq_full);
     umma_commit(&sh.qdo_empty[s]);
-    if (n + 1 < n_iter) {
-      const int s1 = (n + 1) % C::QST;
-      if (!mbar_wait(&sh.qdo_full[s1], ((n + 1) / C::QST) & 1, &sh.abort_flag, lim)) return fail();
-      if (!mbar_wait(&sh.pv_done, n & 1, &sh.abort_flag, lim)) return fail();
-      tc_fence_after_sync();
-      issue_sq(C::REG_A, k_addr, q_addr + s1 * C::TILE_BYTES);  // S^T(n+1) over the consumed P^T(n)
-      umma_commit(&sh.s_full);
+    if (has_next) {
       if (!mbar_wait(&sh.dq_free, n & 1, &sh.abort_flag, lim)) return fail();
       tc_fence_after_sync();
       issue_sq(C::REG_B, v_addr, do_addr + s1 * C::TILE_BYTES);  // dP^T(n+1) over the drained dQ_n
@@ -305,9 +318,11 @@ __device__ void bwd_mma_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sK, uin
   umma_commit(&sh.acc_done);
 }
 
-// Warpgroup w (w = 0, 1) owns query columns [64w, 64w + 64) of every tile;
-// thread r owns key r (TMEM lane r) for phases A and B and query r for the
-// dQ drain.
+// Warpgroup w (w = 0, 1) owns query columns [64w, 64w + 64) of every tile:
+// thread r owns key r (TMEM lane r) in phases A and B, and head-dim column r
+// (d = 128) or query r (d = 64) in the dQ drain. Per tile n the order is
+// B(n), A(n+1), drain(n): phase A(n+1) overlaps the dK(n) and dQ_n MMAs and
+// the drain's reductions overlap dP^T(n+1) and dV(n+1).
 template <int HD, bool CAUSAL>
 __device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS, float* sLD, uint8_t* sDQ,
                                  uint32_t tmem, int w, const BwdWork<CAUSAL>& wk) {
@@ -326,31 +341,27 @@ __device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS
   const float* D_bh = p.D + static_cast<size_t>(wk.bh) * p.Npad + 64 * w;
   const int n_iter = wk.n_iter();
   const uint32_t bar_id = 1 + w;
+  const uint32_t tA = tmem + lane_base + C::REG_A + 64 * w;
+  const uint32_t tB = tmem + lane_base + C::REG_B + 64 * w;
   bool alive = true;
+  float pv[64];  // P^T of the current tile (fp32), from phase A to phase B
 
   // L2 / D of query tile i for this warpgroup's 64 columns: thread r < 64
   // loads L2[r], thread r >= 64 loads D[r - 64] * scale.
   auto fetch_ld = [&](int i) -> float {
     return r < 64 ? __ldg(lse2_bh + i * 128 + r) : __ldg(D_bh + i * 128 + (r - 64)) * sc;
   };
-  {
-    const float v = fetch_ld(wk.i0);
-    sLD[w * 128 + r] = v;
-    named_barrier_sync(bar_id, 128);
-  }
 
-  for (int n = 0; n < n_iter; ++n) {
+  // ---- phase A: P^T = 2^(S^T * scale * log2e - L2), written back to TMEM as bf16.
+  // After a timed-out wait a warp stops working but still passes every named
+  // barrier, so the warpgroup's barrier counts stay matched.
+  auto phase_a = [&](int n) {
     const int i = wk.i0 + n;
-    const uint32_t tA = tmem + lane_base + C::REG_A + 64 * w;
-    const uint32_t tB = tmem + lane_base + C::REG_B + 64 * w;
-    // ---- phase A: P^T = 2^(S^T * scale * log2e - L2), written back to TMEM as bf16
-    // After a timed-out wait the warp stops working but still passes every
-    // named barrier below, so the warpgroup's barrier counts stay matched.
     alive = alive && __all_sync(0xffffffffu, mbar_wait(&sh.s_full, n & 1, &sh.abort_flag, lim));
     if (!alive) record_timeout(p.status, &sh.abort_flag, WHERE_BWD_SOFTMAX);
     tc_fence_after_sync();
-    float pv[64];
-    if (alive) {
+    if (!alive) return;
+    {
       uint32_t a[32], b[32];
       tmem_ld32(tA, a);
       tmem_ld32(tA + 32, b);
@@ -361,20 +372,21 @@ __device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS
         pv[32 + c] = __uint_as_float(b[c]);
       }
     }
-    // causal diagonal tile: query (64w + c) sees key r only if 64w + c >= r
-    const int c_lo = (CAUSAL && i == wk.j) ? r - 64 * w : 0;
-    if (alive) {
+    // Only the key-tail tile and the causal diagonal tile need masking:
+    // query (64w + c) sees key r only if 64w + c >= r.
+    const bool masked = !key_valid || (CAUSAL && i == wk.j);
+    const int c_lo = !key_valid ? 64 : ((CAUSAL && i == wk.j) ? r - 64 * w : 0);
     uint32_t pk[32];
 #pragma unroll
     for (int c4 = 0; c4 < 64; c4 += 4) {
       const float4 l = *reinterpret_cast<const float4*>(ld_l2 + c4);
       const float lv[4] = {l.x, l.y, l.z, l.w};
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int c = c4 + u;
-        float e = ex2_approx(fmaf(pv[c], c2, -lv[u]));
-        if (!key_valid || c < c_lo) e = 0.f;
-        pv[c] = e;
+      for (int u = 0; u < 4; ++u) pv[c4 + u] = ex2_approx(fmaf(pv[c4 + u], c2, -lv[u]));
+      if (masked) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (c4 + u < c_lo) pv[c4 + u] = 0.f;
       }
       pk[c4 / 2] = pack_bf16x2(pv[c4], pv[c4 + 1]);
       pk[c4 / 2 + 1] = pack_bf16x2(pv[c4 + 2], pv[c4 + 3]);
@@ -383,13 +395,14 @@ __device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS
     tmem_st_wait();
     tc_fence_before_sync();
     mbar_arrive(&sh.pa_ready);
-    }
+  };
 
-    // ---- phase B: dS^T = P^T o (dP^T - D) * scale -> smem (bf16, swizzled)
+  // ---- phase B: dS^T = P^T o (dP^T - D) * scale -> smem (bf16, swizzled)
+  auto phase_b = [&](int n) {
     alive = alive && __all_sync(0xffffffffu, mbar_wait(&sh.dp_full, n & 1, &sh.abort_flag, lim));
     if (!alive) record_timeout(p.status, &sh.abort_flag, WHERE_BWD_SOFTMAX);
     tc_fence_after_sync();
-    if (alive) {
+    if (!alive) return;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       uint32_t dpv[32];
@@ -413,31 +426,29 @@ __device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS
     fence_proxy_async_smem();
     tc_fence_before_sync();
     mbar_arrive(&sh.ds_ready);
-    }
+  };
 
-    // ---- next tile's L2 / D (latency hidden behind the dQ wait)
-    const bool has_next = n + 1 < n_iter;
-    const float next_ld = has_next ? fetch_ld(i + 1) : 0.f;
-
-    // ---- dQ drain: columns [w*HD/2, (w+1)*HD/2) of region B, query r
+  // ---- dQ drain of tile n out of region B
+  auto drain = [&](int n) {
+    const int i = wk.i0 + n;
     alive = alive && __all_sync(0xffffffffu, mbar_wait(&sh.dq_full, n & 1, &sh.abort_flag, lim));
     if (!alive) record_timeout(p.status, &sh.abort_flag, WHERE_BWD_DQ);
     tc_fence_after_sync();
-    if (alive && C::DQ_T) {
-      // lane r = head-dim column r; this warpgroup's 64 queries along the
-      // columns. For a fixed query the warp's 32 lanes add into 32
-      // consecutive floats: one full 128-byte line per reduction.
+    if constexpr (C::DQ_T) {
+      // lane r = head-dim column r, this warpgroup's 64 queries along the
+      // columns: for a fixed query the warp's 32 lanes add into 32
+      // consecutive floats, one full 128-byte line per reduction.
+      if (!alive) return;
       float* dst = p.dq_acc + (static_cast<size_t>(wk.bh) * p.Npad + i * 128 + 64 * w) * HD + r;
       uint32_t v[64];
-      const uint32_t tq = tmem + lane_base + C::REG_B + 64 * w;
-      tmem_ld32(tq, *reinterpret_cast<uint32_t(*)[32]>(v));
-      tmem_ld32(tq + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+      tmem_ld32(tB, *reinterpret_cast<uint32_t(*)[32]>(v));
+      tmem_ld32(tB + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
       tmem_ld_wait();
       tc_fence_before_sync();
       mbar_arrive(&sh.dq_free);
 #pragma unroll
       for (int c = 0; c < 64; ++c) red_add_f32(dst + static_cast<size_t>(c) * HD, __uint_as_float(v[c]));
-    } else if (C::DQ_TMA) {
+    } else {
       // lane r = query r, head-dim columns [32w, 32w + 32): stage the row in
       // this warpgroup's swizzled smem chunk, then one thread reduce-adds the
       // 128 x 32 chunk into the accumulator through TMA.
@@ -462,29 +473,28 @@ __device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS
         tma_reduce_add_3d(&p.tmdQacc, chunk, 32 * w, i * 128, wk.bh);
         tma_store_commit();
       }
-    } else if (alive) {
-      // lane r = query r; columns [w*HD/2, (w+1)*HD/2) of the head dimension
-      constexpr int HALF = HD / 2;
-      float* dst = p.dq_acc + (static_cast<size_t>(wk.bh) * p.Npad + i * 128 + r) * HD + w * HALF;
-      uint32_t v[HALF];
-      const uint32_t tq = tmem + lane_base + C::REG_B + w * HALF;
-#pragma unroll
-      for (int c = 0; c < HALF; c += 32) tmem_ld32(tq + c, *reinterpret_cast<uint32_t(*)[32]>(v + c));
-      tmem_ld_wait();
-      tc_fence_before_sync();
-      mbar_arrive(&sh.dq_free);
-#pragma unroll
-      for (int k = 0; k < HALF; k += 4)
-        red_add_v4(dst + k, __uint_as_float(v[k]), __uint_as_float(v[k + 1]), __uint_as_float(v[k + 2]),
-                   __uint_as_float(v[k + 3]));
     }
+  };
+
+  {
+    const float v0 = fetch_ld(wk.i0);
+    sLD[w * 128 + r] = v0;
+    named_barrier_sync(bar_id, 128);
+  }
+  phase_a(0);
+  for (int n = 0; n < n_iter; ++n) {
+    const bool has_next = n + 1 < n_iter;
+    const float next_ld = has_next ? fetch_ld(wk.i0 + n + 1) : 0.f;  // lands during phase B
+    phase_b(n);
     if (has_next) {
       named_barrier_sync(bar_id, 128);  // every thread is done reading this tile's L2 / D
       sLD[w * 128 + r] = next_ld;
       named_barrier_sync(bar_id, 128);
+      phase_a(n + 1);
     }
+    drain(n);
   }
-  if (C::DQ_TMA && r == 0) tma_store_wait_all();  // reduce-adds complete before the CTA can exit
+  if (!C::DQ_T && r == 0) tma_store_wait_all();  // reduce-adds complete before the CTA can exit
 }
 
 // Warpgroup w after the loop: w = 0 stores dK, w = 1 stores dV
@@ -546,6 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
   float* sLD = reinterpret_cast<float*>(sDS + C::DS_BYTES);
   uint8_t* sDQ = sDS + C::DS_BYTES + C::LD_BYTES;  // 1024-aligned: DS and LD sizes are multiples of 1024
   const int warp = threadIdx.x >> 5;
+  const int wg = warp >> 2;
   const BwdWork<CAUSAL> wk(blockIdx.x, p.BH, p.N);
 
   if (threadIdx.x == 0) {
@@ -579,9 +590,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
   } else if (warp == kMmaWarp) {
     if (lane_id() == 0) bwd_mma_role<HD, CAUSAL>(p, sh, sK, sV, sQ, sdO, sDS, tmem, wk);
   } else {
-    const int w = warp >> 2;  // warpgroup 0 or 1
-    bwd_softmax_role<HD, CAUSAL>(p, sh, sDS, sLD, sDQ, tmem, w, wk);
-    bwd_epilogue<HD, CAUSAL>(p, sh, sK, sV, tmem, w, wk);
+    bwd_softmax_role<HD, CAUSAL>(p, sh, sDS, sLD, sDQ, tmem, wg, wk);
+    bwd_epilogue<HD, CAUSAL>(p, sh, sK, sV, tmem, wg, wk);
   }
 
   tc_fence_before_sync();
