@@ -344,7 +344,9 @@ __device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS
   const uint32_t tA = tmem + lane_base + C::REG_A + 64 * w;
   const uint32_t tB = tmem + lane_base + C::REG_B + 64 * w;
   bool alive = true;
-  float pv[64];  // P^T of the current tile (fp32), from phase A to phase B
+  // P^T of the current tile as the bf16 pairs written to TMEM, kept from
+  // phase A to phase B: dS uses the same rounded P as the dV MMA.
+  uint32_t pk[32];
 
   // L2 / D of query tile i for this warpgroup's 64 columns: thread r < 64
   // loads L2[r], thread r >= 64 loads D[r - 64] * scale.
@@ -361,6 +363,7 @@ __device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS
     if (!alive) record_timeout(p.status, &sh.abort_flag, WHERE_BWD_SOFTMAX);
     tc_fence_after_sync();
     if (!alive) return;
+    float pv[64];
     {
       uint32_t a[32], b[32];
       tmem_ld32(tA, a);
@@ -376,7 +379,6 @@ __device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS
     // query (64w + c) sees key r only if 64w + c >= r.
     const bool masked = !key_valid || (CAUSAL && i == wk.j);
     const int c_lo = !key_valid ? 64 : ((CAUSAL && i == wk.j) ? r - 64 * w : 0);
-    uint32_t pk[32];
 #pragma unroll
     for (int c4 = 0; c4 < 64; c4 += 4) {
       const float4 l = *reinterpret_cast<const float4*>(ld_l2 + c4);
@@ -415,7 +417,11 @@ __device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS
         const float dv4[4] = {dd.x, dd.y, dd.z, dd.w};
         float ds[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) ds[u] = pv[32 * h + c4 + u] * fmaf(__uint_as_float(dpv[c4 + u]), sc, -dv4[u]);
+        const float2 p01 = unpack_bf16x2(pk[16 * h + c4 / 2]);
+        const float2 p23 = unpack_bf16x2(pk[16 * h + c4 / 2 + 1]);
+        const float pp[4] = {p01.x, p01.y, p23.x, p23.y};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) ds[u] = pp[u] * fmaf(__uint_as_float(dpv[c4 + u]), sc, -dv4[u]);
         dk[c4 / 2] = pack_bf16x2(ds[0], ds[1]);
         dk[c4 / 2 + 1] = pack_bf16x2(ds[2], ds[3]);
       }
@@ -437,7 +443,9 @@ __device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS
     if constexpr (C::DQ_T) {
       // lane r = head-dim column r, this warpgroup's 64 queries along the
       // columns: for a fixed query the warp's 32 lanes add into 32
-      // consecutive floats, one full 128-byte line per reduction.
+      // consecutive floats, one full 128-byte line per reduction. (Staging
+      // the tile for TMA reduce-adds through the dS^T tile measured slower:
+      // the staging reads land on the softmax warps' path.)
       if (!alive) return;
       float* dst = p.dq_acc + (static_cast<size_t>(wk.bh) * p.Npad + i * 128 + 64 * w) * HD + r;
       uint32_t v[64];
