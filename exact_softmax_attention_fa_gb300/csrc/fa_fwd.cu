@@ -317,15 +317,16 @@ __device__ void fwd_softmax_role(const FwdLaunch& p, FwdShared& sh, uint8_t* sQ,
       for (int i = 0; i < 128; ++i)
         if (i > lim_col) s[i] = -INFINITY;
     }
-    float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+    // columns 0-7 seed four accumulators, then 8-127 two at a time each
+    float mx0 = fmaxf(s[0], s[1]), mx1 = fmaxf(s[2], s[3]), mx2 = fmaxf(s[4], s[5]), mx3 = fmaxf(s[6], s[7]);
 #pragma unroll
-    for (int i = 4; i < 128; i += 4) {
-      mx0 = fmaxf(mx0, s[i]);
-      mx1 = fmaxf(mx1, s[i + 1]);
-      mx2 = fmaxf(mx2, s[i + 2]);
-      mx3 = fmaxf(mx3, s[i + 3]);
+    for (int i = 8; i < 128; i += 8) {
+      mx0 = fmax3(mx0, s[i], s[i + 1]);
+      mx1 = fmax3(mx1, s[i + 2], s[i + 3]);
+      mx2 = fmax3(mx2, s[i + 4], s[i + 5]);
+      mx3 = fmax3(mx3, s[i + 6], s[i + 7]);
     }
-    const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+    const float mx = fmax3(fmaxf(mx0, mx1), mx2, mx3);
     // m2 is the reference max the exponentials and both accumulators are
     // relative to. It moves to the running max only when some row of the
     // warp has outgrown it by more than kRescaleSlack (then O~ and l are
@@ -337,26 +338,25 @@ __device__ void fwd_softmax_role(const FwdLaunch& p, FwdShared& sh, uint8_t* sQ,
     const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
     const float alpha = ex2_approx(m2 - m_use);  // 0 on the first block, 1 when the reference is kept
     const float neg = -m_use;
-    float sum0 = 0.f, sum1 = 0.f;
+    float2 sum_a = make_float2(0.f, 0.f), sum_b = make_float2(0.f, 0.f);
     uint32_t pk0[32], pk1[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-      const float p0 = ex2_approx(fmaf(s[2 * i], c2, neg));
-      const float p1 = ex2_approx(fmaf(s[2 * i + 1], c2, neg));
-      sum0 += p0;
-      sum1 += p1;
-      pk0[i] = pack_bf16x2(p0, p1);
+      const float2 x = ffma2_bcast(s[2 * i], s[2 * i + 1], c2, neg);
+      const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+      if (i & 1) sum_b = fadd2(sum_b, e); else sum_a = fadd2(sum_a, e);
+      pk0[i] = pack_bf16x2(e.x, e.y);
     }
+    tmem_st32(tP, pk0);  // first 64 keys of P~: frees registers for the second half
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-      const float p0 = ex2_approx(fmaf(s[64 + 2 * i], c2, neg));
-      const float p1 = ex2_approx(fmaf(s[64 + 2 * i + 1], c2, neg));
-      sum0 += p0;
-      sum1 += p1;
-      pk1[i] = pack_bf16x2(p0, p1);
+      const float2 x = ffma2_bcast(s[64 + 2 * i], s[64 + 2 * i + 1], c2, neg);
+      const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+      if (i & 1) sum_b = fadd2(sum_b, e); else sum_a = fadd2(sum_a, e);
+      pk1[i] = pack_bf16x2(e.x, e.y);
     }
-    l = l * alpha + (sum0 + sum1);
-    tmem_st32(tP, pk0);
+    const float2 sum2 = fadd2(sum_a, sum_b);
+    l = l * alpha + (sum2.x + sum2.y);
     tmem_st32(tP + 32, pk1);
     // Rescale O~ only when the reference max moved.
     if (j > 0 && move) {
