@@ -383,8 +383,12 @@ __device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS
     for (int c4 = 0; c4 < 64; c4 += 4) {
       const float4 l = *reinterpret_cast<const float4*>(ld_l2 + c4);
       const float lv[4] = {l.x, l.y, l.z, l.w};
-#pragma unroll
-      for (int u = 0; u < 4; ++u) pv[c4 + u] = ex2_approx(fmaf(pv[c4 + u], c2, -lv[u]));
+      const float2 x01 = ffma2_bcast_mul(pv[c4], pv[c4 + 1], c2, -lv[0], -lv[1]);
+      const float2 x23 = ffma2_bcast_mul(pv[c4 + 2], pv[c4 + 3], c2, -lv[2], -lv[3]);
+      pv[c4] = ex2_approx(x01.x);
+      pv[c4 + 1] = ex2_approx(x01.y);
+      pv[c4 + 2] = ex2_approx(x23.x);
+      pv[c4 + 3] = ex2_approx(x23.y);
       if (masked) {
 #pragma unroll
         for (int u = 0; u < 4; ++u)
@@ -415,15 +419,16 @@ __device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS
       for (int c4 = 0; c4 < 32; c4 += 4) {
         const float4 dd = *reinterpret_cast<const float4*>(ld_d + 32 * h + c4);
         const float dv4[4] = {dd.x, dd.y, dd.z, dd.w};
-        float ds[4];
-#pragma unroll
         const float2 p01 = unpack_bf16x2(pk[16 * h + c4 / 2]);
         const float2 p23 = unpack_bf16x2(pk[16 * h + c4 / 2 + 1]);
-        const float pp[4] = {p01.x, p01.y, p23.x, p23.y};
-#pragma unroll
-        for (int u = 0; u < 4; ++u) ds[u] = pp[u] * fmaf(__uint_as_float(dpv[c4 + u]), sc, -dv4[u]);
-        dk[c4 / 2] = pack_bf16x2(ds[0], ds[1]);
-        dk[c4 / 2 + 1] = pack_bf16x2(ds[2], ds[3]);
+        const float2 g01 =
+            ffma2_bcast_mul(__uint_as_float(dpv[c4]), __uint_as_float(dpv[c4 + 1]), sc, -dv4[0], -dv4[1]);
+        const float2 g23 =
+            ffma2_bcast_mul(__uint_as_float(dpv[c4 + 2]), __uint_as_float(dpv[c4 + 3]), sc, -dv4[2], -dv4[3]);
+        const float2 ds01 = fmul2(p01, g01);
+        const float2 ds23 = fmul2(p23, g23);
+        dk[c4 / 2] = pack_bf16x2(ds01.x, ds01.y);
+        dk[c4 / 2 + 1] = pack_bf16x2(ds23.x, ds23.y);
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u)

@@ -302,6 +302,33 @@ __device__ __forceinline__ float2 ffma2_bcast(float x0, float x1, float m, float
   return r;
 }
 
+// (x0, x1) * (m, m) + (a0, a1)
+__device__ __forceinline__ float2 ffma2_bcast_mul(float x0, float x1, float m, float a0, float a1) {
+  float2 r;
+  asm("{\n\t.reg .b64 x, y, z;\n\t"
+      "mov.b64 x, {%2, %3};\n\t"
+      "mov.b64 y, {%4, %4};\n\t"
+      "mov.b64 z, {%5, %6};\n\t"
+      "fma.rn.f32x2 x, x, y, z;\n\t"
+      "mov.b64 {%0, %1}, x;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(x0), "f"(x1), "f"(m), "f"(a0), "f"(a1));
+  return r;
+}
+
+// (a0, a1) * (b0, b1)
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  float2 r;
+  asm("{\n\t.reg .b64 x, y;\n\t"
+      "mov.b64 x, {%2, %3};\n\t"
+      "mov.b64 y, {%4, %5};\n\t"
+      "mul.rn.f32x2 x, x, y;\n\t"
+      "mov.b64 {%0, %1}, x;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+
 // (a0, a1) + (b0, b1)
 __device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
   float2 r;
