@@ -75,30 +75,32 @@ struct FwdCfg {
 };
 
 struct FwdShared {
-  uint64_t q_full;
+  uint64_t q_full, q_free[2];
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
-  uint64_t s_full[2], p_full[2], pv_done[2];
+  uint64_t s_full[2], p_full[2], pv_done[2], o_free[2];
   uint32_t tmem_base;
   int abort_flag;
 };
 
-// Work item of one CTA: NT consecutive 128-row query tiles of head `bh`.
+// Work item: NT consecutive 128-row query tiles of head `bh`. Items are
+// numbered longest-first under a causal mask (the last query tiles see the
+// most keys); non-causal items of one head are adjacent (K/V reuse in L2).
 template <int NT, bool CAUSAL>
 struct FwdWork {
   int bh;
   int qt[NT];       // query tile indices
   int last_kv[NT];  // last key tile each query tile needs; -1 if the tile is past the end
   int nkv;          // number of key tiles streamed
-  __device__ FwdWork(int block, int BH, int N) {
+  __device__ FwdWork(int item, int BH, int N) {
     const int T = (N + 127) / 128;
     const int n_w = (T + NT - 1) / NT;
     int w;
-    if (CAUSAL) {  // longest work first: the last query tiles see the most keys
-      bh = block % BH;
-      w = n_w - 1 - block / BH;
+    if (CAUSAL) {
+      bh = item % BH;
+      w = n_w - 1 - item / BH;
     } else {
-      bh = block / n_w;
-      w = block % n_w;
+      bh = item / n_w;
+      w = item % n_w;
     }
     nkv = 0;
 #pragma unroll
@@ -110,61 +112,100 @@ struct FwdWork {
   }
 };
 
+// Persistent schedule: CTA b of G takes items in rounds k = 0, 1, ...; round
+// k holds items [kG, kG + G) and is walked forwards on even rounds and
+// backwards on odd ones, so with items sorted longest-first every CTA gets a
+// similar total.
+__device__ __forceinline__ int sched_item(int k, int b, int G) { return k * G + ((k & 1) ? G - 1 - b : b); }
+
+__device__ __forceinline__ int total_items(int BH, int N, int NT) {
+  const int T = (N + 127) / 128;
+  return BH * ((T + NT - 1) / NT);
+}
+
 // ---------------------------------------------------------------------------
 // TMA producer (one thread)
 // ---------------------------------------------------------------------------
 template <int HD, bool CAUSAL>
-__device__ void fwd_load_role(const FwdLaunch& p, FwdShared& sh, uint8_t* sQ, uint8_t* sK, uint8_t* sV,
-                              const FwdWork<FwdCfg<HD>::NT, CAUSAL>& wk) {
+__device__ void fwd_load_role(const FwdLaunch& p, FwdShared& sh, uint8_t* sQ, uint8_t* sK, uint8_t* sV) {
   using C = FwdCfg<HD>;
   tma_prefetch_desc(&p.tmQ);
   tma_prefetch_desc(&p.tmK);
   tma_prefetch_desc(&p.tmV);
   tma_prefetch_desc(&p.tmO);
-  uint32_t qbytes = 0;
-#pragma unroll
-  for (int t = 0; t < C::NT; ++t)
-    if (wk.last_kv[t] >= 0) qbytes += C::TILE_BYTES;
-  mbar_arrive_expect_tx(&sh.q_full, qbytes);
-#pragma unroll
-  for (int t = 0; t < C::NT; ++t) {
-    if (wk.last_kv[t] < 0) continue;
-#pragma unroll
-    for (int c = 0; c < C::CHUNKS; ++c)
-      tma_load_3d(sQ + t * C::TILE_BYTES + c * C::CHUNK_BYTES, &p.tmQ, &sh.q_full, c * 64, wk.qt[t] * 128, wk.bh);
-  }
+  const int total = total_items(p.BH, p.N, C::NT);
+  const int G = gridDim.x;
+  const uint64_t lim = p.wait_limit_ns;
+  int kv = 0;     // running count of K/V tiles loaded by this CTA
+  int items = 0;  // items started
   int k_issued = 0, v_issued = 0;
   bool aborted = false;
-  for (int j = 0; j < wk.nkv && !aborted; ++j) {
-    const int ks = j % C::KST;
-    if (j >= C::KST && !mbar_wait(&sh.k_empty[ks], ((j / C::KST) - 1) & 1, &sh.abort_flag, p.wait_limit_ns)) {
-      aborted = true;
-      break;
-    }
-    mbar_arrive_expect_tx(&sh.k_full[ks], C::TILE_BYTES);
+  for (int k = 0; k * G < total && !aborted; ++k) {
+    const int item = sched_item(k, blockIdx.x, G);
+    if (item >= total) continue;
+    const FwdWork<C::NT, CAUSAL> wk(item, p.BH, p.N);
+    // Q_t's smem was the previous item's O staging: wait until its store read
+    // it. The item's first K/V tile is issued before that wait so it loads
+    // while the previous epilogue runs.
+    auto load_q = [&]() -> bool {
+      if (items > 0) {
 #pragma unroll
-    for (int c = 0; c < C::CHUNKS; ++c)
-      tma_load_3d(sK + ks * C::TILE_BYTES + c * C::CHUNK_BYTES, &p.tmK, &sh.k_full[ks], c * 64, j * 128, wk.bh);
-    ++k_issued;
-    const int vs = j % C::VST;
-    if (j >= C::VST && !mbar_wait(&sh.v_empty[vs], ((j / C::VST) - 1) & 1, &sh.abort_flag, p.wait_limit_ns)) {
-      aborted = true;
-      break;
-    }
-    mbar_arrive_expect_tx(&sh.v_full[vs], C::TILE_BYTES);
+        for (int t = 0; t < C::NT; ++t)
+          if (!mbar_wait(&sh.q_free[t], (items - 1) & 1, &sh.abort_flag, lim)) return false;
+      }
+      uint32_t qbytes = 0;
 #pragma unroll
-    for (int c = 0; c < C::CHUNKS; ++c)
-      tma_load_3d(sV + vs * C::TILE_BYTES + c * C::CHUNK_BYTES, &p.tmV, &sh.v_full[vs], c * 64, j * 128, wk.bh);
-    ++v_issued;
+      for (int t = 0; t < C::NT; ++t)
+        if (wk.last_kv[t] >= 0) qbytes += C::TILE_BYTES;
+      mbar_arrive_expect_tx(&sh.q_full, qbytes);
+#pragma unroll
+      for (int t = 0; t < C::NT; ++t) {
+        if (wk.last_kv[t] < 0) continue;
+#pragma unroll
+        for (int c = 0; c < C::CHUNKS; ++c)
+          tma_load_3d(sQ + t * C::TILE_BYTES + c * C::CHUNK_BYTES, &p.tmQ, &sh.q_full, c * 64, wk.qt[t] * 128,
+                      wk.bh);
+      }
+      return true;
+    };
+    for (int j = 0; j < wk.nkv; ++j, ++kv) {
+      const int ks = kv % C::KST;
+      if (kv >= C::KST && !mbar_wait(&sh.k_empty[ks], ((kv / C::KST) - 1) & 1, &sh.abort_flag, lim)) {
+        aborted = true;
+        break;
+      }
+      mbar_arrive_expect_tx(&sh.k_full[ks], C::TILE_BYTES);
+#pragma unroll
+      for (int c = 0; c < C::CHUNKS; ++c)
+        tma_load_3d(sK + ks * C::TILE_BYTES + c * C::CHUNK_BYTES, &p.tmK, &sh.k_full[ks], c * 64, j * 128, wk.bh);
+      ++k_issued;
+      if (j == 0 && !load_q()) {
+        aborted = true;
+        break;
+      }
+      const int vs = kv % C::VST;
+      if (kv >= C::VST && !mbar_wait(&sh.v_empty[vs], ((kv / C::VST) - 1) & 1, &sh.abort_flag, lim)) {
+        aborted = true;
+        break;
+      }
+      mbar_arrive_expect_tx(&sh.v_full[vs], C::TILE_BYTES);
+#pragma unroll
+      for (int c = 0; c < C::CHUNKS; ++c)
+        tma_load_3d(sV + vs * C::TILE_BYTES + c * C::CHUNK_BYTES, &p.tmV, &sh.v_full[vs], c * 64, j * 128, wk.bh);
+      ++v_issued;
+    }
+    if (aborted) break;
+    ++items;
   }
   if (aborted) {
     record_timeout(p.status, &sh.abort_flag, WHERE_FWD_LOAD);
     // Let the copies already issued land before the CTA can exit.
     const int zero = 0;
     for (int jj = max(0, k_issued - C::KST); jj < k_issued; ++jj)
-      mbar_wait(&sh.k_full[jj % C::KST], (jj / C::KST) & 1, &zero, p.wait_limit_ns);
+      mbar_wait(&sh.k_full[jj % C::KST], (jj / C::KST) & 1, &zero, lim);
     for (int jj = max(0, v_issued - C::VST); jj < v_issued; ++jj)
-      mbar_wait(&sh.v_full[jj % C::VST], (jj / C::VST) & 1, &zero, p.wait_limit_ns);
+      mbar_wait(&sh.v_full[jj % C::VST], (jj / C::VST) & 1, &zero, lim);
+    if (items > 0 || k_issued > 0) mbar_wait(&sh.q_full, items & 1, &zero, lim);
   }
 }
 
@@ -173,16 +214,18 @@ __device__ void fwd_load_role(const FwdLaunch& p, FwdShared& sh, uint8_t* sQ, ui
 // ---------------------------------------------------------------------------
 template <int HD, bool CAUSAL>
 __device__ void fwd_mma_role(const FwdLaunch& p, FwdShared& sh, uint8_t* sQ, uint8_t* sK, uint8_t* sV,
-                             uint32_t tmem, const FwdWork<FwdCfg<HD>::NT, CAUSAL>& wk) {
+                             uint32_t tmem) {
   using C = FwdCfg<HD>;
   constexpr uint32_t kIdescS = make_idesc_bf16_f32(128, 128, false, false);
   constexpr uint32_t kIdescPV = make_idesc_bf16_f32(128, HD, false, true);
   const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV);
   const uint64_t lim = p.wait_limit_ns;
+  const int total = total_items(p.BH, p.N, C::NT);
+  const int G = gridDim.x;
 
-  auto issue_s = [&](int t, int j) {
+  auto issue_s = [&](int t, int g) {  // g: running K/V tile index
     const uint32_t qa = q_addr + t * C::TILE_BYTES;
-    const uint32_t ka = k_addr + (j % C::KST) * C::TILE_BYTES;
+    const uint32_t ka = k_addr + (g % C::KST) * C::TILE_BYTES;
 #pragma unroll
     for (int ks = 0; ks < HD / 16; ++ks) {
       const uint32_t off = (ks >> 2) * C::CHUNK_BYTES + (ks & 3) * 32;
@@ -191,82 +234,90 @@ __device__ void fwd_mma_role(const FwdLaunch& p, FwdShared& sh, uint8_t* sQ, uin
     }
     umma_commit(&sh.s_full[t]);
   };
-  auto issue_pv = [&](int t, int j) {
-    const uint32_t va = v_addr + (j % C::VST) * C::TILE_BYTES;
+  auto issue_pv = [&](int t, int g, bool first) {
+    const uint32_t va = v_addr + (g % C::VST) * C::TILE_BYTES;
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks)
       umma_ts(tmem + C::o_col(t), tmem + C::p_col(t) + ks * 8, make_smem_desc_sw128(va + ks * 2048, C::CHUNK_BYTES, 1024),
-              kIdescPV, (j > 0 || ks > 0) ? 1u : 0u);
+              kIdescPV, (!first || ks > 0) ? 1u : 0u);
     umma_commit(&sh.pv_done[t]);
   };
+  auto fail = [&]() { record_timeout(p.status, &sh.abort_flag, WHERE_FWD_MMA); };
 
-  if (!mbar_wait(&sh.q_full, 0, &sh.abort_flag, lim) || !mbar_wait(&sh.k_full[0], 0, &sh.abort_flag, lim)) {
-    record_timeout(p.status, &sh.abort_flag, WHERE_FWD_MMA);
-    return;
-  }
-  tc_fence_after_sync();
-#pragma unroll
-  for (int t = 0; t < C::NT; ++t)
-    if (wk.last_kv[t] >= 0) issue_s(t, 0);
-  umma_commit(&sh.k_empty[0]);
-
-  for (int j = 0; j < wk.nkv; ++j) {
-    const int vs = j % C::VST;
-    if (!mbar_wait(&sh.v_full[vs], (j / C::VST) & 1, &sh.abort_flag, lim)) {
-      record_timeout(p.status, &sh.abort_flag, WHERE_FWD_MMA);
-      return;
-    }
-    const bool has_next = j + 1 < wk.nkv;
-    const int ks_next = (j + 1) % C::KST;
-    bool k_next_ready = false;
-    auto wait_k_next = [&]() -> bool {
-      if (k_next_ready) return true;
-      if (!mbar_wait(&sh.k_full[ks_next], ((j + 1) / C::KST) & 1, &sh.abort_flag, lim)) return false;
-      tc_fence_after_sync();
-      k_next_ready = true;
-      return true;
-    };
+  int kv = 0;             // running K/V tile index
+  int items = 0;          // items processed
+  int cnt[2] = {0, 0};    // running S / P / PV count per query-tile slot
+  for (int k = 0; k * G < total; ++k) {
+    const int item = sched_item(k, blockIdx.x, G);
+    if (item >= total) continue;
+    const FwdWork<C::NT, CAUSAL> wk(item, p.BH, p.N);
+    if (!mbar_wait(&sh.q_full, items & 1, &sh.abort_flag, lim)) return fail();
+    if (!mbar_wait(&sh.k_full[kv % C::KST], (kv / C::KST) & 1, &sh.abort_flag, lim)) return fail();
+    tc_fence_after_sync();
 #pragma unroll
     for (int t = 0; t < C::NT; ++t) {
-      if (j > wk.last_kv[t]) continue;
-      if (!mbar_wait(&sh.p_full[t], j & 1, &sh.abort_flag, lim)) {
-        record_timeout(p.status, &sh.abort_flag, WHERE_FWD_MMA);
-        return;
-      }
+      if (wk.last_kv[t] < 0) continue;
+      // S_t(0) overwrites S_t / P~_t of the previous item: its last PV must be done.
+      if (C::P_ALIAS && cnt[t] > 0 && !mbar_wait(&sh.pv_done[t], (cnt[t] - 1) & 1, &sh.abort_flag, lim))
+        return fail();
       tc_fence_after_sync();
-      issue_pv(t, j);
-      if (!C::P_ALIAS && has_next && j + 1 <= wk.last_kv[t]) {
-        if (!wait_k_next()) {
-          record_timeout(p.status, &sh.abort_flag, WHERE_FWD_MMA);
-          return;
-        }
-        issue_s(t, j + 1);
-      }
+      issue_s(t, kv);
     }
-    if (C::P_ALIAS && has_next) {
+    umma_commit(&sh.k_empty[kv % C::KST]);
+
+    for (int j = 0; j < wk.nkv; ++j) {
+      const int g = kv + j;
+      const int vs = g % C::VST;
+      if (!mbar_wait(&sh.v_full[vs], (g / C::VST) & 1, &sh.abort_flag, lim)) return fail();
+      const bool has_next = j + 1 < wk.nkv;
+      const int gn = g + 1;
+      bool k_next_ready = false;
+      auto wait_k_next = [&]() -> bool {
+        if (k_next_ready) return true;
+        if (!mbar_wait(&sh.k_full[gn % C::KST], (gn / C::KST) & 1, &sh.abort_flag, lim)) return false;
+        tc_fence_after_sync();
+        k_next_ready = true;
+        return true;
+      };
 #pragma unroll
       for (int t = 0; t < C::NT; ++t) {
-        if (j + 1 > wk.last_kv[t]) continue;
-        // S_t(j+1) overwrites the TMEM columns P_t(j) is read from.
-        if (!wait_k_next() || !mbar_wait(&sh.pv_done[t], j & 1, &sh.abort_flag, lim)) {
-          record_timeout(p.status, &sh.abort_flag, WHERE_FWD_MMA);
-          return;
-        }
+        if (j > wk.last_kv[t]) continue;
+        if (!mbar_wait(&sh.p_full[t], (cnt[t] + j) & 1, &sh.abort_flag, lim)) return fail();
+        // PV_t(0) overwrites O~_t: the previous item's epilogue must have read it.
+        if (j == 0 && items > 0 && !mbar_wait(&sh.o_free[t], (items - 1) & 1, &sh.abort_flag, lim)) return fail();
         tc_fence_after_sync();
-        issue_s(t, j + 1);
+        issue_pv(t, g, j == 0);
+        if (!C::P_ALIAS && has_next && j + 1 <= wk.last_kv[t]) {
+          if (!wait_k_next()) return fail();
+          issue_s(t, gn);
+        }
       }
+      if (C::P_ALIAS && has_next) {
+#pragma unroll
+        for (int t = 0; t < C::NT; ++t) {
+          if (j + 1 > wk.last_kv[t]) continue;
+          // S_t(j+1) overwrites the TMEM columns P_t(j) is read from.
+          if (!wait_k_next() || !mbar_wait(&sh.pv_done[t], (cnt[t] + j) & 1, &sh.abort_flag, lim)) return fail();
+          tc_fence_after_sync();
+          issue_s(t, gn);
+        }
+      }
+      if (has_next) umma_commit(&sh.k_empty[gn % C::KST]);
+      umma_commit(&sh.v_empty[vs]);
     }
-    if (has_next) umma_commit(&sh.k_empty[ks_next]);
-    umma_commit(&sh.v_empty[vs]);
+#pragma unroll
+    for (int t = 0; t < C::NT; ++t)
+      if (wk.last_kv[t] >= 0) cnt[t] += wk.last_kv[t] + 1;
+    kv += wk.nkv;
+    ++items;
   }
 }
 
 // ---------------------------------------------------------------------------
-// Softmax + correction + epilogue (one warpgroup per query tile)
+// Softmax + correction + epilogue (warpgroup t owns query-tile slot t)
 // ---------------------------------------------------------------------------
 template <int HD, bool CAUSAL>
-__device__ void fwd_softmax_role(const FwdLaunch& p, FwdShared& sh, uint8_t* sQ, uint32_t tmem, int t,
-                                 const FwdWork<FwdCfg<HD>::NT, CAUSAL>& wk) {
+__device__ void fwd_softmax_role(const FwdLaunch& p, FwdShared& sh, uint8_t* sQ, uint32_t tmem, int t) {
   using C = FwdCfg<HD>;
   const int r = threadIdx.x & 127;
   const uint32_t lane_base = static_cast<uint32_t>((threadIdx.x >> 5) & 3) << 21;  // (warp % 4) * 32 lanes
@@ -275,143 +326,168 @@ __device__ void fwd_softmax_role(const FwdLaunch& p, FwdShared& sh, uint8_t* sQ,
   const uint32_t tO = tmem + lane_base + C::o_col(t);
   const int N = p.N;
   const int T = (N + 127) / 128;
-  const int qt = wk.qt[t];
-  const int last_kv = wk.last_kv[t];
-  const int row = qt * 128 + r;
   const float c2 = p.scale_log2;
   const uint64_t lim = p.wait_limit_ns;
+  const int total = total_items(p.BH, N, C::NT);
+  const int G = gridDim.x;
+  uint8_t* stage = sQ + t * C::TILE_BYTES;  // O staging: Q_t once its last S MMA is done
+  // After a timed-out wait a warp stops working but keeps passing every named
+  // barrier and arrival, so the warpgroup's barrier counts stay matched.
+  bool alive = true;
+  int cnt = 0;  // running S / P count of this slot
 
-  float m2 = -INFINITY;  // running max of S * scale * log2(e)
-  float l = 0.f;         // running sum of P~ (unrounded fp32)
-  bool ok = true;
-  for (int j = 0; j <= last_kv; ++j) {
-    ok = __all_sync(0xffffffffu, mbar_wait(&sh.s_full[t], j & 1, &sh.abort_flag, lim));
-    if (!ok) {
-      record_timeout(p.status, &sh.abort_flag, WHERE_FWD_SOFTMAX);
-      break;
-    }
-    tc_fence_after_sync();
-    float s[128];
-    {
-      uint32_t a[32], b[32], c[32], d[32];
-      tmem_ld32(tS + 0, a);
-      tmem_ld32(tS + 32, b);
-      tmem_ld32(tS + 64, c);
-      tmem_ld32(tS + 96, d);
-      tmem_ld_wait();
+  for (int k = 0; k * G < total; ++k) {
+    const int item = sched_item(k, blockIdx.x, G);
+    if (item >= total) continue;
+    const FwdWork<C::NT, CAUSAL> wk(item, p.BH, N);
+    const int qt = wk.qt[t];
+    const int last_kv = wk.last_kv[t];
+    const int row = qt * 128 + r;
+
+    float m2 = -INFINITY;  // reference max of S * scale * log2(e)
+    float l = 0.f;         // running sum of P~ (unrounded fp32)
+    for (int j = 0; j <= last_kv; ++j) {
+      alive = alive && __all_sync(0xffffffffu, mbar_wait(&sh.s_full[t], (cnt + j) & 1, &sh.abort_flag, lim));
+      if (!alive) {
+        record_timeout(p.status, &sh.abort_flag, WHERE_FWD_SOFTMAX);
+        break;
+      }
+      tc_fence_after_sync();
+      float s[128];
+      {
+        uint32_t a[32], b[32], c[32], d[32];
+        tmem_ld32(tS + 0, a);
+        tmem_ld32(tS + 32, b);
+        tmem_ld32(tS + 64, c);
+        tmem_ld32(tS + 96, d);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          s[i] = __uint_as_float(a[i]);
+          s[32 + i] = __uint_as_float(b[i]);
+          s[64 + i] = __uint_as_float(c[i]);
+          s[96 + i] = __uint_as_float(d[i]);
+        }
+      }
+      // Element-wise mask only on the key-tail tile and the causal diagonal tile.
+      const bool mask_tail = (j == T - 1) && (N & 127);
+      const bool mask_diag = CAUSAL && (j == qt);
+      if (mask_tail || mask_diag) {
+        int lim_col = N - 1 - j * 128;
+        if (CAUSAL) lim_col = min(lim_col, row - j * 128);
+#pragma unroll
+        for (int i = 0; i < 128; ++i)
+          if (i > lim_col) s[i] = -INFINITY;
+      }
+      // columns 0-7 seed four accumulators, then 8-127 two at a time each
+      float mx0 = fmaxf(s[0], s[1]), mx1 = fmaxf(s[2], s[3]), mx2 = fmaxf(s[4], s[5]), mx3 = fmaxf(s[6], s[7]);
+#pragma unroll
+      for (int i = 8; i < 128; i += 8) {
+        mx0 = fmax3(mx0, s[i], s[i + 1]);
+        mx1 = fmax3(mx1, s[i + 2], s[i + 3]);
+        mx2 = fmax3(mx2, s[i + 4], s[i + 5]);
+        mx3 = fmax3(mx3, s[i + 6], s[i + 7]);
+      }
+      const float mx = fmax3(fmaxf(mx0, mx1), mx2, mx3);
+      // m2 is the reference max the exponentials and both accumulators are
+      // relative to. It moves to the running max only when some row of the
+      // warp has outgrown it by more than kRescaleSlack (then O~ and l are
+      // rescaled); otherwise P~ = 2^(S c - m2) <= 2^kRescaleSlack. Either way
+      // O~ / l is the same in exact arithmetic.
+      const float m_run = fmaxf(m2, mx * c2);
+      const bool move = __any_sync(0xffffffffu, m_run > m2 + kRescaleSlack);
+      const float m_ref = move ? m_run : m2;
+      const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+      const float alpha = ex2_approx(m2 - m_use);  // 0 on the first block, 1 when the reference is kept
+      const float neg = -m_use;
+      float2 sum_a = make_float2(0.f, 0.f), sum_b = make_float2(0.f, 0.f);
+      uint32_t pk0[32], pk1[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        s[i] = __uint_as_float(a[i]);
-        s[32 + i] = __uint_as_float(b[i]);
-        s[64 + i] = __uint_as_float(c[i]);
-        s[96 + i] = __uint_as_float(d[i]);
+        const float2 x = ffma2_bcast(s[2 * i], s[2 * i + 1], c2, neg);
+        const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+        if (i & 1) sum_b = fadd2(sum_b, e); else sum_a = fadd2(sum_a, e);
+        pk0[i] = pack_bf16x2(e.x, e.y);
       }
-    }
-    // Element-wise mask only on the key-tail tile and the causal diagonal tile.
-    const bool mask_tail = (j == T - 1) && (N & 127);
-    const bool mask_diag = CAUSAL && (j == qt);
-    if (mask_tail || mask_diag) {
-      int lim_col = N - 1 - j * 128;
-      if (CAUSAL) lim_col = min(lim_col, row - j * 128);
+      tmem_st32(tP, pk0);  // first 64 keys of P~: frees registers for the second half
 #pragma unroll
-      for (int i = 0; i < 128; ++i)
-        if (i > lim_col) s[i] = -INFINITY;
-    }
-    // columns 0-7 seed four accumulators, then 8-127 two at a time each
-    float mx0 = fmaxf(s[0], s[1]), mx1 = fmaxf(s[2], s[3]), mx2 = fmaxf(s[4], s[5]), mx3 = fmaxf(s[6], s[7]);
+      for (int i = 0; i < 32; ++i) {
+        const float2 x = ffma2_bcast(s[64 + 2 * i], s[64 + 2 * i + 1], c2, neg);
+        const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+        if (i & 1) sum_b = fadd2(sum_b, e); else sum_a = fadd2(sum_a, e);
+        pk1[i] = pack_bf16x2(e.x, e.y);
+      }
+      const float2 sum2 = fadd2(sum_a, sum_b);
+      l = l * alpha + (sum2.x + sum2.y);
+      tmem_st32(tP + 32, pk1);
+      // Rescale O~ only when the reference max moved.
+      if (j > 0 && move) {
+#pragma unroll 1
+        for (int c = 0; c < HD; c += 32) {
+          uint32_t o[32];
+          tmem_ld32(tO + c, o);
+          tmem_ld_wait();
 #pragma unroll
-    for (int i = 8; i < 128; i += 8) {
-      mx0 = fmax3(mx0, s[i], s[i + 1]);
-      mx1 = fmax3(mx1, s[i + 2], s[i + 3]);
-      mx2 = fmax3(mx2, s[i + 4], s[i + 5]);
-      mx3 = fmax3(mx3, s[i + 6], s[i + 7]);
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(tO + c, o);
+        }
+      }
+      m2 = m_ref;
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(&sh.p_full[t]);
     }
-    const float mx = fmax3(fmaxf(mx0, mx1), mx2, mx3);
-    // m2 is the reference max the exponentials and both accumulators are
-    // relative to. It moves to the running max only when some row of the
-    // warp has outgrown it by more than kRescaleSlack (then O~ and l are
-    // rescaled); otherwise P~ = 2^(S c - m2) <= 2^kRescaleSlack. Either way
-    // O~ / l is the same in exact arithmetic.
-    const float m_run = fmaxf(m2, mx * c2);
-    const bool move = __any_sync(0xffffffffu, m_run > m2 + kRescaleSlack);
-    const float m_ref = move ? m_run : m2;
-    const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
-    const float alpha = ex2_approx(m2 - m_use);  // 0 on the first block, 1 when the reference is kept
-    const float neg = -m_use;
-    float2 sum_a = make_float2(0.f, 0.f), sum_b = make_float2(0.f, 0.f);
-    uint32_t pk0[32], pk1[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const float2 x = ffma2_bcast(s[2 * i], s[2 * i + 1], c2, neg);
-      const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-      if (i & 1) sum_b = fadd2(sum_b, e); else sum_a = fadd2(sum_a, e);
-      pk0[i] = pack_bf16x2(e.x, e.y);
+
+    // Epilogue: wait for the last O~ += P~ V, normalise, store through the
+    // (now free) Q_t smem; then hand O~_t and Q_t's smem back to the MMA and
+    // load threads for the next item.
+    const bool active = last_kv >= 0;
+    if (alive && active) {
+      alive = __all_sync(0xffffffffu, mbar_wait(&sh.pv_done[t], (cnt + last_kv) & 1, &sh.abort_flag, lim));
+      if (!alive) record_timeout(p.status, &sh.abort_flag, WHERE_FWD_SOFTMAX);
     }
-    tmem_st32(tP, pk0);  // first 64 keys of P~: frees registers for the second half
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const float2 x = ffma2_bcast(s[64 + 2 * i], s[64 + 2 * i + 1], c2, neg);
-      const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-      if (i & 1) sum_b = fadd2(sum_b, e); else sum_a = fadd2(sum_a, e);
-      pk1[i] = pack_bf16x2(e.x, e.y);
-    }
-    const float2 sum2 = fadd2(sum_a, sum_b);
-    l = l * alpha + (sum2.x + sum2.y);
-    tmem_st32(tP + 32, pk1);
-    // Rescale O~ only when the reference max moved.
-    if (j > 0 && move) {
+    tc_fence_after_sync();
+    if (alive && active) {
+      const float inv_l = 1.f / l;
+      const uint32_t stage_addr = smem_u32(stage);
 #pragma unroll 1
       for (int c = 0; c < HD; c += 32) {
         uint32_t o[32];
         tmem_ld32(tO + c, o);
         tmem_ld_wait();
+        if (c + 32 >= HD) {  // O~_t fully read: the next item's first PV may overwrite it
+          tc_fence_before_sync();
+          mbar_arrive(&sh.o_free[t]);
+        }
 #pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-        tmem_st32(tO + c, o);
+        for (int u = 0; u < 4; ++u) {
+          const int col = c + u * 8;
+          const uint32_t w0 = pack_bf16x2(__uint_as_float(o[u * 8 + 0]) * inv_l, __uint_as_float(o[u * 8 + 1]) * inv_l);
+          const uint32_t w1 = pack_bf16x2(__uint_as_float(o[u * 8 + 2]) * inv_l, __uint_as_float(o[u * 8 + 3]) * inv_l);
+          const uint32_t w2 = pack_bf16x2(__uint_as_float(o[u * 8 + 4]) * inv_l, __uint_as_float(o[u * 8 + 5]) * inv_l);
+          const uint32_t w3 = pack_bf16x2(__uint_as_float(o[u * 8 + 6]) * inv_l, __uint_as_float(o[u * 8 + 7]) * inv_l);
+          st_shared_v4(stage_addr + (col >> 6) * C::CHUNK_BYTES + sw128_offset(r, (col & 63) >> 3), w0, w1, w2, w3);
+        }
       }
+      fence_proxy_async_smem();
+      if (row < N) p.lse[static_cast<size_t>(wk.bh) * N + row] = (m2 + log2f(l)) * kLn2;
+    } else {
+      mbar_arrive(&sh.o_free[t]);
     }
-    m2 = m_ref;
-    tmem_st_wait();
-    tc_fence_before_sync();
-    mbar_arrive(&sh.p_full[t]);
-  }
-
-  // Epilogue: wait for the last O~ += P~ V, normalise, store.
-  if (ok && last_kv >= 0) {
-    ok = __all_sync(0xffffffffu, mbar_wait(&sh.pv_done[t], last_kv & 1, &sh.abort_flag, lim));
-    if (!ok) record_timeout(p.status, &sh.abort_flag, WHERE_FWD_SOFTMAX);
-  }
-  tc_fence_after_sync();
-  uint8_t* stage = sQ + t * C::TILE_BYTES;  // Q_t is no longer read by any MMA
-  const bool active = ok && last_kv >= 0;
-  if (active) {
-    const float inv_l = 1.f / l;
-    const uint32_t stage_addr = smem_u32(stage);
-#pragma unroll 1
-    for (int c = 0; c < HD; c += 32) {
-      uint32_t o[32];
-      tmem_ld32(tO + c, o);
-      tmem_ld_wait();
+    named_barrier_sync(1 + t, 128);
+    if (r == 0) {
+      if (alive && active && !*reinterpret_cast<volatile int*>(&sh.abort_flag)) {
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int col = c + u * 8;
-        const uint32_t w0 = pack_bf16x2(__uint_as_float(o[u * 8 + 0]) * inv_l, __uint_as_float(o[u * 8 + 1]) * inv_l);
-        const uint32_t w1 = pack_bf16x2(__uint_as_float(o[u * 8 + 2]) * inv_l, __uint_as_float(o[u * 8 + 3]) * inv_l);
-        const uint32_t w2 = pack_bf16x2(__uint_as_float(o[u * 8 + 4]) * inv_l, __uint_as_float(o[u * 8 + 5]) * inv_l);
-        const uint32_t w3 = pack_bf16x2(__uint_as_float(o[u * 8 + 6]) * inv_l, __uint_as_float(o[u * 8 + 7]) * inv_l);
-        st_shared_v4(stage_addr + (col >> 6) * C::CHUNK_BYTES + sw128_offset(r, (col & 63) >> 3), w0, w1, w2, w3);
+        for (int c = 0; c < C::CHUNKS; ++c)
+          tma_store_3d(&p.tmO, stage + c * C::CHUNK_BYTES, c * 64, qt * 128, wk.bh);
+        tma_store_commit();
+        tma_store_wait_read_all();  // the staging can be overwritten by the next Q tile
       }
+      mbar_arrive(&sh.q_free[t]);
     }
-    fence_proxy_async_smem();
+    if (active) cnt += last_kv + 1;
   }
-  named_barrier_sync(1 + t, 128);
-  if (active && r == 0 && !*reinterpret_cast<volatile int*>(&sh.abort_flag)) {
-#pragma unroll
-    for (int c = 0; c < C::CHUNKS; ++c) tma_store_3d(&p.tmO, stage + c * C::CHUNK_BYTES, c * 64, qt * 128, wk.bh);
-    tma_store_commit();
-    tma_store_wait_all();
-  }
-  if (active && row < N) p.lse[static_cast<size_t>(wk.bh) * N + row] = (m2 + log2f(l)) * kLn2;
+  if (r == 0) tma_store_wait_all();  // O stores complete before the CTA can exit
 }
 
 template <int HD, bool CAUSAL>
@@ -424,7 +500,6 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   uint8_t* sK = sQ + C::NT * C::TILE_BYTES;
   uint8_t* sV = sK + C::KST * C::TILE_BYTES;
   const int warp = threadIdx.x >> 5;
-  const FwdWork<C::NT, CAUSAL> wk(blockIdx.x, p.BH, p.N);
 
   if (threadIdx.x == 0) {
     mbar_init(&sh.q_full, 1);
@@ -438,6 +513,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       mbar_init(&sh.s_full[t], 1);
       mbar_init(&sh.p_full[t], 128);
       mbar_init(&sh.pv_done[t], 1);
+      mbar_init(&sh.o_free[t], 128);
+      mbar_init(&sh.q_free[t], 1);
     }
     sh.abort_flag = 0;
     fence_mbarrier_init();
@@ -452,11 +529,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   const uint32_t tmem = sh.tmem_base;
 
   if (warp == kLoadWarp) {
-    if (lane_id() == 0) fwd_load_role<HD, CAUSAL>(p, sh, sQ, sK, sV, wk);
+    if (lane_id() == 0) fwd_load_role<HD, CAUSAL>(p, sh, sQ, sK, sV);
   } else if (warp == kMmaWarp) {
-    if (lane_id() == 0) fwd_mma_role<HD, CAUSAL>(p, sh, sQ, sK, sV, tmem, wk);
+    if (lane_id() == 0) fwd_mma_role<HD, CAUSAL>(p, sh, sQ, sK, sV, tmem);
   } else if (warp < 4 * C::NT) {
-    fwd_softmax_role<HD, CAUSAL>(p, sh, sQ, tmem, warp >> 2, wk);
+    fwd_softmax_role<HD, CAUSAL>(p, sh, sQ, tmem, warp >> 2);
   }
 
   tc_fence_before_sync();
@@ -472,8 +549,11 @@ cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const int T = (a.N + 127) / 128;
-  const long long blocks = static_cast<long long>(a.BH) * ((T + C::NT - 1) / C::NT);
-  kern<<<static_cast<unsigned>(blocks), kThreads, C::SMEM_BYTES, stream>>>(a);
+  const long long items = static_cast<long long>(a.BH) * ((T + C::NT - 1) / C::NT);
+  // Persistent: one CTA per SM (the smem footprint allows no more), each
+  // looping over its share of the items.
+  const long long grid = items < a.num_sms ? items : a.num_sms;
+  kern<<<static_cast<unsigned>(grid), kThreads, C::SMEM_BYTES, stream>>>(a);
   return cudaGetLastError();
 }
 
