@@ -149,7 +149,7 @@ int round_up_128(int n) { return (n + 127) / 128 * 128; }
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct BwdWorkspaceLayout {
-  size_t D_off, lse2_off, dq_off, total;
+  size_t D_off, lse2_off, dq_off, sched_off, total;
 };
 
 BwdWorkspaceLayout bwd_layout(long long BH, int N, int d) {
@@ -158,7 +158,8 @@ BwdWorkspaceLayout bwd_layout(long long BH, int N, int d) {
   w.D_off = 0;
   w.lse2_off = align_up(w.D_off + rows * 4, 256);
   w.dq_off = align_up(w.lse2_off + rows * 4, 256);
-  w.total = align_up(w.dq_off + rows * static_cast<size_t>(d) * 4, 256);
+  w.sched_off = align_up(w.dq_off + rows * static_cast<size_t>(d) * 4, 256);
+  w.total = w.sched_off + 256;
   return w;
 }
 
@@ -270,9 +271,12 @@ fa_status_t prepare_bwd(const BwdTensors& t, int B, int H, int N, int d, int cau
   a->dO = static_cast<const __nv_bfloat16*>(t.dO);
   a->lse = t.lse;
   a->dq = static_cast<__nv_bfloat16*>(t.dq);
+  a->dk = static_cast<__nv_bfloat16*>(t.dk);
+  a->dv = static_cast<__nv_bfloat16*>(t.dv);
   a->D = reinterpret_cast<float*>(ws + wl.D_off);
   a->lse2 = reinterpret_cast<float*>(ws + wl.lse2_off);
   a->dq_acc = reinterpret_cast<float*>(ws + wl.dq_off);
+  a->sched = reinterpret_cast<uint32_t*>(ws + wl.sched_off);
   if (!make_map_f32_acc(&a->tmdQacc, a->dq_acc, BH, round_up_128(N), d)) return FA_ERR_CUDA;
   a->status = ds->status;
   a->N = N;

@@ -15,22 +15,26 @@
 //      base-2 logsumexp L*log2(e), and zeroes the fp32 dQ accumulator. Every
 //      head is padded to a multiple of 128 rows; padding rows get D = 0 and
 //      L = +inf so their probabilities are exactly 0.
-//   2. fa_bwd_kernel: one CTA per (head, 128-key tile j). Everything is
-//      computed transposed, with keys on the 128 TMEM lanes:
+//   2. fa_bwd_kernel: persistent, one CTA per SM taking work items
+//      (head, 128-key tile j) from a global counter (causal: longest first).
+//      Everything is computed transposed, with keys on the 128 TMEM lanes:
 //        S^T = K_j Q_i^T and dP^T = V_j dO_i^T   (SS MMAs into TMEM)
-//        warpgroup 0, thread r = key r: P^T = 2^(S^T scale log2e - L log2e),
+//        two softmax warpgroups, each owning 64 of the tile's queries; thread
+//          r = key r: P^T = 2^(S^T scale log2e - L log2e) and
 //          dS^T = P^T o (dP^T - D) * scale; P^T (bf16) goes back to TMEM,
 //          dS^T (bf16) to a 128-byte-swizzled smem tile
 //        dV += P^T dO_i      (A = P^T from TMEM, B = dO_i MN-major)
 //        dK += dS^T Q_i      (A = dS^T smem, K-major; B = Q_i MN-major)
-//        dQ_i = dS K_j       (A = the same smem tile read MN-major,
-//                             B = K_j MN-major), into TMEM, queries on lanes
-//        warpgroup 1, thread q = query q: reads its dQ_i row from TMEM and
-//          adds it into the fp32 accumulator with 16-byte vector reductions.
-//      Two 128-column TMEM regions alternate: S^T(i) and later dQ_i use one,
-//      dP^T(i) and then P^T(i) the other; S^T(i+1) reuses the P^T region once
-//      dV(i) is done and dP^T(i+1) reuses the dQ region once it was drained.
-//      dK, dV (fp32, TMEM) are written once at the end through TMA stores.
+//        dQ_i (d = 64) = dS K_j, or dQ_i^T (d = 128) = K_j^T dS^T, from the
+//          same smem tile read MN-major, into TMEM; the softmax warpgroups
+//          drain it into the fp32 accumulator with reductions (d = 128:
+//          scalar reductions that cover whole 128-byte lines; d = 64: TMA
+//          reduce-adds of a swizzled smem staging tile).
+//      Two 128-column TMEM regions alternate: S^T(i) and then P^T(i) use
+//      one, dP^T(i) and then dQ_i the other; S^T(i+1) reuses the P^T region
+//      once dV(i) is done and dP^T(i+1) reuses the dQ region once it was
+//      drained. dK, dV (fp32, TMEM) are written once per item, straight from
+//      TMEM to global memory, while the MMA warp starts the next item.
 //   3. bwd_post_kernel (HBM-bound): dQ = bf16(accumulator).
 //
 // TMEM columns (512 allocated): dK [0, d), dV [d, 2d), region 0 [256, 384),
@@ -79,27 +83,49 @@ struct BwdShared {
   uint64_t kv_full;
   uint64_t qdo_full[4], qdo_empty[4];
   uint64_t s_full, dp_full, pa_ready, ds_ready, pv_done, dq_full, dq_free, acc_done;
+  uint64_t acc_free;  // dK, dV of the previous item read out of TMEM
+  // Work-item queue filled by the load thread (item >= BH*T ends the loop).
+  uint64_t item_full[4], item_empty[4];
+  int item_ring[4];
   uint32_t tmem_base;
   int abort_flag;
 };
 
 // Work item: key tile j of head bh; query tiles i0..T-1 (causal: i0 = j).
+// Causal items are numbered most-work-first (key tile j meets T - j query
+// tiles); non-causal items of one head are adjacent (Q/dO reuse in L2).
 template <bool CAUSAL>
 struct BwdWork {
   int bh, j, i0, T;
-  __device__ BwdWork(int block, int BH, int N) {
+  __device__ BwdWork(int item, int BH, int N) {
     T = (N + 127) / 128;
-    if (CAUSAL) {  // most work first: key tile j meets T - j query tiles
-      bh = block % BH;
-      j = block / BH;
+    if (CAUSAL) {
+      bh = item % BH;
+      j = item / BH;
     } else {
-      bh = block / T;
-      j = block % T;
+      bh = item / T;
+      j = item % T;
     }
     i0 = CAUSAL ? j : 0;
   }
   __device__ int n_iter() const { return T - i0; }
 };
+
+// Dynamic schedule: CTA b starts on item b; afterwards the load thread claims
+// item G + atomicAdd(sched[0], 1) each time it finishes issuing an item's
+// loads, so CTAs that run ahead take more items (causal items come heaviest
+// first). The claimed index goes through a 4-slot smem queue to the MMA
+// thread and the 256 softmax threads.
+constexpr int kItemSlots = 4;
+constexpr int kItemConsumers = 1 + 256;
+
+__device__ __forceinline__ int take_item(BwdShared& sh, int u, uint64_t lim) {
+  const int s = u % kItemSlots;
+  if (!mbar_wait(&sh.item_full[s], (u / kItemSlots) & 1, &sh.abort_flag, lim)) return -1;
+  const int item = *reinterpret_cast<volatile int*>(&sh.item_ring[s]);
+  mbar_arrive(&sh.item_empty[s]);
+  return item;
+}
 
 // ---------------------------------------------------------------------------
 // 1. preprocess
@@ -110,8 +136,10 @@ template <int HD>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
                                                       const __nv_bfloat16* __restrict__ dO,
                                                       const float* __restrict__ lse, float* __restrict__ D,
-                                                      float* __restrict__ lse2, float* __restrict__ dq_acc, int N,
-                                                      int Npad, long long total_rows) {
+                                                      float* __restrict__ lse2, float* __restrict__ dq_acc,
+                                                      uint32_t* __restrict__ sched, int N, int Npad,
+                                                      long long total_rows) {
+  if (blockIdx.x == 0 && threadIdx.x < 2) sched[threadIdx.x] = 0u;
   constexpr int LPR = HD / 8;  // lanes per row, 16 bytes of O and dO each
   constexpr int RPW = 32 / LPR;
   const long long row = (static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32) * RPW +
@@ -177,65 +205,105 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const float* __restrict__
 // ---------------------------------------------------------------------------
 // 2. main kernel roles
 // ---------------------------------------------------------------------------
+// TMA producer (one thread). Per item: the first Q_i/dO_i tile, then K_j and
+// V_j once every MMA of the previous item has completed (they read the old
+// K_j/V_j), then the remaining Q_i/dO_i tiles through the ring (global tile
+// counter g).
 template <int HD, bool CAUSAL>
 __device__ void bwd_load_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sK, uint8_t* sV, uint8_t* sQ,
-                              uint8_t* sdO, const BwdWork<CAUSAL>& wk) {
+                              uint8_t* sdO) {
   using C = BwdCfg<HD>;
   tma_prefetch_desc(&p.tmQ);
   tma_prefetch_desc(&p.tmK);
   tma_prefetch_desc(&p.tmV);
   tma_prefetch_desc(&p.tmdO);
   tma_prefetch_desc(&p.tmdQacc);
-  mbar_arrive_expect_tx(&sh.kv_full, 2 * C::TILE_BYTES);
-#pragma unroll
-  for (int c = 0; c < C::CHUNKS; ++c) {
-    tma_load_3d(sK + c * C::CHUNK_BYTES, &p.tmK, &sh.kv_full, c * 64, wk.j * 128, wk.bh);
-    tma_load_3d(sV + c * C::CHUNK_BYTES, &p.tmV, &sh.kv_full, c * 64, wk.j * 128, wk.bh);
-  }
-  const int n_iter = wk.n_iter();
-  int issued = 0;
+  const int T = (p.N + 127) / 128;
+  const int total = p.BH * T;
+  const int G = gridDim.x;
+  const uint64_t lim = p.wait_limit_ns;
+  int g = 0, items = 0, issued = 0, kv_issued = 0;
   bool aborted = false;
-  for (int n = 0; n < n_iter; ++n) {
-    const int s = n % C::QST;
-    if (n >= C::QST && !mbar_wait(&sh.qdo_empty[s], ((n / C::QST) - 1) & 1, &sh.abort_flag, p.wait_limit_ns)) {
-      aborted = true;
-      break;
-    }
-    const int i = wk.i0 + n;
+  auto publish = [&](int u, int item) -> bool {
+    const int s = u % kItemSlots;
+    if (u >= kItemSlots && !mbar_wait(&sh.item_empty[s], ((u / kItemSlots) - 1) & 1, &sh.abort_flag, lim))
+      return false;
+    *reinterpret_cast<volatile int*>(&sh.item_ring[s]) = item;
+    mbar_arrive(&sh.item_full[s]);
+    return true;
+  };
+  auto load_qdo = [&](int gg, int i, int bh) -> bool {
+    const int s = gg % C::QST;
+    if (gg >= C::QST && !mbar_wait(&sh.qdo_empty[s], ((gg / C::QST) - 1) & 1, &sh.abort_flag, lim)) return false;
     mbar_arrive_expect_tx(&sh.qdo_full[s], 2 * C::TILE_BYTES);
 #pragma unroll
     for (int c = 0; c < C::CHUNKS; ++c) {
-      tma_load_3d(sQ + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &p.tmQ, &sh.qdo_full[s], c * 64, i * 128, wk.bh);
-      tma_load_3d(sdO + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &p.tmdO, &sh.qdo_full[s], c * 64, i * 128, wk.bh);
+      tma_load_3d(sQ + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &p.tmQ, &sh.qdo_full[s], c * 64, i * 128, bh);
+      tma_load_3d(sdO + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &p.tmdO, &sh.qdo_full[s], c * 64, i * 128, bh);
     }
     ++issued;
+    return true;
+  };
+  int item = blockIdx.x;  // the grid never exceeds the item count
+  while (!aborted) {
+    if (!publish(items, item)) {
+      aborted = true;
+      break;
+    }
+    if (item >= total) break;
+    const BwdWork<CAUSAL> wk(item, p.BH, p.N);
+    const int n_iter = wk.n_iter();
+    if (!load_qdo(g, wk.i0, wk.bh)) {
+      aborted = true;
+      break;
+    }
+    if (items > 0 && !mbar_wait(&sh.acc_done, (items - 1) & 1, &sh.abort_flag, lim)) {
+      aborted = true;
+      break;
+    }
+    mbar_arrive_expect_tx(&sh.kv_full, 2 * C::TILE_BYTES);
+#pragma unroll
+    for (int c = 0; c < C::CHUNKS; ++c) {
+      tma_load_3d(sK + c * C::CHUNK_BYTES, &p.tmK, &sh.kv_full, c * 64, wk.j * 128, wk.bh);
+      tma_load_3d(sV + c * C::CHUNK_BYTES, &p.tmV, &sh.kv_full, c * 64, wk.j * 128, wk.bh);
+    }
+    ++kv_issued;
+    for (int n = 1; n < n_iter; ++n) {
+      if (!load_qdo(g + n, wk.i0 + n, wk.bh)) {
+        aborted = true;
+        break;
+      }
+    }
+    g += n_iter;
+    ++items;
+    if (!aborted) item = G + static_cast<int>(atomicAdd(p.sched, 1u));
+  }
+  // The last CTA done claiming resets the counter for the next launch.
+  if (atomicAdd(p.sched + 1, 1u) == static_cast<uint32_t>(G - 1)) {
+    atomicExch(p.sched, 0u);
+    atomicExch(p.sched + 1, 0u);
   }
   const int zero = 0;
   if (aborted) {
     record_timeout(p.status, &sh.abort_flag, WHERE_BWD_LOAD);
     for (int n = max(0, issued - C::QST); n < issued; ++n)
-      mbar_wait(&sh.qdo_full[n % C::QST], (n / C::QST) & 1, &zero, p.wait_limit_ns);
+      mbar_wait(&sh.qdo_full[n % C::QST], (n / C::QST) & 1, &zero, lim);
   }
-  mbar_wait(&sh.kv_full, 0, &zero, p.wait_limit_ns);
+  if (kv_issued > 0) mbar_wait(&sh.kv_full, (kv_issued - 1) & 1, &zero, lim);
 }
 
-// One thread issues every MMA. Per query tile n (regions A = S^T then P^T,
-// B = dP^T then dQ_i):
-//   dV += P^T dO_n       after phase A(n)           (overlaps phase B(n))
-//   dK += dS^T Q_n       after phase B(n)
-//   dQ_n = dS K_j -> B   after phase B(n)
-//   S^T(n+1) -> A        after dV(n) released P^T   (overlaps the dQ drain)
-//   dP^T(n+1) -> B       after the dQ drain         (overlaps phase A(n+1))
-// One thread issues every MMA. Per query tile n (region A: S^T then P^T;
-// region B: dP^T then dQ_n):
+// One thread issues every MMA. Per query tile n of an item (global index g;
+// region A: S^T then P^T; region B: dP^T then dQ_n):
 //   dV += P^T dO_n        after phase A(n)          (overlaps phase B(n))
 //   S^T(n+1) -> A         after dV(n) released P^T (overlaps phase B(n))
 //   dK += dS^T Q_n        after phase B(n)          (overlaps phase A(n+1))
 //   dQ_n -> B             after phase B(n)          (overlaps phase A(n+1))
-//   dP^T(n+1) -> B        after the drain warpgroup read dQ_n out of TMEM
+//   dP^T(n+1) -> B        after the dQ_n drain
+// An item's first dV/dK (which overwrite the accumulators) wait until the
+// previous item's epilogue has read dK/dV out of TMEM.
 template <int HD, bool CAUSAL>
 __device__ void bwd_mma_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sK, uint8_t* sV, uint8_t* sQ,
-                             uint8_t* sdO, uint8_t* sDS, uint32_t tmem, const BwdWork<CAUSAL>& wk) {
+                             uint8_t* sdO, uint8_t* sDS, uint32_t tmem) {
   using C = BwdCfg<HD>;
   constexpr uint32_t kIdescSq = make_idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
   constexpr uint32_t kIdescAcc = make_idesc_bf16_f32(128, HD, false, true);   // dV, dK
@@ -243,7 +311,8 @@ __device__ void bwd_mma_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sK, uin
   const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV), q_addr = smem_u32(sQ), do_addr = smem_u32(sdO),
                  ds_addr = smem_u32(sDS);
   const uint64_t lim = p.wait_limit_ns;
-  const int n_iter = wk.n_iter();
+  const int T = (p.N + 127) / 128;
+  const int total = p.BH * T;
 
   // D[tmem] = A (128 x HD, K-major) * B (128 x HD, K-major)^T
   auto issue_sq = [&](uint32_t d_col, uint32_t a_addr, uint32_t b_addr) {
@@ -256,112 +325,129 @@ __device__ void bwd_mma_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sK, uin
   };
   auto fail = [&]() { record_timeout(p.status, &sh.abort_flag, WHERE_BWD_MMA); };
 
-  if (!mbar_wait(&sh.kv_full, 0, &sh.abort_flag, lim) || !mbar_wait(&sh.qdo_full[0], 0, &sh.abort_flag, lim)) {
-    fail();
-    return;
-  }
-  tc_fence_after_sync();
-  issue_sq(C::REG_A, k_addr, q_addr);  // S^T(i0)
-  umma_commit(&sh.s_full);
-  issue_sq(C::REG_B, v_addr, do_addr);  // dP^T(i0)
-  umma_commit(&sh.dp_full);
+  int g = 0, items = 0;
+  while (true) {
+    const int item = take_item(sh, items, lim);
+    if (item < 0) return fail();
+    if (item >= total) break;
+    const BwdWork<CAUSAL> wk(item, p.BH, p.N);
+    const int n_iter = wk.n_iter();
+    const int s0 = g % C::QST;
+    if (!mbar_wait(&sh.kv_full, items & 1, &sh.abort_flag, lim) ||
+        !mbar_wait(&sh.qdo_full[s0], (g / C::QST) & 1, &sh.abort_flag, lim))
+      return fail();
+    // Region A held the previous item's last P^T, region B its last dQ.
+    if (g > 0 && !mbar_wait(&sh.pv_done, (g - 1) & 1, &sh.abort_flag, lim)) return fail();
+    tc_fence_after_sync();
+    issue_sq(C::REG_A, k_addr, q_addr + s0 * C::TILE_BYTES);  // S^T(first)
+    umma_commit(&sh.s_full);
+    if (g > 0 && !mbar_wait(&sh.dq_free, (g - 1) & 1, &sh.abort_flag, lim)) return fail();
+    tc_fence_after_sync();
+    issue_sq(C::REG_B, v_addr, do_addr + s0 * C::TILE_BYTES);  // dP^T(first)
+    umma_commit(&sh.dp_full);
 
-  for (int n = 0; n < n_iter; ++n) {
-    const int s = n % C::QST;
-    const bool has_next = n + 1 < n_iter;
-    const int s1 = (n + 1) % C::QST;
-    const uint32_t qa = q_addr + s * C::TILE_BYTES, doa = do_addr + s * C::TILE_BYTES;
-    if (!mbar_wait(&sh.pa_ready, n & 1, &sh.abort_flag, lim)) return fail();
-    tc_fence_after_sync();
-    // dV += P^T dO_n; P^T (bf16) sits in columns [0,32) and [64,96) of region A
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks)
-      umma_ts(tmem + C::DV_COL, tmem + C::REG_A + (ks >> 2) * 64 + (ks & 3) * 8,
-              make_smem_desc_sw128(doa + ks * 2048, C::CHUNK_BYTES, 1024), kIdescAcc, (n > 0 || ks > 0) ? 1u : 0u);
-    umma_commit(&sh.pv_done);
-    if (has_next) {
-      // S^T(n+1) overwrites P^T(n): wait until dV(n) has read it.
-      if (!mbar_wait(&sh.qdo_full[s1], ((n + 1) / C::QST) & 1, &sh.abort_flag, lim)) return fail();
-      if (!mbar_wait(&sh.pv_done, n & 1, &sh.abort_flag, lim)) return fail();
+    for (int n = 0; n < n_iter; ++n, ++g) {
+      const int s = g % C::QST;
+      const bool has_next = n + 1 < n_iter;
+      const int s1 = (g + 1) % C::QST;
+      const uint32_t qa = q_addr + s * C::TILE_BYTES, doa = do_addr + s * C::TILE_BYTES;
+      if (!mbar_wait(&sh.pa_ready, g & 1, &sh.abort_flag, lim)) return fail();
+      if (n == 0 && items > 0 && !mbar_wait(&sh.acc_free, (items - 1) & 1, &sh.abort_flag, lim)) return fail();
       tc_fence_after_sync();
-      issue_sq(C::REG_A, k_addr, q_addr + s1 * C::TILE_BYTES);
-      umma_commit(&sh.s_full);
-    }
-    if (!mbar_wait(&sh.ds_ready, n & 1, &sh.abort_flag, lim)) return fail();
-    tc_fence_after_sync();
-    // dK += dS^T Q_n
+      // dV += P^T dO_n; P^T (bf16) sits in columns [0,32) and [64,96) of region A
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks)
-      umma_ss(tmem + C::DK_COL, make_smem_desc_sw128(ds_addr + (ks >> 2) * C::CHUNK_BYTES + (ks & 3) * 32, 16, 1024),
-              make_smem_desc_sw128(qa + ks * 2048, C::CHUNK_BYTES, 1024), kIdescAcc, (n > 0 || ks > 0) ? 1u : 0u);
-    // dQ_n into region B. d = 128: dQ_n^T = K_j^T dS^T (head-dim columns on
-    // the lanes, queries along the columns), so the drain's reductions cover
-    // whole 128-byte lines. d = 64: dQ_n = dS K_j (queries on the lanes).
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      const uint64_t ds_mn = make_smem_desc_sw128(ds_addr + ks * 2048, C::CHUNK_BYTES, 1024);
-      const uint64_t k_mn = make_smem_desc_sw128(k_addr + ks * 2048, C::CHUNK_BYTES, 1024);
-      if constexpr (C::DQ_T)
-        umma_ss(tmem + C::REG_B, k_mn, ds_mn, kIdescDq, ks > 0 ? 1u : 0u);
-      else
-        umma_ss(tmem + C::REG_B, ds_mn, k_mn, kIdescDq, ks > 0 ? 1u : 0u);
-    }
-    umma_commit(&sh.dq_full);
-    umma_commit(&sh.qdo_empty[s]);
-    if (has_next) {
-      if (!mbar_wait(&sh.dq_free, n & 1, &sh.abort_flag, lim)) return fail();
+      for (int ks = 0; ks < 8; ++ks)
+        umma_ts(tmem + C::DV_COL, tmem + C::REG_A + (ks >> 2) * 64 + (ks & 3) * 8,
+                make_smem_desc_sw128(doa + ks * 2048, C::CHUNK_BYTES, 1024), kIdescAcc, (n > 0 || ks > 0) ? 1u : 0u);
+      umma_commit(&sh.pv_done);
+      if (has_next) {
+        // S^T(n+1) overwrites P^T(n): wait until dV(n) has read it.
+        if (!mbar_wait(&sh.qdo_full[s1], ((g + 1) / C::QST) & 1, &sh.abort_flag, lim)) return fail();
+        if (!mbar_wait(&sh.pv_done, g & 1, &sh.abort_flag, lim)) return fail();
+        tc_fence_after_sync();
+        issue_sq(C::REG_A, k_addr, q_addr + s1 * C::TILE_BYTES);
+        umma_commit(&sh.s_full);
+      }
+      if (!mbar_wait(&sh.ds_ready, g & 1, &sh.abort_flag, lim)) return fail();
       tc_fence_after_sync();
-      issue_sq(C::REG_B, v_addr, do_addr + s1 * C::TILE_BYTES);  // dP^T(n+1) over the drained dQ_n
-      umma_commit(&sh.dp_full);
+      // dK += dS^T Q_n
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)
+        umma_ss(tmem + C::DK_COL, make_smem_desc_sw128(ds_addr + (ks >> 2) * C::CHUNK_BYTES + (ks & 3) * 32, 16, 1024),
+                make_smem_desc_sw128(qa + ks * 2048, C::CHUNK_BYTES, 1024), kIdescAcc, (n > 0 || ks > 0) ? 1u : 0u);
+      // dQ_n into region B. d = 128: dQ_n^T = K_j^T dS^T (head-dim columns on
+      // the lanes, queries along the columns), so the drain's reductions
+      // cover whole 128-byte lines. d = 64: dQ_n = dS K_j (queries on lanes).
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint64_t ds_mn = make_smem_desc_sw128(ds_addr + ks * 2048, C::CHUNK_BYTES, 1024);
+        const uint64_t k_mn = make_smem_desc_sw128(k_addr + ks * 2048, C::CHUNK_BYTES, 1024);
+        if constexpr (C::DQ_T)
+          umma_ss(tmem + C::REG_B, k_mn, ds_mn, kIdescDq, ks > 0 ? 1u : 0u);
+        else
+          umma_ss(tmem + C::REG_B, ds_mn, k_mn, kIdescDq, ks > 0 ? 1u : 0u);
+      }
+      umma_commit(&sh.dq_full);
+      umma_commit(&sh.qdo_empty[s]);
+      if (has_next) {
+        if (!mbar_wait(&sh.dq_free, g & 1, &sh.abort_flag, lim)) return fail();
+        tc_fence_after_sync();
+        issue_sq(C::REG_B, v_addr, do_addr + s1 * C::TILE_BYTES);  // dP^T(n+1) over the drained dQ_n
+        umma_commit(&sh.dp_full);
+      }
     }
+    umma_commit(&sh.acc_done);
+    ++items;
   }
-  umma_commit(&sh.acc_done);
 }
 
 // Warpgroup w (w = 0, 1) owns query columns [64w, 64w + 64) of every tile:
 // thread r owns key r (TMEM lane r) in phases A and B, and head-dim column r
 // (d = 128) or query r (d = 64) in the dQ drain. Per tile n the order is
 // B(n), A(n+1), drain(n): phase A(n+1) overlaps the dK(n) and dQ_n MMAs and
-// the drain's reductions overlap dP^T(n+1) and dV(n+1).
+// the drain's reductions overlap dP^T(n+1) and dV(n+1). After an item's last
+// tile, warpgroup 0 writes dK_j and warpgroup 1 dV_j straight from TMEM to
+// global memory while the MMA warp already starts the next item.
 template <int HD, bool CAUSAL>
 __device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS, float* sLD, uint8_t* sDQ,
-                                 uint32_t tmem, int w, const BwdWork<CAUSAL>& wk) {
+                                 uint32_t tmem, int w) {
   using C = BwdCfg<HD>;
   const int r = threadIdx.x & 127;
   const uint32_t lane_base = static_cast<uint32_t>((threadIdx.x >> 5) & 3) << 21;
-  const int key = wk.j * 128 + r;
-  const bool key_valid = key < p.N;
   const float c2 = p.scale_log2;
   const float sc = p.scale;
   const uint64_t lim = p.wait_limit_ns;
   const uint32_t ds_chunk = smem_u32(sDS) + w * C::CHUNK_BYTES;  // queries 64w .. 64w+63
   float* ld_l2 = sLD + w * 128;  // 64 base-2 logsumexps, then 64 scaled D values
   float* ld_d = ld_l2 + 64;
-  const float* lse2_bh = p.lse2 + static_cast<size_t>(wk.bh) * p.Npad + 64 * w;
-  const float* D_bh = p.D + static_cast<size_t>(wk.bh) * p.Npad + 64 * w;
-  const int n_iter = wk.n_iter();
   const uint32_t bar_id = 1 + w;
   const uint32_t tA = tmem + lane_base + C::REG_A + 64 * w;
   const uint32_t tB = tmem + lane_base + C::REG_B + 64 * w;
+  const int T = (p.N + 127) / 128;
+  const int total = p.BH * T;
   bool alive = true;
   // P^T of the current tile as the bf16 pairs written to TMEM, kept from
   // phase A to phase B: dS uses the same rounded P as the dV MMA.
   uint32_t pk[32];
 
-  // L2 / D of query tile i for this warpgroup's 64 columns: thread r < 64
-  // loads L2[r], thread r >= 64 loads D[r - 64] * scale.
-  auto fetch_ld = [&](int i) -> float {
-    return r < 64 ? __ldg(lse2_bh + i * 128 + r) : __ldg(D_bh + i * 128 + (r - 64)) * sc;
+  // L2 / D of query tile i of head bh for this warpgroup's 64 columns:
+  // thread r < 64 loads L2[r], thread r >= 64 loads D[r - 64] * scale.
+  auto fetch_ld = [&](int bh, int i) -> float {
+    const size_t row = static_cast<size_t>(bh) * p.Npad + i * 128 + 64 * w;
+    return r < 64 ? __ldg(p.lse2 + row + r) : __ldg(p.D + row + (r - 64)) * sc;
+  };
+  auto wait_all = [&](uint64_t* bar, int parity, int where) {
+    alive = alive && __all_sync(0xffffffffu, mbar_wait(bar, parity, &sh.abort_flag, lim));
+    if (!alive) record_timeout(p.status, &sh.abort_flag, where);
+    tc_fence_after_sync();
   };
 
-  // ---- phase A: P^T = 2^(S^T * scale * log2e - L2), written back to TMEM as bf16.
-  // After a timed-out wait a warp stops working but still passes every named
-  // barrier, so the warpgroup's barrier counts stay matched.
-  auto phase_a = [&](int n) {
-    const int i = wk.i0 + n;
-    alive = alive && __all_sync(0xffffffffu, mbar_wait(&sh.s_full, n & 1, &sh.abort_flag, lim));
-    if (!alive) record_timeout(p.status, &sh.abort_flag, WHERE_BWD_SOFTMAX);
-    tc_fence_after_sync();
+  // ---- phase A of query tile i (global tile g): P^T = 2^(S^T * scale *
+  // log2e - L2), written back to TMEM as bf16. After a timed-out wait a warp
+  // stops working but still passes every named barrier, so the warpgroup's
+  // barrier counts stay matched.
+  auto phase_a = [&](const BwdWork<CAUSAL>& wk, int i, int g) {
+    wait_all(&sh.s_full, g & 1, WHERE_BWD_SOFTMAX);
     if (!alive) return;
     float pv[64];
     {
@@ -377,6 +463,7 @@ __device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS
     }
     // Only the key-tail tile and the causal diagonal tile need masking:
     // query (64w + c) sees key r only if 64w + c >= r.
+    const bool key_valid = wk.j * 128 + r < p.N;
     const bool masked = !key_valid || (CAUSAL && i == wk.j);
     const int c_lo = !key_valid ? 64 : ((CAUSAL && i == wk.j) ? r - 64 * w : 0);
 #pragma unroll
@@ -404,10 +491,8 @@ __device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS
   };
 
   // ---- phase B: dS^T = P^T o (dP^T - D) * scale -> smem (bf16, swizzled)
-  auto phase_b = [&](int n) {
-    alive = alive && __all_sync(0xffffffffu, mbar_wait(&sh.dp_full, n & 1, &sh.abort_flag, lim));
-    if (!alive) record_timeout(p.status, &sh.abort_flag, WHERE_BWD_SOFTMAX);
-    tc_fence_after_sync();
+  auto phase_b = [&](int g) {
+    wait_all(&sh.dp_full, g & 1, WHERE_BWD_SOFTMAX);
     if (!alive) return;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -439,12 +524,9 @@ __device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS
     mbar_arrive(&sh.ds_ready);
   };
 
-  // ---- dQ drain of tile n out of region B
-  auto drain = [&](int n) {
-    const int i = wk.i0 + n;
-    alive = alive && __all_sync(0xffffffffu, mbar_wait(&sh.dq_full, n & 1, &sh.abort_flag, lim));
-    if (!alive) record_timeout(p.status, &sh.abort_flag, WHERE_BWD_DQ);
-    tc_fence_after_sync();
+  // ---- dQ drain of query tile i (global tile g) out of region B
+  auto drain = [&](int bh, int i, int g) {
+    wait_all(&sh.dq_full, g & 1, WHERE_BWD_DQ);
     if constexpr (C::DQ_T) {
       // lane r = head-dim column r, this warpgroup's 64 queries along the
       // columns: for a fixed query the warp's 32 lanes add into 32
@@ -452,7 +534,7 @@ __device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS
       // the tile for TMA reduce-adds through the dS^T tile measured slower:
       // the staging reads land on the softmax warps' path.)
       if (!alive) return;
-      float* dst = p.dq_acc + (static_cast<size_t>(wk.bh) * p.Npad + i * 128 + 64 * w) * HD + r;
+      float* dst = p.dq_acc + (static_cast<size_t>(bh) * p.Npad + i * 128 + 64 * w) * HD + r;
       uint32_t v[64];
       tmem_ld32(tB, *reinterpret_cast<uint32_t(*)[32]>(v));
       tmem_ld32(tB + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
@@ -483,76 +565,90 @@ __device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS
       }
       named_barrier_sync(bar_id, 128);
       if (alive && r == 0) {
-        tma_reduce_add_3d(&p.tmdQacc, chunk, 32 * w, i * 128, wk.bh);
+        tma_reduce_add_3d(&p.tmdQacc, chunk, 32 * w, i * 128, bh);
         tma_store_commit();
       }
     }
   };
 
-  {
-    const float v0 = fetch_ld(wk.i0);
-    sLD[w * 128 + r] = v0;
-    named_barrier_sync(bar_id, 128);
-  }
-  phase_a(0);
-  for (int n = 0; n < n_iter; ++n) {
-    const bool has_next = n + 1 < n_iter;
-    const float next_ld = has_next ? fetch_ld(wk.i0 + n + 1) : 0.f;  // lands during phase B
-    phase_b(n);
-    if (has_next) {
-      named_barrier_sync(bar_id, 128);  // every thread is done reading this tile's L2 / D
-      sLD[w * 128 + r] = next_ld;
-      named_barrier_sync(bar_id, 128);
-      phase_a(n + 1);
-    }
-    drain(n);
-  }
-  if (!C::DQ_T && r == 0) tma_store_wait_all();  // reduce-adds complete before the CTA can exit
-}
-
-// Warpgroup w after the loop: w = 0 stores dK, w = 1 stores dV
-// (fp32 TMEM -> bf16 -> smem over K_j / V_j -> TMA store).
-template <int HD, bool CAUSAL>
-__device__ void bwd_epilogue(const BwdLaunch& p, BwdShared& sh, uint8_t* sK, uint8_t* sV, uint32_t tmem, int w,
-                             const BwdWork<CAUSAL>& wk) {
-  using C = BwdCfg<HD>;
-  const int r = threadIdx.x & 127;
-  const uint32_t lane_base = static_cast<uint32_t>((threadIdx.x >> 5) & 3) << 21;
-  bool ok = !*reinterpret_cast<volatile int*>(&sh.abort_flag);
-  if (ok) {
-    ok = __all_sync(0xffffffffu, mbar_wait(&sh.acc_done, 0, &sh.abort_flag, p.wait_limit_ns));
-    if (!ok) record_timeout(p.status, &sh.abort_flag, WHERE_BWD_SOFTMAX);
-  }
-  tc_fence_after_sync();
-  uint8_t* stage = w == 0 ? sK : sV;
-  if (ok) {
+  // ---- item epilogue: w = 0 writes dK_j, w = 1 writes dV_j (fp32 TMEM ->
+  // bf16 -> global; thread r writes key row r, rows past N are skipped).
+  auto epilogue = [&](const BwdWork<CAUSAL>& wk, int items) {
+    wait_all(&sh.acc_done, items & 1, WHERE_BWD_SOFTMAX);
+    if (!alive) return;
+    const int key = wk.j * 128 + r;
     const uint32_t t = tmem + lane_base + (w == 0 ? C::DK_COL : C::DV_COL);
-    const uint32_t st = smem_u32(stage);
+    __nv_bfloat16* dst = (w == 0 ? p.dk : p.dv) + (static_cast<size_t>(wk.bh) * p.N + key) * HD;
 #pragma unroll 1
     for (int c = 0; c < HD; c += 32) {
       uint32_t v[32];
       tmem_ld32(t + c, v);
       tmem_ld_wait();
+      if (c + 32 == HD) {  // both accumulators read: the next item may overwrite them
+        tc_fence_before_sync();
+        mbar_arrive(&sh.acc_free);
+      }
+      if (key < p.N) {
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int col = c + u * 8;
-        st_shared_v4(st + (col >> 6) * C::CHUNK_BYTES + sw128_offset(r, (col & 63) >> 3),
-                     pack_bf16x2(__uint_as_float(v[u * 8 + 0]), __uint_as_float(v[u * 8 + 1])),
-                     pack_bf16x2(__uint_as_float(v[u * 8 + 2]), __uint_as_float(v[u * 8 + 3])),
-                     pack_bf16x2(__uint_as_float(v[u * 8 + 4]), __uint_as_float(v[u * 8 + 5])),
-                     pack_bf16x2(__uint_as_float(v[u * 8 + 6]), __uint_as_float(v[u * 8 + 7])));
+        for (int u = 0; u < 4; ++u)
+          *reinterpret_cast<uint4*>(dst + c + 8 * u) =
+              make_uint4(pack_bf16x2(__uint_as_float(v[8 * u + 0]), __uint_as_float(v[8 * u + 1])),
+                         pack_bf16x2(__uint_as_float(v[8 * u + 2]), __uint_as_float(v[8 * u + 3])),
+                         pack_bf16x2(__uint_as_float(v[8 * u + 4]), __uint_as_float(v[8 * u + 5])),
+                         pack_bf16x2(__uint_as_float(v[8 * u + 6]), __uint_as_float(v[8 * u + 7])));
       }
     }
-    fence_proxy_async_smem();
+  };
+
+  // The next work item, agreed on by the whole warpgroup: a warp whose wait
+  // timed out makes every warp of the group leave the loop at the same point.
+  auto next_item = [&](int u) -> int {
+    const int it = alive ? take_item(sh, u, lim) : -1;
+    if (!named_barrier_and(bar_id, 128, it >= 0)) {
+      if (alive) record_timeout(p.status, &sh.abort_flag, WHERE_BWD_SOFTMAX);
+      alive = false;
+      return total;
+    }
+    return it;
+  };
+
+  int g = 0, items = 0;
+  int item = next_item(0);
+  float ld = 0.f;
+  if (item < total) {
+    const BwdWork<CAUSAL> wk0(item, p.BH, p.N);
+    ld = fetch_ld(wk0.bh, wk0.i0);
   }
-  named_barrier_sync(1 + w, 128);
-  if (ok && r == 0 && !*reinterpret_cast<volatile int*>(&sh.abort_flag)) {
-    const CUtensorMap* map = w == 0 ? &p.tmdK : &p.tmdV;
-#pragma unroll
-    for (int c = 0; c < C::CHUNKS; ++c) tma_store_3d(map, stage + c * C::CHUNK_BYTES, c * 64, wk.j * 128, wk.bh);
-    tma_store_commit();
-    tma_store_wait_all();
+  while (item < total) {
+    const BwdWork<CAUSAL> wk(item, p.BH, p.N);
+    const int n_iter = wk.n_iter();
+    if (items > 0) named_barrier_sync(bar_id, 128);  // the previous item's L2 / D reads are done
+    sLD[w * 128 + r] = ld;
+    named_barrier_sync(bar_id, 128);
+    phase_a(wk, wk.i0, g);
+    for (int n = 0; n < n_iter; ++n) {
+      const bool has_next = n + 1 < n_iter;
+      const float next_ld = has_next ? fetch_ld(wk.bh, wk.i0 + n + 1) : 0.f;  // lands during phase B
+      phase_b(g + n);
+      if (has_next) {
+        named_barrier_sync(bar_id, 128);  // every thread is done reading this tile's L2 / D
+        sLD[w * 128 + r] = next_ld;
+        named_barrier_sync(bar_id, 128);
+        phase_a(wk, wk.i0 + n + 1, g + n + 1);
+      }
+      drain(wk.bh, wk.i0 + n, g + n);
+    }
+    const int item_next = next_item(items + 1);
+    if (item_next < total) {
+      const BwdWork<CAUSAL> wk1(item_next, p.BH, p.N);
+      ld = fetch_ld(wk1.bh, wk1.i0);  // lands during the epilogue
+    }
+    epilogue(wk, items);
+    g += n_iter;
+    ++items;
+    item = item_next;
   }
+  if (!C::DQ_T && r == 0) tma_store_wait_all();  // reduce-adds complete before the CTA can exit
 }
 
 template <int HD, bool CAUSAL>
@@ -570,7 +666,6 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
   uint8_t* sDQ = sDS + C::DS_BYTES + C::LD_BYTES;  // 1024-aligned: DS and LD sizes are multiples of 1024
   const int warp = threadIdx.x >> 5;
   const int wg = warp >> 2;
-  const BwdWork<CAUSAL> wk(blockIdx.x, p.BH, p.N);
 
   if (threadIdx.x == 0) {
     mbar_init(&sh.kv_full, 1);
@@ -586,6 +681,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
     mbar_init(&sh.dq_full, 1);
     mbar_init(&sh.dq_free, 256);
     mbar_init(&sh.acc_done, 1);
+    mbar_init(&sh.acc_free, 256);
+    for (int s = 0; s < kItemSlots; ++s) {
+      mbar_init(&sh.item_full[s], 1);
+      mbar_init(&sh.item_empty[s], kItemConsumers);
+    }
     sh.abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -599,12 +699,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
   const uint32_t tmem = sh.tmem_base;
 
   if (warp == kLoadWarp) {
-    if (lane_id() == 0) bwd_load_role<HD, CAUSAL>(p, sh, sK, sV, sQ, sdO, wk);
+    if (lane_id() == 0) bwd_load_role<HD, CAUSAL>(p, sh, sK, sV, sQ, sdO);
   } else if (warp == kMmaWarp) {
-    if (lane_id() == 0) bwd_mma_role<HD, CAUSAL>(p, sh, sK, sV, sQ, sdO, sDS, tmem, wk);
+    if (lane_id() == 0) bwd_mma_role<HD, CAUSAL>(p, sh, sK, sV, sQ, sdO, sDS, tmem);
   } else {
-    bwd_softmax_role<HD, CAUSAL>(p, sh, sDS, sLD, sDQ, tmem, wg, wk);
-    bwd_epilogue<HD, CAUSAL>(p, sh, sK, sV, tmem, wg, wk);
+    bwd_softmax_role<HD, CAUSAL>(p, sh, sDS, sLD, sDQ, tmem, wg);
   }
 
   tc_fence_before_sync();
@@ -618,8 +717,8 @@ cudaError_t launch_pre_t(const BwdLaunch& a, cudaStream_t stream) {
   const long long rows = static_cast<long long>(a.BH) * a.Npad;
   constexpr int RPB = 8 * (32 / (HD / 8));  // rows per 256-thread block
   const long long blocks = (rows + RPB - 1) / RPB;
-  bwd_pre_kernel<HD><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a.o, a.dO, a.lse, a.D, a.lse2, a.dq_acc, a.N,
-                                                                        a.Npad, rows);
+  bwd_pre_kernel<HD><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a.o, a.dO, a.lse, a.D, a.lse2, a.dq_acc, a.sched,
+                                                                        a.N, a.Npad, rows);
   return cudaGetLastError();
 }
 
@@ -630,7 +729,10 @@ cudaError_t launch_main_t(const BwdLaunch& a, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const int T = (a.N + 127) / 128;
-  kern<<<static_cast<unsigned>(static_cast<long long>(a.BH) * T), kThreads, C::SMEM_BYTES, stream>>>(a);
+  const long long items = static_cast<long long>(a.BH) * T;
+  // Persistent: one CTA per SM (the smem footprint allows no more).
+  const long long grid = items < a.num_sms ? items : a.num_sms;
+  kern<<<static_cast<unsigned>(grid), kThreads, C::SMEM_BYTES, stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -43,9 +43,12 @@ struct BwdLaunch {
   const __nv_bfloat16* dO;
   const float* lse;
   __nv_bfloat16* dq;
+  __nv_bfloat16* dk;  // [BH][N][d]
+  __nv_bfloat16* dv;  // [BH][N][d]
   float* D;       // [BH][Npad]
   float* lse2;    // [BH][Npad], base-2 logsumexp (+inf on padding rows)
   float* dq_acc;  // [BH][Npad][d]
+  uint32_t* sched;  // [2]: next work item to hand out, CTAs done claiming
   uint32_t* status;
   int N, Npad, BH, d, causal;
   float scale;       // softmax scale (dK, dQ carry it)

@@ -72,7 +72,8 @@ fa_status_t fa_fwd(const void* q, const void* k, const void* v, void* o, float* 
 /*
  * Bytes of device workspace fa_bwd needs: D and the base-2 logsumexp
  * (fp32 per query row) and the fp32 dQ accumulator, with every head padded
- * to a multiple of 128 rows. Returns 0 for invalid or empty sizes.
+ * to a multiple of 128 rows, plus 256 bytes for the main kernel's work-item
+ * counter. Returns 0 for invalid or empty sizes.
  */
 size_t fa_bwd_workspace_size(int B, int H, int N, int d);
 
@@ -101,7 +102,8 @@ fa_status_t fa_bwd(const void* q, const void* k, const void* v, const void* o, c
  *
  * fa_bwd_preprocess: D_i = sum_k dO_ik O_ik (the row-wise correction that
  *   reading note 5.3 precomputes before the block loops), the base-2 logsumexp
- *   L_i * log2(e), and a zeroed fp32 dQ accumulator, all in the workspace.
+ *   L_i * log2(e), a zeroed fp32 dQ accumulator and a zeroed work-item
+ *   counter, all in the workspace.
  *   Reads o, lse, dO. HBM-bound.
  * fa_bwd_main: the block loops of reading note 5.3 (key blocks outer): writes
  *   dk and dv, and adds every dS K_j into the workspace's dQ accumulator.

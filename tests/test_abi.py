@@ -84,13 +84,13 @@ def test_backward_workspace_checks(lib):
 
 
 def test_workspace_size_formula(lib):
-    # D and base-2 L (fp32 per padded row) + fp32 dQ accumulator, heads padded to 128 rows
+    # D and base-2 L (fp32 per padded row) + fp32 dQ accumulator, heads padded
+    # to 128 rows, + 256 bytes of work-item counter
     for B, H, N, d in ((2, 4, 1024, 64), (1, 16, 1000, 128), (1, 2, 1, 256)):
         rows = B * H * ((N + 127) // 128 * 128)
         expect = 0
-        for nbytes in (rows * 4, rows * 4, rows * d * 4):
+        for nbytes in (rows * 4, rows * 4, rows * d * 4, 256):
             expect = (expect + 255) // 256 * 256 + nbytes
-        expect = (expect + 255) // 256 * 256
         assert lib.fa_bwd_workspace_size(B, H, N, d) == expect
 
 
