@@ -22,6 +22,11 @@ What is computed, per (batch, head), for Q, K, V in R^{N x d}:
     dV = P^T dO, dP = dO V^T,
     dS_i = P_i o (dP_i - <P_i, dP_i>)   (softmax Jacobian applied to dP_i)
     dQ = scale * dS K, dK = scale * dS^T Q   (the scale comes from S = scale*QK^T)
+  Grouped / multi-query heads:          [note] §5.6, [summary] "Multi-query and
+                                        grouped-query attention"
+    K and V may have H_kv heads with H_q = g * H_kv; query head h reads K/V
+    head floor(h / g), and dK, dV of a K/V head are the sums over its g query
+    heads. g = 1 is ordinary multi-head attention.
 
 attention_forward / attention_backward are the plain definitions: S and P are
 materialised (in chunks of query rows, which changes nothing but memory use).
@@ -39,7 +44,10 @@ logistic closed form; non-causal results are invariant under a joint
 permutation of K/V rows; shifting every key by u shifts L_i by scale q_i.u and
 leaves O unchanged; sum_j dK_j = 0 and sum_j dV_j = sum_i dO_i; the tiled
 variants agree to 1e-12; torch's float64 CPU attention plus autograd agrees to
-1e-12; central finite differences match the gradients. Every function here is
+1e-12; central finite differences match the gradients. Grouped K/V heads:
+torch's float64 attention with enable_gqa plus autograd agrees; K/V repeated
+along the head axis give the same O, L, dQ and, summed over each group, dK and
+dV; the tiled variants and finite differences agree. Every function here is
 pinned by at least one of these.
 """
 
@@ -51,15 +59,24 @@ _ROW_CHUNK = 256
 
 
 def _check(q, k, v=None):
+    """Promote to float64 and return (q, k, v, g): q is [B, H_q, N, d], k and v
+    are [B, H_kv, N, d] with H_q = g * H_kv ([note] §5.6)."""
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
-    if q.ndim != 4 or k.shape != q.shape:
-        raise ValueError("q, k must be [B, H, N, d] with equal shapes")
+    if q.ndim != 4 or k.ndim != 4 or k.shape[0] != q.shape[0] or k.shape[2:] != q.shape[2:]:
+        raise ValueError("q must be [B, H_q, N, d] and k [B, H_kv, N, d]")
+    if k.shape[1] < 1 or q.shape[1] % k.shape[1] != 0:
+        raise ValueError("H_q must be a multiple of H_kv")
     if v is not None:
         v = np.asarray(v, dtype=np.float64)
-        if v.shape != q.shape:
-            raise ValueError("v must match q")
-    return q, k, v
+        if v.shape != k.shape:
+            raise ValueError("v must match k")
+    return q, k, v, q.shape[1] // k.shape[1]
+
+
+def _kv_head(h, g):
+    """K/V head read by query head h when g query heads share one ([note] §5.6)."""
+    return h // g
 
 
 def _scores(q_rows, k, row_ids, causal, scale):
@@ -83,28 +100,29 @@ def softmax_rows(s):
 
 def attention_probabilities(q, k, causal, scale):
     """The full P = softmax(S) as a [B, H, N, N] array (small inputs only)."""
-    q, k, _ = _check(q, k)
+    q, k, _, g = _check(q, k)
     B, H, N, _d = q.shape
     out = np.zeros((B, H, N, N))
     rows = np.arange(N)
     for b in range(B):
         for h in range(H):
-            out[b, h], _ = softmax_rows(_scores(q[b, h], k[b, h], rows, causal, scale))
+            out[b, h], _ = softmax_rows(_scores(q[b, h], k[b, _kv_head(h, g)], rows, causal, scale))
     return out
 
 
 def attention_forward(q, k, v, causal, scale):
     """O = softmax(S) V and L = logsumexp(S) per row; returns (O [B,H,N,d], L [B,H,N])."""
-    q, k, v = _check(q, k, v)
+    q, k, v, g = _check(q, k, v)
     B, H, N, d = q.shape
     o = np.zeros((B, H, N, d))
     lse = np.zeros((B, H, N))
     for b in range(B):
         for h in range(H):
+            hk = _kv_head(h, g)
             for r0 in range(0, N, _ROW_CHUNK):
                 rows = np.arange(r0, min(N, r0 + _ROW_CHUNK))
-                p, l_rows = softmax_rows(_scores(q[b, h, rows], k[b, h], rows, causal, scale))
-                o[b, h, rows] = p @ v[b, h]
+                p, l_rows = softmax_rows(_scores(q[b, h, rows], k[b, hk], rows, causal, scale))
+                o[b, h, rows] = p @ v[b, hk]
                 lse[b, h, rows] = l_rows
     return o, lse
 
@@ -130,25 +148,29 @@ def attention_backward(q, k, v, do, causal, scale, heads=None):
 
     P is rebuilt from S (not from a stored L), and the softmax backward uses
     <P_i, dP_i> directly rather than the rowsum(dO o O) shortcut. `heads`, if
-    given, is a list of (b, h) pairs to compute; other heads are left zero.
+    given, is a list of (b, h) query-head pairs to compute; other heads are
+    left zero (and contribute nothing to dK, dV). With grouped K/V heads, dK
+    and dV have K's shape and sum the contributions of each group's query
+    heads ([note] §5.6).
     """
-    q, k, v = _check(q, k, v)
+    q, k, v, g = _check(q, k, v)
     do = np.asarray(do, dtype=np.float64)
     B, H, N, d = q.shape
     dq = np.zeros_like(q)
-    dk = np.zeros_like(q)
-    dv = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(k)
     pairs = heads if heads is not None else [(b, h) for b in range(B) for h in range(H)]
     for b, h in pairs:
+        hk = _kv_head(h, g)
         for r0 in range(0, N, _ROW_CHUNK):
             rows = np.arange(r0, min(N, r0 + _ROW_CHUNK))
-            p, _ = softmax_rows(_scores(q[b, h, rows], k[b, h], rows, causal, scale))
+            p, _ = softmax_rows(_scores(q[b, h, rows], k[b, hk], rows, causal, scale))
             do_rows = do[b, h, rows]
-            dv[b, h] += p.T @ do_rows
-            dp = do_rows @ v[b, h].T
+            dv[b, hk] += p.T @ do_rows
+            dp = do_rows @ v[b, hk].T
             ds = p * (dp - np.sum(p * dp, axis=1, keepdims=True))
-            dq[b, h, rows] = scale * (ds @ k[b, h])
-            dk[b, h] += scale * (ds.T @ q[b, h, rows])
+            dq[b, h, rows] = scale * (ds @ k[b, hk])
+            dk[b, hk] += scale * (ds.T @ q[b, h, rows])
     return dq, dk, dv
 
 
@@ -184,12 +206,13 @@ def tiled_forward(q, k, v, causal, scale, block_rows, block_cols):
     L_i = m + log l. Blocks need not divide N. Causal key blocks entirely
     to the right of the query block are skipped.
     """
-    q, k, v = _check(q, k, v)
+    q, k, v, g = _check(q, k, v)
     B, H, N, d = q.shape
     o = np.zeros((B, H, N, d))
     lse = np.zeros((B, H, N))
     for b in range(B):
         for h in range(H):
+            kh, vh = k[b, _kv_head(h, g)], v[b, _kv_head(h, g)]
             for i0 in range(0, N, block_rows):
                 i1 = min(N, i0 + block_rows)
                 qi = q[b, h, i0:i1]
@@ -200,7 +223,7 @@ def tiled_forward(q, k, v, causal, scale, block_rows, block_cols):
                     if causal and j0 > i1 - 1:
                         break
                     j1 = min(N, j0 + block_cols)
-                    s = scale * (qi @ k[b, h, j0:j1].T)
+                    s = scale * (qi @ kh[j0:j1].T)
                     if causal:
                         rr = np.arange(i0, i1)[:, None]
                         cc = np.arange(j0, j1)[None, :]
@@ -209,7 +232,7 @@ def tiled_forward(q, k, v, causal, scale, block_rows, block_cols):
                     p_tilde = np.exp(s - m_new[:, None])
                     corr = np.exp(m - m_new)
                     l_run = corr * l_run + np.sum(p_tilde, axis=1)
-                    acc = corr[:, None] * acc + p_tilde @ v[b, h, j0:j1]
+                    acc = corr[:, None] * acc + p_tilde @ vh[j0:j1]
                     m = m_new
                 o[b, h, i0:i1] = acc / l_run[:, None]
                 lse[b, h, i0:i1] = m + np.log(l_run)
@@ -222,22 +245,24 @@ def tiled_backward(q, k, v, o, lse, do, causal, scale, block_rows, block_cols):
     D = rowsum(dO o O); for each key block j: dK_j = dV_j = 0; for each query
     block i: S_ij = scale Q_i K_j^T (masked), P_ij = exp(S_ij - L_i),
     dV_j += P_ij^T dO_i, dP_ij = dO_i V_j^T, dS_ij = P_ij o (dP_ij - D_i),
-    dQ_i += scale dS_ij K_j, dK_j += scale dS_ij^T Q_i.
+    dQ_i += scale dS_ij K_j, dK_j += scale dS_ij^T Q_i. With grouped K/V
+    heads each query head adds its dK_j, dV_j into its K/V head's ([note] §5.6).
     """
-    q, k, v = _check(q, k, v)
+    q, k, v, g = _check(q, k, v)
     o = np.asarray(o, dtype=np.float64)
     do = np.asarray(do, dtype=np.float64)
     lse = np.asarray(lse, dtype=np.float64)
     B, H, N, d = q.shape
     dq = np.zeros_like(q)
-    dk = np.zeros_like(q)
-    dv = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(k)
     D = np.sum(do * o, axis=-1)
     for b in range(B):
         for h in range(H):
+            hk = _kv_head(h, g)
             for j0 in range(0, N, block_cols):
                 j1 = min(N, j0 + block_cols)
-                kj, vj = k[b, h, j0:j1], v[b, h, j0:j1]
+                kj, vj = k[b, hk, j0:j1], v[b, hk, j0:j1]
                 dkj = np.zeros((j1 - j0, d))
                 dvj = np.zeros((j1 - j0, d))
                 for i0 in range(0, N, block_rows):
@@ -255,6 +280,6 @@ def tiled_backward(q, k, v, o, lse, do, causal, scale, block_rows, block_cols):
                     ds = p * (dp - D[b, h, i0:i1, None])
                     dq[b, h, i0:i1] += scale * (ds @ kj)
                     dkj += scale * (ds.T @ q[b, h, i0:i1])
-                dk[b, h, j0:j1] = dkj
-                dv[b, h, j0:j1] = dvj
+                dk[b, hk, j0:j1] += dkj
+                dv[b, hk, j0:j1] += dvj
     return dq, dk, dv

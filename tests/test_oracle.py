@@ -288,3 +288,96 @@ def test_planted_wrong_softmax_gradient_sign_is_caught(monkeypatch):
     monkeypatch.setattr(oa, "softmax_rows", lambda s: (real(s)[0].T.copy(), real(s)[1]))
     _, _, dv_bad = oracle.attention_backward(q, k, v, do, False, 0.5)
     assert not np.allclose(dv_bad.sum(axis=2), do.sum(axis=2), atol=1e-9)
+
+
+# ---- grouped / multi-query K/V heads (reading note §5.6) ---------------------
+
+def gqa_inputs(B, Hq, Hkv, N, d, seed):
+    return (rand((B, Hq, N, d), seed), rand((B, Hkv, N, d), seed + 1), rand((B, Hkv, N, d), seed + 2),
+            rand((B, Hq, N, d), seed + 3))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Hq,Hkv", [(4, 2), (6, 1), (3, 3)])
+def test_grouped_heads_torch_sdpa_agrees(causal, Hq, Hkv):
+    # torch's float64 CPU attention with enable_gqa (query head h reads K/V
+    # head h // g) plus autograd, which sums dK, dV over each group
+    torch = pytest.importorskip("torch")
+    q, k, v, do = gqa_inputs(2, Hq, Hkv, 27, 8, 50)
+    scale = 0.3
+    tq, tk, tv = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (q, k, v))
+    to = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=causal, scale=scale,
+                                                          enable_gqa=True)
+    to.backward(torch.tensor(do))
+    o, _ = oracle.attention_forward(q, k, v, causal, scale)
+    np.testing.assert_allclose(o, to.detach().numpy(), rtol=0, atol=1e-12)
+    dq, dk, dv = oracle.attention_backward(q, k, v, do, causal, scale)
+    assert dk.shape == k.shape and dv.shape == v.shape
+    np.testing.assert_allclose(dq, tq.grad.numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dk, tk.grad.numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dv, tv.grad.numpy(), rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_grouped_heads_equal_replicated_heads(causal):
+    # K/V physically repeated along the head axis turn the grouped problem into
+    # ordinary multi-head attention; its dK, dV summed over each group of
+    # copies are the grouped gradients
+    B, Hq, Hkv, N, d = 2, 6, 2, 21, 5
+    g = Hq // Hkv
+    q, k, v, do = gqa_inputs(B, Hq, Hkv, N, d, 60)
+    kr, vr = np.repeat(k, g, axis=1), np.repeat(v, g, axis=1)
+    o, lse = oracle.attention_forward(q, k, v, causal, 0.4)
+    o_r, lse_r = oracle.attention_forward(q, kr, vr, causal, 0.4)
+    np.testing.assert_allclose(o, o_r, rtol=0, atol=1e-14)
+    np.testing.assert_allclose(lse, lse_r, rtol=0, atol=1e-14)
+    dq, dk, dv = oracle.attention_backward(q, k, v, do, causal, 0.4)
+    dq_r, dk_r, dv_r = oracle.attention_backward(q, kr, vr, do, causal, 0.4)
+    np.testing.assert_allclose(dq, dq_r, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(dk, dk_r.reshape(B, Hkv, g, N, d).sum(2), rtol=0, atol=1e-13)
+    np.testing.assert_allclose(dv, dv_r.reshape(B, Hkv, g, N, d).sum(2), rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_grouped_heads_tiled_variants_agree(causal):
+    q, k, v, do = gqa_inputs(1, 4, 2, 45, 6, 70)
+    o, lse = oracle.attention_forward(q, k, v, causal, 0.35)
+    ot, lset = oracle.tiled_forward(q, k, v, causal, 0.35, 16, 12)
+    np.testing.assert_allclose(ot, o, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lset, lse, rtol=0, atol=1e-12)
+    grads = oracle.attention_backward(q, k, v, do, causal, 0.35)
+    tgrads = oracle.tiled_backward(q, k, v, o, lse, do, causal, 0.35, 16, 12)
+    for a, b in zip(tgrads, grads):
+        np.testing.assert_allclose(a, b, rtol=0, atol=1e-12)
+
+
+def test_grouped_heads_finite_differences():
+    q, k, v, do = gqa_inputs(1, 2, 1, 5, 2, 80)
+    scale = 0.8
+    dq, dk, dv = oracle.attention_backward(q, k, v, do, True, scale)
+
+    def loss(k_, v_):
+        o, _ = oracle.attention_forward(q, k_, v_, True, scale)
+        return float(np.sum(o * do))
+
+    h = 1e-6
+    for which, (x, g) in enumerate(((k, dk), (v, dv))):
+        num = np.zeros_like(x)
+        for pos in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[pos] += h
+            xm[pos] -= h
+            num[pos] = ((loss(xp, v) - loss(xm, v)) if which == 0 else (loss(k, xp) - loss(k, xm))) / (2 * h)
+        np.testing.assert_allclose(g, num, rtol=1e-6, atol=1e-8)
+
+
+def test_planted_wrong_group_mapping_is_caught(monkeypatch):
+    # h mod H_kv instead of floor(h / g) gives a different, valid-looking
+    # result that the replicated-heads identity rejects
+    B, Hq, Hkv, N, d = 1, 4, 2, 9, 3
+    q, k, v, _ = gqa_inputs(B, Hq, Hkv, N, d, 90)
+    kr, vr = np.repeat(k, 2, axis=1), np.repeat(v, 2, axis=1)
+    o_r, _ = oracle.attention_forward(q, kr, vr, False, 0.5)
+    monkeypatch.setattr(oa, "_kv_head", lambda h, g: h % Hkv)
+    o_bad, _ = oracle.attention_forward(q, k, v, False, 0.5)
+    assert not np.allclose(o_bad, o_r, atol=1e-6)
