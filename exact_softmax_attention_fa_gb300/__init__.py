@@ -15,7 +15,7 @@ import math
 
 from ._lib import load, check, FAError, header_functions, STATUS_NAMES  # noqa: F401
 
-__all__ = ["fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_postprocess", "fa_bwd_noalloc", "fa_get_device_status", "fa_set_wait_limit_ns",
+__all__ = ["fa_fwd", "fa_bwd", "fa_fwd_gqa", "fa_bwd_gqa", "fa_bwd_workspace_size", "fa_bwd_gqa_workspace_size", "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_postprocess", "fa_bwd_noalloc", "fa_get_device_status", "fa_set_wait_limit_ns",
            "fa_debug_timeout_probe", "forward", "backward", "FAError", "flops"]
 
 _SUPPORTED_D = (64, 128, 256)
@@ -68,8 +68,53 @@ def fa_fwd(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> None:
                                B, H, N, d, int(bool(causal)), float(scale), _stream_handle(stream)))
 
 
+def _gqa_dims(q, k):
+    """(B, Hq, Hkv, N, d) for q [B, Hq, N, d] and k [B, Hkv, N, d]."""
+    B, Hq, N, d = _dims(q)
+    if k.dim() != 4 or k.shape[0] != B or tuple(k.shape[2:]) != (N, d):
+        raise ValueError("k must be [B, Hkv, N, d] with q's B, N, d")
+    Hkv = int(k.shape[1])
+    if Hkv < 1 or Hq % Hkv != 0:
+        raise ValueError(f"the query heads ({Hq}) must be a multiple of the K/V heads ({Hkv})")
+    return B, Hq, Hkv, N, d
+
+
+def fa_fwd_gqa(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> None:
+    """fa_fwd_gqa of the C ABI: q, o [B, Hq, N, d]; k, v [B, Hkv, N, d]; lse [B, Hq, N]."""
+    B, Hq, Hkv, N, d = _gqa_dims(q, k)
+    for name, t, shape in (("q", q, (B, Hq, N, d)), ("k", k, (B, Hkv, N, d)), ("v", v, (B, Hkv, N, d)),
+                           ("o", o, (B, Hq, N, d))):
+        _check_bf16(name, t, shape)
+    _check_lse(lse, (B, Hq, N, d))
+    lib = load()
+    check("fa_fwd_gqa", lib.fa_fwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                       B, Hq, Hkv, N, d, int(bool(causal)), float(scale), _stream_handle(stream)))
+
+
+def fa_bwd_gqa(q, k, v, o, lse, do, dq, dk, dv, causal: bool, scale: float, workspace, stream=None) -> None:
+    """fa_bwd_gqa of the C ABI: q, o, do, dq [B, Hq, N, d]; k, v, dk, dv [B, Hkv, N, d].
+
+    `workspace` is a CUDA uint8 tensor of at least fa_bwd_workspace_size(B, Hq, N, d) bytes.
+    """
+    B, Hq, Hkv, N, d = _gqa_dims(q, k)
+    qs, ks = (B, Hq, N, d), (B, Hkv, N, d)
+    for name, t, shape in (("q", q, qs), ("k", k, ks), ("v", v, ks), ("o", o, qs), ("do", do, qs), ("dq", dq, qs),
+                           ("dk", dk, ks), ("dv", dv, ks)):
+        _check_bf16(name, t, shape)
+    _check_lse(lse, qs)
+    lib = load()
+    check("fa_bwd_gqa", lib.fa_bwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                       do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                                       B, Hq, Hkv, N, d, int(bool(causal)), float(scale), *_ws(workspace),
+                                       _stream_handle(stream)))
+
+
 def fa_bwd_workspace_size(B: int, H: int, N: int, d: int) -> int:
     return int(load().fa_bwd_workspace_size(B, H, N, d))
+
+
+def fa_bwd_gqa_workspace_size(B: int, Hq: int, Hkv: int, N: int, d: int) -> int:
+    return int(load().fa_bwd_gqa_workspace_size(B, Hq, Hkv, N, d))
 
 
 def fa_bwd(q, k, v, o, lse, do, dq, dk, dv, causal: bool, scale: float, workspace, stream=None) -> None:
@@ -163,27 +208,37 @@ def fa_debug_timeout_probe(limit_ns: int, stream=None) -> None:
 
 
 def forward(q, k, v, causal: bool = False, scale: float | None = None, stream=None):
-    """Allocate O (bf16) and L (fp32) with torch and run fa_fwd."""
+    """Allocate O (bf16) and L (fp32) with torch and run fa_fwd (fa_fwd_gqa when
+    k, v have fewer heads than q)."""
     import torch
     B, H, N, d = _dims(q)
     if scale is None:
         scale = default_scale(d)
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    fa_fwd(q, k, v, o, lse, causal, scale, stream)
+    if k.dim() == 4 and k.shape[1] != H:
+        fa_fwd_gqa(q, k, v, o, lse, causal, scale, stream)
+    else:
+        fa_fwd(q, k, v, o, lse, causal, scale, stream)
     return o, lse
 
 
 def backward(q, k, v, o, lse, do, causal: bool = False, scale: float | None = None, workspace=None, stream=None):
-    """Allocate dQ, dK, dV (and the workspace if not given) with torch and run fa_bwd."""
+    """Allocate dQ, dK, dV (and the workspace if not given) with torch and run fa_bwd
+    (fa_bwd_gqa when k, v have fewer heads than q)."""
     import torch
     B, H, N, d = _dims(q)
     if scale is None:
         scale = default_scale(d)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    grouped = k.dim() == 4 and k.shape[1] != H
     if workspace is None:
-        workspace = torch.empty(max(1, fa_bwd_workspace_size(B, H, N, d)), dtype=torch.uint8, device=q.device)
-    fa_bwd(q, k, v, o, lse, do, dq, dk, dv, causal, scale, workspace, stream)
+        size = fa_bwd_gqa_workspace_size(B, H, int(k.shape[1]), N, d) if grouped else fa_bwd_workspace_size(B, H, N, d)
+        workspace = torch.empty(max(1, size), dtype=torch.uint8, device=q.device)
+    if grouped:
+        fa_bwd_gqa(q, k, v, o, lse, do, dq, dk, dv, causal, scale, workspace, stream)
+    else:
+        fa_bwd(q, k, v, o, lse, do, dq, dk, dv, causal, scale, workspace, stream)
     return dq, dk, dv
 
 

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -144,6 +145,13 @@ fa_status_t check_common(int B, int H, int N, int d, int causal, float scale, bo
   return FA_OK;
 }
 
+// Grouped K/V heads: Hkv >= 1 dividing Hq (nothing to check when Hq == 0).
+fa_status_t check_heads(int Hq, int Hkv) {
+  if (Hkv < 0) return FA_ERR_INVALID_ARG;
+  if (Hq > 0 && (Hkv == 0 || Hq % Hkv != 0)) return FA_ERR_INVALID_ARG;
+  return FA_OK;
+}
+
 int round_up_128(int n) { return (n + 127) / 128 * 128; }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -161,6 +169,40 @@ BwdWorkspaceLayout bwd_layout(long long BH, int N, int d) {
   w.sched_off = align_up(w.dq_off + rows * static_cast<size_t>(d) * 4, 256);
   w.total = w.sched_off + 256;
   return w;
+}
+
+// fp32 partial dK + dV of one chunk of a group, for every K/V head.
+size_t kv_part_bytes(long long BHkv, int N, int d) { return static_cast<size_t>(BHkv) * N * d * 4 * 2; }
+
+// How many work items share one (K/V head, key tile) when g query heads read
+// the same K/V head. One item per group keeps dK, dV on chip; splitting the
+// group adds items (fewer idle SMs in the last round) and, under a causal
+// mask, shortens the longest item, at the price of fp32 partials written to
+// the workspace and summed by a post kernel. The estimate compares, per
+// candidate, the tiles the busiest SM processes (a tile = 5 MMAs of 128x128xd
+// at ~6 TFLOP/s per SM) plus the post kernel's read of the partials at
+// ~6 TB/s (their writes overlap the main kernel's compute); a split must win
+// by 2 %. d = 256 keeps one item per group.
+int choose_kv_chunks(long long BHkv, int g, int N, int d, int causal, int sms, size_t part_room) {
+  if (g <= 1 || d == 256 || sms <= 0) return 1;
+  const double T = static_cast<double>((N + 127) / 128);
+  const double t_tile = 10.0 * 128 * 128 * d / 6.0e12;
+  const double total = static_cast<double>(BHkv) * g * (causal ? T * (T + 1) / 2 : T * T);
+  int best = 1;
+  double best_t = 1e300;
+  for (int chunks = 1; chunks <= g; ++chunks) {
+    if (g % chunks != 0) continue;
+    if (chunks > 1 && static_cast<size_t>(chunks) * kv_part_bytes(BHkv, N, d) > part_room) break;
+    const double gs = g / chunks;
+    const double items = static_cast<double>(BHkv) * chunks * T;
+    const double tiles = causal ? std::max(gs * T, total / sms) : std::ceil(items / sms) * gs * T;
+    const double t = tiles * t_tile + (chunks > 1 ? chunks * kv_part_bytes(BHkv, N, d) / 6.0e12 : 0.0);
+    if (t < best_t * 0.98) {
+      best_t = t;
+      best = chunks;
+    }
+  }
+  return best;
 }
 
 fa_status_t from_cuda(cudaError_t e) {
@@ -198,10 +240,12 @@ void fa_set_wait_limit_ns(unsigned long long limit_ns) {
   g_wait_limit_ns.store(limit_ns == 0 ? kDefaultWaitLimitNs : limit_ns);
 }
 
-fa_status_t fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
-                   int causal, float scale, cudaStream_t stream) {
+fa_status_t fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                       int N, int d, int causal, float scale, cudaStream_t stream) {
   bool empty = false;
-  fa_status_t st = check_common(B, H, N, d, causal, scale, &empty);
+  fa_status_t st = check_common(B, Hq, N, d, causal, scale, &empty);
+  if (st != FA_OK) return st;
+  st = check_heads(Hq, Hkv);
   if (st != FA_OK) return st;
   if (empty) return FA_OK;
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
@@ -210,8 +254,8 @@ fa_status_t fa_fwd(const void* q, const void* k, const void* v, void* o, float* 
   DeviceState* ds = device_state(&st);
   if (!ds) return st;
   FwdLaunch a{};
-  const int BH = B * H;
-  if (!make_map(&a.tmQ, q, BH, N, d) || !make_map(&a.tmK, k, BH, N, d) || !make_map(&a.tmV, v, BH, N, d) ||
+  const int BH = B * Hq, BHkv = B * Hkv;
+  if (!make_map(&a.tmQ, q, BH, N, d) || !make_map(&a.tmK, k, BHkv, N, d) || !make_map(&a.tmV, v, BHkv, N, d) ||
       !make_map(&a.tmO, o, BH, N, d))
     return FA_ERR_CUDA;
   a.lse = lse;
@@ -220,10 +264,25 @@ fa_status_t fa_fwd(const void* q, const void* k, const void* v, void* o, float* 
   a.BH = BH;
   a.d = d;
   a.causal = causal;
+  a.group = Hq / Hkv;
   a.scale_log2 = static_cast<float>(static_cast<double>(scale) * kLog2e);
   a.wait_limit_ns = g_wait_limit_ns.load();
   a.num_sms = ds->num_sms;
   return from_cuda(launch_fwd(a, stream));
+}
+
+fa_status_t fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                   int causal, float scale, cudaStream_t stream) {
+  return fa_fwd_gqa(q, k, v, o, lse, B, H, H, N, d, causal, scale, stream);
+}
+
+size_t fa_bwd_gqa_workspace_size(int B, int Hq, int Hkv, int N, int d) {
+  bool empty = false;
+  if (check_common(B, Hq, N, d, 0, 1.0f, &empty) != FA_OK || check_heads(Hq, Hkv) != FA_OK || empty) return 0;
+  const size_t base = bwd_layout(static_cast<long long>(B) * Hq, N, d).total;
+  const int g = Hq / Hkv;
+  if (g <= 1 || d == 256) return base;
+  return base + static_cast<size_t>(g) * kv_part_bytes(static_cast<long long>(B) * Hkv, N, d);
 }
 
 size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
@@ -244,9 +303,11 @@ struct BwdTensors {
   void *dq, *dk, *dv;
 };
 
-fa_status_t prepare_bwd(const BwdTensors& t, int B, int H, int N, int d, int causal, float scale, void* workspace,
-                        size_t workspace_bytes, bool* empty, BwdLaunch* a) {
+fa_status_t prepare_bwd(const BwdTensors& t, int B, int H, int Hkv, int N, int d, int causal, float scale,
+                        void* workspace, size_t workspace_bytes, bool* empty, BwdLaunch* a) {
   fa_status_t st = check_common(B, H, N, d, causal, scale, empty);
+  if (st != FA_OK) return st;
+  st = check_heads(H, Hkv);
   if (st != FA_OK || *empty) return st;
   const void* bf16_ptrs[] = {t.q, t.k, t.v, t.o, t.dO, t.dq, t.dk, t.dv};
   for (const void* p : bf16_ptrs)
@@ -259,12 +320,15 @@ fa_status_t prepare_bwd(const BwdTensors& t, int B, int H, int N, int d, int cau
   DeviceState* ds = device_state(&st);
   if (!ds) return st;
   *a = BwdLaunch{};
-  auto map = [&](CUtensorMap* m, const void* ptr, unsigned rows) { return !ptr || make_map(m, ptr, BH, N, d, rows); };
+  const int BHkv = B * Hkv;
+  auto map = [&](CUtensorMap* m, const void* ptr, int heads, unsigned rows) {
+    return !ptr || make_map(m, ptr, heads, N, d, rows);
+  };
   // d = 256 streams Q and dO in 64-row query tiles (smem budget); all other
-  // tiles are 128 rows.
+  // tiles are 128 rows. Q, dO have BH heads, K, V, dK, dV have BHkv.
   const unsigned q_rows = d == 256 ? 64 : 128;
-  if (!map(&a->tmQ, t.q, q_rows) || !map(&a->tmK, t.k, 128) || !map(&a->tmV, t.v, 128) ||
-      !map(&a->tmdO, t.dO, q_rows) || !map(&a->tmdK, t.dk, 128) || !map(&a->tmdV, t.dv, 128))
+  if (!map(&a->tmQ, t.q, BH, q_rows) || !map(&a->tmK, t.k, BHkv, 128) || !map(&a->tmV, t.v, BHkv, 128) ||
+      !map(&a->tmdO, t.dO, BH, q_rows) || !map(&a->tmdK, t.dk, BHkv, 128) || !map(&a->tmdV, t.dv, BHkv, 128))
     return FA_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   a->o = static_cast<const __nv_bfloat16*>(t.o);
@@ -277,11 +341,17 @@ fa_status_t prepare_bwd(const BwdTensors& t, int B, int H, int N, int d, int cau
   a->lse2 = reinterpret_cast<float*>(ws + wl.lse2_off);
   a->dq_acc = reinterpret_cast<float*>(ws + wl.dq_off);
   a->sched = reinterpret_cast<uint32_t*>(ws + wl.sched_off);
+  // Room after the fixed layout holds the split groups' dK, dV partials.
+  const size_t part_room = workspace_bytes > wl.total ? workspace_bytes - wl.total : 0;
+  a->chunks = choose_kv_chunks(BHkv, H / (Hkv > 0 ? Hkv : 1), N, d, causal, ds->num_sms, part_room);
+  a->kv_part = reinterpret_cast<float*>(ws + wl.total);
   if (!make_map_f32_acc(&a->tmdQacc, a->dq_acc, BH, round_up_128(N), d)) return FA_ERR_CUDA;
   a->status = ds->status;
   a->N = N;
   a->Npad = round_up_128(N);
   a->BH = BH;
+  a->BHkv = BHkv;
+  a->group = H / Hkv;
   a->d = d;
   a->causal = causal;
   a->scale = scale;
@@ -295,22 +365,31 @@ fa_status_t prepare_bwd(const BwdTensors& t, int B, int H, int N, int d, int cau
 
 extern "C" {
 
-fa_status_t fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
-                   void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal, float scale,
-                   void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+fa_status_t fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                       const void* dO, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N, int d,
+                       int causal, float scale, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   bool empty = false;
-  fa_status_t st = check_common(B, H, N, d, causal, scale, &empty);
+  fa_status_t st = check_common(B, Hq, N, d, causal, scale, &empty);
+  if (st != FA_OK) return st;
+  st = check_heads(Hq, Hkv);
   if (st != FA_OK) return st;
   if (empty) return FA_OK;
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
   BwdLaunch a;
-  st = prepare_bwd(BwdTensors{q, k, v, o, dO, lse, dq, dk, dv}, B, H, N, d, causal, scale, workspace,
+  st = prepare_bwd(BwdTensors{q, k, v, o, dO, lse, dq, dk, dv}, B, Hq, Hkv, N, d, causal, scale, workspace,
                    workspace_bytes, &empty, &a);
   if (st != FA_OK || empty) return st;
   cudaError_t e = launch_bwd_pre(a, stream);
   if (e == cudaSuccess) e = launch_bwd_main(a, stream);
   if (e == cudaSuccess) e = launch_bwd_post(a, stream);
   return from_cuda(e);
+}
+
+fa_status_t fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                   void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal, float scale,
+                   void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return fa_bwd_gqa(q, k, v, o, lse, dO, dq, dk, dv, B, H, H, N, d, causal, scale, workspace, workspace_bytes,
+                    stream);
 }
 
 fa_status_t fa_bwd_preprocess(const void* o, const float* lse, const void* dO, int B, int H, int N, int d,
@@ -321,7 +400,7 @@ fa_status_t fa_bwd_preprocess(const void* o, const float* lse, const void* dO, i
   if (empty) return FA_OK;
   if (!o || !lse || !dO) return FA_ERR_INVALID_ARG;
   BwdLaunch a;
-  st = prepare_bwd(BwdTensors{nullptr, nullptr, nullptr, o, dO, lse, nullptr, nullptr, nullptr}, B, H, N, d, 0, 1.0f,
+  st = prepare_bwd(BwdTensors{nullptr, nullptr, nullptr, o, dO, lse, nullptr, nullptr, nullptr}, B, H, H, N, d, 0, 1.0f,
                    workspace, workspace_bytes, &empty, &a);
   if (st != FA_OK || empty) return st;
   return from_cuda(launch_bwd_pre(a, stream));
@@ -336,7 +415,7 @@ fa_status_t fa_bwd_main(const void* q, const void* k, const void* v, const void*
   if (empty) return FA_OK;
   if (!q || !k || !v || !dO || !dk || !dv) return FA_ERR_INVALID_ARG;
   BwdLaunch a;
-  st = prepare_bwd(BwdTensors{q, k, v, nullptr, dO, nullptr, nullptr, dk, dv}, B, H, N, d, causal, scale, workspace,
+  st = prepare_bwd(BwdTensors{q, k, v, nullptr, dO, nullptr, nullptr, dk, dv}, B, H, H, N, d, causal, scale, workspace,
                    workspace_bytes, &empty, &a);
   if (st != FA_OK || empty) return st;
   return from_cuda(launch_bwd_main(a, stream));
@@ -350,7 +429,7 @@ fa_status_t fa_bwd_postprocess(void* dq, int B, int H, int N, int d, void* works
   if (empty) return FA_OK;
   if (!dq) return FA_ERR_INVALID_ARG;
   BwdLaunch a;
-  st = prepare_bwd(BwdTensors{nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, dq, nullptr, nullptr}, B, H, N,
+  st = prepare_bwd(BwdTensors{nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, dq, nullptr, nullptr}, B, H, H, N,
                    d, 0, 1.0f, workspace, workspace_bytes, &empty, &a);
   if (st != FA_OK || empty) return st;
   return from_cuda(launch_bwd_post(a, stream));

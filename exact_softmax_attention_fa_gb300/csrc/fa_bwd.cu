@@ -91,24 +91,36 @@ struct BwdShared {
   int abort_flag;
 };
 
-// Work item: key tile j of head bh; query tiles i0..T-1 (causal: i0 = j).
-// Causal items are numbered most-work-first (key tile j meets T - j query
-// tiles); non-causal items of one head are adjacent (Q/dO reuse in L2).
+// Work item: key tile j of K/V head bh and chunk c of the g query heads that
+// share it (query head bh*g + t reads K/V head bh; a group is split into
+// `chunks` chunks of gs = g / chunks heads). Its query stream is, for each
+// query head of the chunk, query tiles i0..T-1 (causal: i0 = j); dK_j and dV_j
+// accumulate over all of them. Causal items are numbered most-work-first (key
+// tile j meets T - j query tiles per head); non-causal items of one chunk are
+// adjacent (Q/dO reuse in L2).
 template <bool CAUSAL>
 struct BwdWork {
-  int bh, j, i0, T;
-  __device__ BwdWork(int item, int BH, int N) {
+  int bh, c, j, i0, T, nq, gs, q0;
+  __device__ BwdWork(int item, int BHkv, int N, int g, int chunks) {
     T = (N + 127) / 128;
+    int unit;  // bh * chunks + c
     if (CAUSAL) {
-      bh = item % BH;
-      j = item / BH;
+      unit = item % (BHkv * chunks);
+      j = item / (BHkv * chunks);
     } else {
-      bh = item / T;
+      unit = item / T;
       j = item % T;
     }
+    bh = unit / chunks;
+    c = unit - bh * chunks;
+    gs = g / chunks;
+    q0 = bh * g + c * gs;
     i0 = CAUSAL ? j : 0;
+    nq = T - i0;
   }
-  __device__ int n_iter() const { return T - i0; }
+  __device__ int n_iter() const { return gs * nq; }
+  __device__ int qbh(int n) const { return q0 + n / nq; }  // query head of step n
+  __device__ int qi(int n) const { return i0 + n % nq; }   // query tile of step n
 };
 
 // Dynamic schedule: CTA b starts on item b; afterwards the load thread claims
@@ -125,6 +137,32 @@ __device__ __forceinline__ int take_item(BwdShared& sh, int u, uint64_t lim) {
   const int item = *reinterpret_cast<volatile int*>(&sh.item_ring[s]);
   mbar_arrive(&sh.item_empty[s]);
   return item;
+}
+
+// Grouped K/V heads split over several work items: dK, dV = bf16 of the sum
+// of the chunks' fp32 partials, added in chunk order (bitwise reproducible).
+// Thread v handles 8 consecutive elements of dK (v < n8) or dV.
+__global__ void __launch_bounds__(256) bwd_kv_sum_kernel(const float* __restrict__ part,
+                                                         __nv_bfloat16* __restrict__ dk,
+                                                         __nv_bfloat16* __restrict__ dv, int chunks, long long n8) {
+  const long long v = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (v >= 2 * n8) return;
+  const bool is_v = v >= n8;
+  const long long e = (is_v ? v - n8 : v) * 8;  // element offset in [BHkv][N][d]
+  const size_t len = static_cast<size_t>(n8) * 8;
+  const float* src = part + (is_v ? static_cast<size_t>(chunks) * len : 0) + e;
+  float4 a = ldg_f4(src), b = ldg_f4(src + 4);
+  for (int c = 1; c < chunks; ++c) {
+    const float4 a2 = ldg_f4(src + c * len), b2 = ldg_f4(src + c * len + 4);
+    a.x += a2.x; a.y += a2.y; a.z += a2.z; a.w += a2.w;
+    b.x += b2.x; b.y += b2.y; b.z += b2.z; b.w += b2.w;
+  }
+  uint4 out;
+  out.x = pack_bf16x2(a.x, a.y);
+  out.y = pack_bf16x2(a.z, a.w);
+  out.z = pack_bf16x2(b.x, b.y);
+  out.w = pack_bf16x2(b.z, b.w);
+  *reinterpret_cast<uint4*>((is_v ? dv : dk) + e) = out;
 }
 
 // ---------------------------------------------------------------------------
@@ -219,7 +257,7 @@ __device__ void bwd_load_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sK, ui
   tma_prefetch_desc(&p.tmdO);
   tma_prefetch_desc(&p.tmdQacc);
   const int T = (p.N + 127) / 128;
-  const int total = p.BH * T;
+  const int total = p.BHkv * p.chunks * T;
   const int G = gridDim.x;
   const uint64_t lim = p.wait_limit_ns;
   int g = 0, items = 0, issued = 0, kv_issued = 0;
@@ -251,9 +289,9 @@ __device__ void bwd_load_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sK, ui
       break;
     }
     if (item >= total) break;
-    const BwdWork<CAUSAL> wk(item, p.BH, p.N);
+    const BwdWork<CAUSAL> wk(item, p.BHkv, p.N, p.group, p.chunks);
     const int n_iter = wk.n_iter();
-    if (!load_qdo(g, wk.i0, wk.bh)) {
+    if (!load_qdo(g, wk.qi(0), wk.qbh(0))) {
       aborted = true;
       break;
     }
@@ -269,7 +307,7 @@ __device__ void bwd_load_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sK, ui
     }
     ++kv_issued;
     for (int n = 1; n < n_iter; ++n) {
-      if (!load_qdo(g + n, wk.i0 + n, wk.bh)) {
+      if (!load_qdo(g + n, wk.qi(n), wk.qbh(n))) {
         aborted = true;
         break;
       }
@@ -312,7 +350,7 @@ __device__ void bwd_mma_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sK, uin
                  ds_addr = smem_u32(sDS);
   const uint64_t lim = p.wait_limit_ns;
   const int T = (p.N + 127) / 128;
-  const int total = p.BH * T;
+  const int total = p.BHkv * p.chunks * T;
 
   // D[tmem] = A (128 x HD, K-major) * B (128 x HD, K-major)^T
   auto issue_sq = [&](uint32_t d_col, uint32_t a_addr, uint32_t b_addr) {
@@ -330,7 +368,7 @@ __device__ void bwd_mma_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sK, uin
     const int item = take_item(sh, items, lim);
     if (item < 0) return fail();
     if (item >= total) break;
-    const BwdWork<CAUSAL> wk(item, p.BH, p.N);
+    const BwdWork<CAUSAL> wk(item, p.BHkv, p.N, p.group, p.chunks);
     const int n_iter = wk.n_iter();
     const int s0 = g % C::QST;
     if (!mbar_wait(&sh.kv_full, items & 1, &sh.abort_flag, lim) ||
@@ -424,7 +462,7 @@ __device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS
   const uint32_t tA = tmem + lane_base + C::REG_A + 64 * w;
   const uint32_t tB = tmem + lane_base + C::REG_B + 64 * w;
   const int T = (p.N + 127) / 128;
-  const int total = p.BH * T;
+  const int total = p.BHkv * p.chunks * T;
   bool alive = true;
   // P^T of the current tile as the bf16 pairs written to TMEM, kept from
   // phase A to phase B: dS uses the same rounded P as the dV MMA.
@@ -571,14 +609,19 @@ __device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS
     }
   };
 
-  // ---- item epilogue: w = 0 writes dK_j, w = 1 writes dV_j (fp32 TMEM ->
-  // bf16 -> global; thread r writes key row r, rows past N are skipped).
+  // ---- item epilogue: w = 0 writes dK_j, w = 1 writes dV_j; thread r
+  // writes key row r, rows past N are skipped. One chunk per group: fp32 TMEM
+  // -> bf16 -> dk / dv. Several: the chunk's fp32 partial sum goes to the
+  // workspace, and the post kernel adds the chunks in a fixed order.
   auto epilogue = [&](const BwdWork<CAUSAL>& wk, int items) {
     wait_all(&sh.acc_done, items & 1, WHERE_BWD_SOFTMAX);
     if (!alive) return;
     const int key = wk.j * 128 + r;
     const uint32_t t = tmem + lane_base + (w == 0 ? C::DK_COL : C::DV_COL);
-    __nv_bfloat16* dst = (w == 0 ? p.dk : p.dv) + (static_cast<size_t>(wk.bh) * p.N + key) * HD;
+    const size_t row = static_cast<size_t>(wk.bh) * p.N + key;
+    __nv_bfloat16* dst = (w == 0 ? p.dk : p.dv) + row * HD;
+    const size_t part_len = static_cast<size_t>(p.chunks) * p.BHkv * p.N * HD;
+    float* part = p.kv_part + (w == 0 ? 0 : part_len) + (static_cast<size_t>(wk.c) * p.BHkv * p.N + row) * HD;
 #pragma unroll 1
     for (int c = 0; c < HD; c += 32) {
       uint32_t v[32];
@@ -589,13 +632,19 @@ __device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS
         mbar_arrive(&sh.acc_free);
       }
       if (key < p.N) {
+        if (p.chunks == 1) {
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-          *reinterpret_cast<uint4*>(dst + c + 8 * u) =
-              make_uint4(pack_bf16x2(__uint_as_float(v[8 * u + 0]), __uint_as_float(v[8 * u + 1])),
-                         pack_bf16x2(__uint_as_float(v[8 * u + 2]), __uint_as_float(v[8 * u + 3])),
-                         pack_bf16x2(__uint_as_float(v[8 * u + 4]), __uint_as_float(v[8 * u + 5])),
-                         pack_bf16x2(__uint_as_float(v[8 * u + 6]), __uint_as_float(v[8 * u + 7])));
+          for (int u = 0; u < 4; ++u)
+            *reinterpret_cast<uint4*>(dst + c + 8 * u) =
+                make_uint4(pack_bf16x2(__uint_as_float(v[8 * u + 0]), __uint_as_float(v[8 * u + 1])),
+                           pack_bf16x2(__uint_as_float(v[8 * u + 2]), __uint_as_float(v[8 * u + 3])),
+                           pack_bf16x2(__uint_as_float(v[8 * u + 4]), __uint_as_float(v[8 * u + 5])),
+                           pack_bf16x2(__uint_as_float(v[8 * u + 6]), __uint_as_float(v[8 * u + 7])));
+        } else {
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            *reinterpret_cast<uint4*>(part + c + 4 * u) = make_uint4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+        }
       }
     }
   };
@@ -616,32 +665,32 @@ __device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS
   int item = next_item(0);
   float ld = 0.f;
   if (item < total) {
-    const BwdWork<CAUSAL> wk0(item, p.BH, p.N);
-    ld = fetch_ld(wk0.bh, wk0.i0);
+    const BwdWork<CAUSAL> wk0(item, p.BHkv, p.N, p.group, p.chunks);
+    ld = fetch_ld(wk0.qbh(0), wk0.qi(0));
   }
   while (item < total) {
-    const BwdWork<CAUSAL> wk(item, p.BH, p.N);
+    const BwdWork<CAUSAL> wk(item, p.BHkv, p.N, p.group, p.chunks);
     const int n_iter = wk.n_iter();
     if (items > 0) named_barrier_sync(bar_id, 128);  // the previous item's L2 / D reads are done
     sLD[w * 128 + r] = ld;
     named_barrier_sync(bar_id, 128);
-    phase_a(wk, wk.i0, g);
+    phase_a(wk, wk.qi(0), g);
     for (int n = 0; n < n_iter; ++n) {
       const bool has_next = n + 1 < n_iter;
-      const float next_ld = has_next ? fetch_ld(wk.bh, wk.i0 + n + 1) : 0.f;  // lands during phase B
+      const float next_ld = has_next ? fetch_ld(wk.qbh(n + 1), wk.qi(n + 1)) : 0.f;  // lands during phase B
       phase_b(g + n);
       if (has_next) {
         named_barrier_sync(bar_id, 128);  // every thread is done reading this tile's L2 / D
         sLD[w * 128 + r] = next_ld;
         named_barrier_sync(bar_id, 128);
-        phase_a(wk, wk.i0 + n + 1, g + n + 1);
+        phase_a(wk, wk.qi(n + 1), g + n + 1);
       }
-      drain(wk.bh, wk.i0 + n, g + n);
+      drain(wk.qbh(n), wk.qi(n), g + n);
     }
     const int item_next = next_item(items + 1);
     if (item_next < total) {
-      const BwdWork<CAUSAL> wk1(item_next, p.BH, p.N);
-      ld = fetch_ld(wk1.bh, wk1.i0);  // lands during the epilogue
+      const BwdWork<CAUSAL> wk1(item_next, p.BHkv, p.N, p.group, p.chunks);
+      ld = fetch_ld(wk1.qbh(0), wk1.qi(0));  // lands during the epilogue
     }
     epilogue(wk, items);
     g += n_iter;
@@ -740,6 +789,11 @@ template <int HD>
 cudaError_t launch_post_t(const BwdLaunch& a, cudaStream_t stream) {
   const long long vec = static_cast<long long>(a.BH) * a.N * (HD / 8);
   bwd_post_kernel<HD><<<static_cast<unsigned>((vec + 255) / 256), 256, 0, stream>>>(a.dq_acc, a.dq, a.N, a.Npad, vec);
+  if (a.chunks > 1) {
+    const long long n8 = static_cast<long long>(a.BHkv) * a.N * HD / 8;
+    bwd_kv_sum_kernel<<<static_cast<unsigned>((2 * n8 + 255) / 256), 256, 0, stream>>>(a.kv_part, a.dk, a.dv,
+                                                                                     a.chunks, n8);
+  }
   return cudaGetLastError();
 }
 

@@ -53,15 +53,18 @@ struct Shared256 {
   int abort_flag;
 };
 
+// Key tile j of K/V head bh, half h of the head dimension. The query stream
+// is, for each of the g query heads that share this K/V head (query head
+// bh*g + t), 64-row query tiles i0..T64-1 (causal: i0 = 2j).
 template <bool CAUSAL>
 struct Work256 {
-  int bh, j, h, i0, T64;
-  __device__ Work256(int block, int BH, int N) {
+  int bh, j, h, i0, T64, nq, g;
+  __device__ Work256(int block, int BHkv, int N, int group) {
     const int T = (N + 127) / 128;
     T64 = (N + 63) / 64;
     if (CAUSAL) {  // key tiles with the most query tiles first
-      j = block / (2 * BH);
-      const int rem = block % (2 * BH);
+      j = block / (2 * BHkv);
+      const int rem = block % (2 * BHkv);
       bh = rem >> 1;
       h = rem & 1;
     } else {
@@ -71,8 +74,12 @@ struct Work256 {
       h = rem & 1;
     }
     i0 = CAUSAL ? 2 * j : 0;
+    nq = T64 - i0;
+    g = group;
   }
-  __device__ int n_iter() const { return T64 - i0; }
+  __device__ int n_iter() const { return g * nq; }
+  __device__ int qbh(int n) const { return bh * g + n / nq; }  // query head of step n
+  __device__ int qi(int n) const { return i0 + n % nq; }       // 64-row query tile of step n
 };
 
 template <bool CAUSAL>
@@ -94,14 +101,14 @@ __device__ void load_role(const BwdLaunch& p, Shared256& sh, uint8_t* sK, uint8_
   int q_issued = 0, do_issued = 0;
   bool aborted = false;
   for (int n = 0; n < n_iter && !aborted; ++n) {
-    const int i = wk.i0 + n;
+    const int i = wk.qi(n), qbh = wk.qbh(n);
     if (n > 0 && !mbar_wait(&sh.q_empty, (n - 1) & 1, &sh.abort_flag, p.wait_limit_ns)) {
       aborted = true;
       break;
     }
     mbar_arrive_expect_tx(&sh.q_full, C::Q_BYTES);
 #pragma unroll
-    for (int c = 0; c < 4; ++c) tma_load_3d(sQ + c * C::Q_CHUNK, &p.tmQ, &sh.q_full, c * 64, i * C::BQ, wk.bh);
+    for (int c = 0; c < 4; ++c) tma_load_3d(sQ + c * C::Q_CHUNK, &p.tmQ, &sh.q_full, c * 64, i * C::BQ, qbh);
     ++q_issued;
     if (n > 0 && !mbar_wait(&sh.do_empty, (n - 1) & 1, &sh.abort_flag, p.wait_limit_ns)) {
       aborted = true;
@@ -109,7 +116,7 @@ __device__ void load_role(const BwdLaunch& p, Shared256& sh, uint8_t* sK, uint8_
     }
     mbar_arrive_expect_tx(&sh.do_full, C::Q_BYTES);
 #pragma unroll
-    for (int c = 0; c < 4; ++c) tma_load_3d(sdO + c * C::Q_CHUNK, &p.tmdO, &sh.do_full, c * 64, i * C::BQ, wk.bh);
+    for (int c = 0; c < 4; ++c) tma_load_3d(sdO + c * C::Q_CHUNK, &p.tmdO, &sh.do_full, c * 64, i * C::BQ, qbh);
     ++do_issued;
   }
   if (aborted) {
@@ -200,28 +207,27 @@ __device__ void softmax_role(const BwdLaunch& p, Shared256& sh, uint8_t* sDS, fl
   const uint64_t lim = p.wait_limit_ns;
   float* ld_l2 = sLD + w * 64;
   float* ld_d = ld_l2 + 32;
-  const float* lse2_bh = p.lse2 + static_cast<size_t>(wk.bh) * p.Npad + 32 * w;
-  const float* D_bh = p.D + static_cast<size_t>(wk.bh) * p.Npad + 32 * w;
   const int n_iter = wk.n_iter();
   const uint32_t bar_id = 1 + w;
   bool alive = true;
 
-  // thread r < 32 holds L2 of query 32w + r of tile i, 32 <= r < 64 its scaled D
-  auto fetch_ld = [&](int i) -> float {
-    if (r < 32) return __ldg(lse2_bh + i * C::BQ + r);
-    if (r < 64) return __ldg(D_bh + i * C::BQ + (r - 32)) * sc;
+  // thread r < 32 holds L2 of query 32w + r of step n's tile, 32 <= r < 64 its scaled D
+  auto fetch_ld = [&](int n) -> float {
+    const size_t row = static_cast<size_t>(wk.qbh(n)) * p.Npad + wk.qi(n) * C::BQ + 32 * w;
+    if (r < 32) return __ldg(p.lse2 + row + r);
+    if (r < 64) return __ldg(p.D + row + (r - 32)) * sc;
     return 0.f;
   };
   {
-    const float v = fetch_ld(wk.i0);
+    const float v = fetch_ld(0);
     if (r < 64) sLD[w * 64 + r] = v;
     named_barrier_sync(bar_id, 128);
   }
 
   for (int n = 0; n < n_iter; ++n) {
-    const int i = wk.i0 + n;
+    const int i = wk.qi(n);
     const bool has_next = n + 1 < n_iter;
-    const float next_ld = has_next ? fetch_ld(i + 1) : 0.f;
+    const float next_ld = has_next ? fetch_ld(n + 1) : 0.f;
     const uint32_t tS = tmem + lane_base + C::REG_S + 32 * w;
     const uint32_t tDP = tmem + lane_base + C::REG_DP + 32 * w;
     // ---- phase A: P^T for this warpgroup's 32 queries, bf16 back into TMEM
@@ -292,7 +298,7 @@ __device__ void softmax_role(const BwdLaunch& p, Shared256& sh, uint8_t* sDS, fl
       tmem_ld_wait();
       tc_fence_before_sync();
       mbar_arrive(&sh.dq_free);
-      float* dst = p.dq_acc + (static_cast<size_t>(wk.bh) * p.Npad + i * C::BQ + 32 * w) * C::HD + 128 * wk.h + r;
+      float* dst = p.dq_acc + (static_cast<size_t>(wk.qbh(n)) * p.Npad + i * C::BQ + 32 * w) * C::HD + 128 * wk.h + r;
 #pragma unroll
       for (int c = 0; c < 32; ++c) red_add_f32(dst + static_cast<size_t>(c) * C::HD, __uint_as_float(v[c]));
     }
@@ -363,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd256_kernel(const __grid_con
   uint8_t* sDS = sdO + C::Q_BYTES;
   float* sLD = reinterpret_cast<float*>(sDS + C::DS_BYTES);
   const int warp = threadIdx.x >> 5;
-  const Work256<CAUSAL> wk(blockIdx.x, p.BH, p.N);
+  const Work256<CAUSAL> wk(blockIdx.x, p.BHkv, p.N, p.group);
 
   if (threadIdx.x == 0) {
     mbar_init(&sh.kv_full, 1);
@@ -413,7 +419,7 @@ cudaError_t launch_t(const BwdLaunch& a, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg256::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const int T = (a.N + 127) / 128;
-  kern<<<static_cast<unsigned>(static_cast<long long>(a.BH) * T * 2), kThreads, Cfg256::SMEM_BYTES, stream>>>(a);
+  kern<<<static_cast<unsigned>(static_cast<long long>(a.BHkv) * T * 2), kThreads, Cfg256::SMEM_BYTES, stream>>>(a);
   return cudaGetLastError();
 }
 

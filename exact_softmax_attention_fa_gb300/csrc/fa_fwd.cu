@@ -144,6 +144,7 @@ __device__ void fwd_load_role(const FwdLaunch& p, FwdShared& sh, uint8_t* sQ, ui
     const int item = sched_item(k, blockIdx.x, G);
     if (item >= total) continue;
     const FwdWork<C::NT, CAUSAL> wk(item, p.BH, p.N);
+    const int kv_bh = wk.bh / p.group;  // grouped K/V heads: query head bh reads K/V head bh / g
     // Q_t's smem was the previous item's O staging: wait until its store read
     // it. The item's first K/V tile is issued before that wait so it loads
     // while the previous epilogue runs.
@@ -177,7 +178,7 @@ __device__ void fwd_load_role(const FwdLaunch& p, FwdShared& sh, uint8_t* sQ, ui
       mbar_arrive_expect_tx(&sh.k_full[ks], C::TILE_BYTES);
 #pragma unroll
       for (int c = 0; c < C::CHUNKS; ++c)
-        tma_load_3d(sK + ks * C::TILE_BYTES + c * C::CHUNK_BYTES, &p.tmK, &sh.k_full[ks], c * 64, j * 128, wk.bh);
+        tma_load_3d(sK + ks * C::TILE_BYTES + c * C::CHUNK_BYTES, &p.tmK, &sh.k_full[ks], c * 64, j * 128, kv_bh);
       ++k_issued;
       if (j == 0 && !load_q()) {
         aborted = true;
@@ -191,7 +192,7 @@ __device__ void fwd_load_role(const FwdLaunch& p, FwdShared& sh, uint8_t* sQ, ui
       mbar_arrive_expect_tx(&sh.v_full[vs], C::TILE_BYTES);
 #pragma unroll
       for (int c = 0; c < C::CHUNKS; ++c)
-        tma_load_3d(sV + vs * C::TILE_BYTES + c * C::CHUNK_BYTES, &p.tmV, &sh.v_full[vs], c * 64, j * 128, wk.bh);
+        tma_load_3d(sV + vs * C::TILE_BYTES + c * C::CHUNK_BYTES, &p.tmV, &sh.v_full[vs], c * 64, j * 128, kv_bh);
       ++v_issued;
     }
     if (aborted) break;

@@ -31,6 +31,7 @@ struct FwdLaunch {
   float* lse;
   uint32_t* status;
   int N, BH, d, causal;
+  int group;         // query heads per K/V head: query head bh reads K/V head bh / group
   float scale_log2;  // scale * log2(e): scores are exponentiated in base 2
   uint64_t wait_limit_ns;
   int num_sms;
@@ -51,6 +52,9 @@ struct BwdLaunch {
   uint32_t* sched;  // [2]: next work item to hand out, CTAs done claiming
   uint32_t* status;
   int N, Npad, BH, d, causal;
+  int BHkv, group;   // K/V heads (B * H_kv) and query heads per K/V head
+  int chunks;        // work items per (K/V head, key tile): the group split into chunks of group/chunks heads
+  float* kv_part;    // chunks > 1: fp32 partial dK [chunks][BHkv][N][d], then partial dV likewise
   float scale;       // softmax scale (dK, dQ carry it)
   float scale_log2;  // scale * log2(e)
   uint64_t wait_limit_ns;

@@ -17,6 +17,7 @@
  *   "FlashAttention" (llm-infra-atlas), section 1, for the 1/sqrt(d) scale.
  *   "FlashAttention-2: ..." (paper-graph-ui summary), "Causal masking
  *   optimization": entries whose column index exceeds the row index are -inf.
+ *   Reading note 5.6 for grouped / multi-query K/V heads (fa_*_gqa).
  *
  * Conventions shared by every entry point:
  *   - Tensors are contiguous, row-major [B][H][N][d]; q, k, v, o, dO, dq, dk,
@@ -70,6 +71,19 @@ fa_status_t fa_fwd(const void* q, const void* k, const void* v, void* o, float* 
                    int causal, float scale, cudaStream_t stream);
 
 /*
+ * Forward pass with grouped / multi-query K/V heads (reading note 5.6;
+ * paper-graph-ui summary, "Multi-query and grouped-query attention"): Hq query
+ * heads share Hkv K/V heads, g = Hq / Hkv query heads per K/V head, and query
+ * head h reads K/V head floor(h / g). Nothing is copied.
+ *   q, o    : bf16 [B][Hq][N][d];  lse : fp32 [B][Hq][N]
+ *   k, v    : bf16 [B][Hkv][N][d]
+ *   Hkv     : >= 1 and dividing Hq (else FA_ERR_INVALID_ARG); Hkv == Hq is fa_fwd.
+ * Other arguments and errors as for fa_fwd.
+ */
+fa_status_t fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                       int N, int d, int causal, float scale, cudaStream_t stream);
+
+/*
  * Bytes of device workspace fa_bwd needs: D and the base-2 logsumexp
  * (fp32 per query row) and the fp32 dQ accumulator, with every head padded
  * to a multiple of 128 rows, plus 256 bytes for the main kernel's work-item
@@ -94,6 +108,29 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d);
 fa_status_t fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
                    void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal, float scale,
                    void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Backward pass with grouped / multi-query K/V heads (reading note 5.6): the
+ * gradient of a shared K/V head is the sum over its g query heads,
+ *   dK_{h_kv} = sum over h with floor(h / g) = h_kv of dK_h (same for dV).
+ * A work item accumulates one key tile's dK, dV on chip over a chunk of the g
+ * query heads. When the problem has too few (K/V head, key tile) pairs to
+ * fill the GPU, or, under a causal mask, too long an item, the library
+ * splits each group into chunks; their fp32 partial sums go to the workspace
+ * and a post kernel adds them in chunk order. Either way dk and dv are
+ * bitwise reproducible.
+ *   q, o, dO, dq : bf16 [B][Hq][N][d];  lse : fp32 [B][Hq][N]
+ *   k, v, dk, dv : bf16 [B][Hkv][N][d]
+ *   workspace    : at least fa_bwd_workspace_size(B, Hq, N, d) bytes; the
+ *                  group is split only as far as the bytes beyond that allow
+ *                  (fa_bwd_gqa_workspace_size leaves room for every split).
+ * Other arguments and errors as for fa_bwd; Hkv == Hq is fa_bwd.
+ */
+size_t fa_bwd_gqa_workspace_size(int B, int Hq, int Hkv, int N, int d);
+
+fa_status_t fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                       const void* dO, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N, int d,
+                       int causal, float scale, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
  * The three phases fa_bwd runs, in order, on one stream (each also callable on

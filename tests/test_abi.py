@@ -65,6 +65,42 @@ def test_empty_problem_is_a_no_op(lib):
         assert lib.fa_bwd_workspace_size(kw.get("B", 1), kw.get("H", 1), kw.get("N", 128), 64) == 0
 
 
+def fwd_gqa(lib, ptr=P, lse=P, B=1, Hq=4, Hkv=2, N=128, d=64, causal=0, scale=0.125):
+    return lib.fa_fwd_gqa(ptr, ptr, ptr, ptr, lse, B, Hq, Hkv, N, d, causal, scale, None)
+
+
+def bwd_gqa(lib, ptr=P, lse=P, ws=P, ws_bytes=1 << 30, B=1, Hq=4, Hkv=2, N=128, d=64, causal=0, scale=0.125):
+    return lib.fa_bwd_gqa(ptr, ptr, ptr, ptr, lse, ptr, ptr, ptr, ptr, B, Hq, Hkv, N, d, causal, scale, ws, ws_bytes,
+                          None)
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(4, 0), (4, -1), (4, 3), (2, 4), (4, 8)])
+def test_grouped_heads_must_divide(lib, Hq, Hkv):
+    assert fwd_gqa(lib, Hq=Hq, Hkv=Hkv) == INVALID
+    assert bwd_gqa(lib, Hq=Hq, Hkv=Hkv) == INVALID
+
+
+def test_grouped_workspace_size(lib):
+    for B, Hq, Hkv, N, d in ((2, 8, 2, 1000, 64), (1, 16, 1, 300, 128), (1, 4, 4, 100, 128), (1, 4, 2, 100, 256)):
+        base = lib.fa_bwd_workspace_size(B, Hq, N, d)
+        g = Hq // Hkv
+        extra = 0 if (g == 1 or d == 256) else g * B * Hkv * N * d * 8  # fp32 dK + dV partial per chunk
+        assert lib.fa_bwd_gqa_workspace_size(B, Hq, Hkv, N, d) == base + extra
+    assert lib.fa_bwd_gqa_workspace_size(1, 4, 3, 128, 64) == 0
+    assert lib.fa_bwd_gqa_workspace_size(1, 4, 0, 128, 64) == 0
+
+
+def test_grouped_heads_other_checks(lib):
+    assert fwd_gqa(lib, d=96) == UNSUPPORTED
+    assert bwd_gqa(lib, scale=0.0) == INVALID
+    assert fwd_gqa(lib, ptr=0) == INVALID
+    assert bwd_gqa(lib, ws=0) == WORKSPACE
+    assert fwd_gqa(lib, ptr=P + 8) == MISALIGNED
+    # empty problems do nothing, null pointers allowed
+    assert fwd_gqa(lib, ptr=0, lse=0, Hq=0, Hkv=0) == OK
+    assert bwd_gqa(lib, ptr=0, lse=0, ws=0, ws_bytes=0, N=0) == OK
+
+
 @pytest.mark.parametrize("which", ["q", "k", "v", "o"])
 def test_misaligned_bf16(lib, which):
     assert fwd(lib, **{which: P + 8}) == MISALIGNED
