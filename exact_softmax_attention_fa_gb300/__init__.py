@@ -15,7 +15,7 @@ import math
 
 from ._lib import load, check, FAError, header_functions, STATUS_NAMES  # noqa: F401
 
-__all__ = ["fa_fwd", "fa_bwd", "fa_fwd_gqa", "fa_bwd_gqa", "fa_bwd_workspace_size", "fa_bwd_gqa_workspace_size", "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_postprocess", "fa_bwd_noalloc", "fa_get_device_status", "fa_set_wait_limit_ns",
+__all__ = ["fa_fwd", "fa_bwd", "fa_fwd_gqa", "fa_bwd_gqa", "fa_bwd_deterministic", "fa_bwd_gqa_deterministic", "fa_bwd_workspace_size", "fa_bwd_gqa_workspace_size", "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_postprocess", "fa_bwd_noalloc", "fa_get_device_status", "fa_set_wait_limit_ns",
            "fa_debug_timeout_probe", "forward", "backward", "FAError", "flops"]
 
 _SUPPORTED_D = (64, 128, 256)
@@ -107,6 +107,35 @@ def fa_bwd_gqa(q, k, v, o, lse, do, dq, dk, dv, causal: bool, scale: float, work
                                        do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
                                        B, Hq, Hkv, N, d, int(bool(causal)), float(scale), *_ws(workspace),
                                        _stream_handle(stream)))
+
+
+def fa_bwd_deterministic(q, k, v, o, lse, do, dq, dk, dv, causal: bool, scale: float, workspace, stream=None) -> None:
+    """fa_bwd_deterministic of the C ABI: fa_bwd with a bitwise-reproducible dq (d = 64, 128)."""
+    shape = _dims(q)
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do), ("dq", dq), ("dk", dk), ("dv", dv)):
+        _check_bf16(name, t, shape)
+    _check_lse(lse, shape)
+    B, H, N, d = shape
+    check("fa_bwd_deterministic",
+          load().fa_bwd_deterministic(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                      do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d,
+                                      int(bool(causal)), float(scale), *_ws(workspace), _stream_handle(stream)))
+
+
+def fa_bwd_gqa_deterministic(q, k, v, o, lse, do, dq, dk, dv, causal: bool, scale: float, workspace,
+                             stream=None) -> None:
+    """fa_bwd_gqa_deterministic of the C ABI: fa_bwd_gqa with a bitwise-reproducible dq (d = 64, 128)."""
+    B, Hq, Hkv, N, d = _gqa_dims(q, k)
+    qs, ks = (B, Hq, N, d), (B, Hkv, N, d)
+    for name, t, shape in (("q", q, qs), ("k", k, ks), ("v", v, ks), ("o", o, qs), ("do", do, qs), ("dq", dq, qs),
+                           ("dk", dk, ks), ("dv", dv, ks)):
+        _check_bf16(name, t, shape)
+    _check_lse(lse, qs)
+    check("fa_bwd_gqa_deterministic",
+          load().fa_bwd_gqa_deterministic(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                          do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv,
+                                          N, d, int(bool(causal)), float(scale), *_ws(workspace),
+                                          _stream_handle(stream)))
 
 
 def fa_bwd_workspace_size(B: int, H: int, N: int, d: int) -> int:
@@ -223,9 +252,11 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, stream=No
     return o, lse
 
 
-def backward(q, k, v, o, lse, do, causal: bool = False, scale: float | None = None, workspace=None, stream=None):
+def backward(q, k, v, o, lse, do, causal: bool = False, scale: float | None = None, workspace=None, stream=None,
+             deterministic: bool = False):
     """Allocate dQ, dK, dV (and the workspace if not given) with torch and run fa_bwd
-    (fa_bwd_gqa when k, v have fewer heads than q)."""
+    (fa_bwd_gqa when k, v have fewer heads than q; the *_deterministic entry
+    points when `deterministic`)."""
     import torch
     B, H, N, d = _dims(q)
     if scale is None:
@@ -236,9 +267,10 @@ def backward(q, k, v, o, lse, do, causal: bool = False, scale: float | None = No
         size = fa_bwd_gqa_workspace_size(B, H, int(k.shape[1]), N, d) if grouped else fa_bwd_workspace_size(B, H, N, d)
         workspace = torch.empty(max(1, size), dtype=torch.uint8, device=q.device)
     if grouped:
-        fa_bwd_gqa(q, k, v, o, lse, do, dq, dk, dv, causal, scale, workspace, stream)
+        fn = fa_bwd_gqa_deterministic if deterministic else fa_bwd_gqa
     else:
-        fa_bwd(q, k, v, o, lse, do, dq, dk, dv, causal, scale, workspace, stream)
+        fn = fa_bwd_deterministic if deterministic else fa_bwd
+    fn(q, k, v, o, lse, do, dq, dk, dv, causal, scale, workspace, stream)
     return dq, dk, dv
 
 

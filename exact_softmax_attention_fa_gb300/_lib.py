@@ -32,6 +32,10 @@ _SIGNATURES = {
     "fa_fwd": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_float, _vp]),
     "fa_fwd_gqa": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_float, _vp]),
     "fa_bwd_workspace_size": (ctypes.c_size_t, [_c_int, _c_int, _c_int, _c_int]),
+    "fa_bwd_deterministic": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
+                                      _c_int, _c_float, _vp, ctypes.c_size_t, _vp]),
+    "fa_bwd_gqa_deterministic": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int,
+                                          _c_int, _c_int, _c_int, _c_float, _vp, ctypes.c_size_t, _vp]),
     "fa_bwd_gqa_workspace_size": (ctypes.c_size_t, [_c_int, _c_int, _c_int, _c_int, _c_int]),
     "fa_bwd_gqa": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int,
                             _c_int, _c_float, _vp, ctypes.c_size_t, _vp]),

@@ -385,6 +385,37 @@ fa_status_t fa_bwd_gqa(const void* q, const void* k, const void* v, const void* 
   return from_cuda(e);
 }
 
+fa_status_t fa_bwd_gqa_deterministic(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                                     const void* dO, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N,
+                                     int d, int causal, float scale, void* workspace, size_t workspace_bytes,
+                                     cudaStream_t stream) {
+  bool empty = false;
+  fa_status_t st = check_common(B, Hq, N, d, causal, scale, &empty);
+  if (st != FA_OK) return st;
+  if (d == 256) return FA_ERR_UNSUPPORTED;
+  st = check_heads(Hq, Hkv);
+  if (st != FA_OK) return st;
+  if (empty) return FA_OK;
+  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  BwdLaunch a;
+  st = prepare_bwd(BwdTensors{q, k, v, o, dO, lse, dq, dk, dv}, B, Hq, Hkv, N, d, causal, scale, workspace,
+                   workspace_bytes, &empty, &a);
+  if (st != FA_OK || empty) return st;
+  a.deterministic = 1;
+  cudaError_t e = launch_bwd_pre(a, stream);
+  if (e == cudaSuccess) e = launch_bwd_main(a, stream);  // dK, dV only
+  if (e == cudaSuccess) e = launch_bwd_dq(a, stream);
+  if (e == cudaSuccess) e = launch_bwd_post(a, stream);  // split groups' dK, dV sums, if any
+  return from_cuda(e);
+}
+
+fa_status_t fa_bwd_deterministic(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                                 const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal,
+                                 float scale, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return fa_bwd_gqa_deterministic(q, k, v, o, lse, dO, dq, dk, dv, B, H, H, N, d, causal, scale, workspace,
+                                  workspace_bytes, stream);
+}
+
 fa_status_t fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
                    void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal, float scale,
                    void* workspace, size_t workspace_bytes, cudaStream_t stream) {

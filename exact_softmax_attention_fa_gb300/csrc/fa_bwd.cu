@@ -123,21 +123,11 @@ struct BwdWork {
   __device__ int qi(int n) const { return i0 + n % nq; }   // query tile of step n
 };
 
-// Dynamic schedule: CTA b starts on item b; afterwards the load thread claims
-// item G + atomicAdd(sched[0], 1) each time it finishes issuing an item's
-// loads, so CTAs that run ahead take more items (causal items come heaviest
-// first). The claimed index goes through a 4-slot smem queue to the MMA
-// thread and the 256 softmax threads.
-constexpr int kItemSlots = 4;
+// Dynamic schedule (fa_kernel_common.cuh): items are claimed from sched[0..1]
+// of the workspace, so CTAs that run ahead take more items and causal items
+// come heaviest first. Consumers of the item queue: the MMA thread and the
+// 256 softmax threads.
 constexpr int kItemConsumers = 1 + 256;
-
-__device__ __forceinline__ int take_item(BwdShared& sh, int u, uint64_t lim) {
-  const int s = u % kItemSlots;
-  if (!mbar_wait(&sh.item_full[s], (u / kItemSlots) & 1, &sh.abort_flag, lim)) return -1;
-  const int item = *reinterpret_cast<volatile int*>(&sh.item_ring[s]);
-  mbar_arrive(&sh.item_empty[s]);
-  return item;
-}
 
 // Grouped K/V heads split over several work items: dK, dV = bf16 of the sum
 // of the chunks' fp32 partials, added in chunk order (bitwise reproducible).
@@ -177,7 +167,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
                                                       float* __restrict__ lse2, float* __restrict__ dq_acc,
                                                       uint32_t* __restrict__ sched, int N, int Npad,
                                                       long long total_rows) {
-  if (blockIdx.x == 0 && threadIdx.x < 2) sched[threadIdx.x] = 0u;
+  if (blockIdx.x == 0 && threadIdx.x < 4) sched[threadIdx.x] = 0u;
   constexpr int LPR = HD / 8;  // lanes per row, 16 bytes of O and dO each
   constexpr int RPW = 32 / LPR;
   const long long row = (static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32) * RPW +
@@ -204,9 +194,11 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
         acc = fmaf(fa.y, fb.y, acc);
       }
     }
-    float4* z = reinterpret_cast<float4*>(dq_acc + static_cast<size_t>(row) * HD + sub * 8);
-    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (dq_acc) {  // null when dQ is formed without the accumulator
+      float4* z = reinterpret_cast<float4*>(dq_acc + static_cast<size_t>(row) * HD + sub * 8);
+      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
   }
 #pragma unroll
   for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
@@ -258,18 +250,9 @@ __device__ void bwd_load_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sK, ui
   tma_prefetch_desc(&p.tmdQacc);
   const int T = (p.N + 127) / 128;
   const int total = p.BHkv * p.chunks * T;
-  const int G = gridDim.x;
   const uint64_t lim = p.wait_limit_ns;
   int g = 0, items = 0, issued = 0, kv_issued = 0;
   bool aborted = false;
-  auto publish = [&](int u, int item) -> bool {
-    const int s = u % kItemSlots;
-    if (u >= kItemSlots && !mbar_wait(&sh.item_empty[s], ((u / kItemSlots) - 1) & 1, &sh.abort_flag, lim))
-      return false;
-    *reinterpret_cast<volatile int*>(&sh.item_ring[s]) = item;
-    mbar_arrive(&sh.item_full[s]);
-    return true;
-  };
   auto load_qdo = [&](int gg, int i, int bh) -> bool {
     const int s = gg % C::QST;
     if (gg >= C::QST && !mbar_wait(&sh.qdo_empty[s], ((gg / C::QST) - 1) & 1, &sh.abort_flag, lim)) return false;
@@ -284,7 +267,7 @@ __device__ void bwd_load_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sK, ui
   };
   int item = blockIdx.x;  // the grid never exceeds the item count
   while (!aborted) {
-    if (!publish(items, item)) {
+    if (!publish_item(sh, items, item, lim)) {
       aborted = true;
       break;
     }
@@ -314,13 +297,9 @@ __device__ void bwd_load_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sK, ui
     }
     g += n_iter;
     ++items;
-    if (!aborted) item = G + static_cast<int>(atomicAdd(p.sched, 1u));
+    if (!aborted) item = claim_item(p.sched);
   }
-  // The last CTA done claiming resets the counter for the next launch.
-  if (atomicAdd(p.sched + 1, 1u) == static_cast<uint32_t>(G - 1)) {
-    atomicExch(p.sched, 0u);
-    atomicExch(p.sched + 1, 0u);
-  }
+  finish_claiming(p.sched);
   const int zero = 0;
   if (aborted) {
     record_timeout(p.status, &sh.abort_flag, WHERE_BWD_LOAD);
@@ -339,7 +318,7 @@ __device__ void bwd_load_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sK, ui
 //   dP^T(n+1) -> B        after the dQ_n drain
 // An item's first dV/dK (which overwrite the accumulators) wait until the
 // previous item's epilogue has read dK/dV out of TMEM.
-template <int HD, bool CAUSAL>
+template <int HD, bool CAUSAL, bool DQ>
 __device__ void bwd_mma_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sK, uint8_t* sV, uint8_t* sQ,
                              uint8_t* sdO, uint8_t* sDS, uint32_t tmem) {
   using C = BwdCfg<HD>;
@@ -379,7 +358,7 @@ __device__ void bwd_mma_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sK, uin
     tc_fence_after_sync();
     issue_sq(C::REG_A, k_addr, q_addr + s0 * C::TILE_BYTES);  // S^T(first)
     umma_commit(&sh.s_full);
-    if (g > 0 && !mbar_wait(&sh.dq_free, (g - 1) & 1, &sh.abort_flag, lim)) return fail();
+    if (DQ && g > 0 && !mbar_wait(&sh.dq_free, (g - 1) & 1, &sh.abort_flag, lim)) return fail();
     tc_fence_after_sync();
     issue_sq(C::REG_B, v_addr, do_addr + s0 * C::TILE_BYTES);  // dP^T(first)
     umma_commit(&sh.dp_full);
@@ -413,22 +392,24 @@ __device__ void bwd_mma_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sK, uin
       for (int ks = 0; ks < 8; ++ks)
         umma_ss(tmem + C::DK_COL, make_smem_desc_sw128(ds_addr + (ks >> 2) * C::CHUNK_BYTES + (ks & 3) * 32, 16, 1024),
                 make_smem_desc_sw128(qa + ks * 2048, C::CHUNK_BYTES, 1024), kIdescAcc, (n > 0 || ks > 0) ? 1u : 0u);
-      // dQ_n into region B. d = 128: dQ_n^T = K_j^T dS^T (head-dim columns on
-      // the lanes, queries along the columns), so the drain's reductions
-      // cover whole 128-byte lines. d = 64: dQ_n = dS K_j (queries on lanes).
+      if constexpr (DQ) {
+        // dQ_n into region B. d = 128: dQ_n^T = K_j^T dS^T (head-dim columns on
+        // the lanes, queries along the columns), so the drain's reductions
+        // cover whole 128-byte lines. d = 64: dQ_n = dS K_j (queries on lanes).
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const uint64_t ds_mn = make_smem_desc_sw128(ds_addr + ks * 2048, C::CHUNK_BYTES, 1024);
-        const uint64_t k_mn = make_smem_desc_sw128(k_addr + ks * 2048, C::CHUNK_BYTES, 1024);
-        if constexpr (C::DQ_T)
-          umma_ss(tmem + C::REG_B, k_mn, ds_mn, kIdescDq, ks > 0 ? 1u : 0u);
-        else
-          umma_ss(tmem + C::REG_B, ds_mn, k_mn, kIdescDq, ks > 0 ? 1u : 0u);
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint64_t ds_mn = make_smem_desc_sw128(ds_addr + ks * 2048, C::CHUNK_BYTES, 1024);
+          const uint64_t k_mn = make_smem_desc_sw128(k_addr + ks * 2048, C::CHUNK_BYTES, 1024);
+          if constexpr (C::DQ_T)
+            umma_ss(tmem + C::REG_B, k_mn, ds_mn, kIdescDq, ks > 0 ? 1u : 0u);
+          else
+            umma_ss(tmem + C::REG_B, ds_mn, k_mn, kIdescDq, ks > 0 ? 1u : 0u);
+        }
+        umma_commit(&sh.dq_full);
       }
-      umma_commit(&sh.dq_full);
       umma_commit(&sh.qdo_empty[s]);
       if (has_next) {
-        if (!mbar_wait(&sh.dq_free, g & 1, &sh.abort_flag, lim)) return fail();
+        if (DQ && !mbar_wait(&sh.dq_free, g & 1, &sh.abort_flag, lim)) return fail();
         tc_fence_after_sync();
         issue_sq(C::REG_B, v_addr, do_addr + s1 * C::TILE_BYTES);  // dP^T(n+1) over the drained dQ_n
         umma_commit(&sh.dp_full);
@@ -446,7 +427,7 @@ __device__ void bwd_mma_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sK, uin
 // the drain's reductions overlap dP^T(n+1) and dV(n+1). After an item's last
 // tile, warpgroup 0 writes dK_j and warpgroup 1 dV_j straight from TMEM to
 // global memory while the MMA warp already starts the next item.
-template <int HD, bool CAUSAL>
+template <int HD, bool CAUSAL, bool DQ>
 __device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS, float* sLD, uint8_t* sDQ,
                                  uint32_t tmem, int w) {
   using C = BwdCfg<HD>;
@@ -685,7 +666,7 @@ __device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS
         named_barrier_sync(bar_id, 128);
         phase_a(wk, wk.qi(n + 1), g + n + 1);
       }
-      drain(wk.qbh(n), wk.qi(n), g + n);
+      if constexpr (DQ) drain(wk.qbh(n), wk.qi(n), g + n);
     }
     const int item_next = next_item(items + 1);
     if (item_next < total) {
@@ -697,10 +678,10 @@ __device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS
     ++items;
     item = item_next;
   }
-  if (!C::DQ_T && r == 0) tma_store_wait_all();  // reduce-adds complete before the CTA can exit
+  if (DQ && !C::DQ_T && r == 0) tma_store_wait_all();  // reduce-adds complete before the CTA can exit
 }
 
-template <int HD, bool CAUSAL>
+template <int HD, bool CAUSAL, bool DQ>
 __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_constant__ BwdLaunch p) {
   using C = BwdCfg<HD>;
   extern __shared__ uint8_t smem_dyn[];
@@ -750,9 +731,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
   if (warp == kLoadWarp) {
     if (lane_id() == 0) bwd_load_role<HD, CAUSAL>(p, sh, sK, sV, sQ, sdO);
   } else if (warp == kMmaWarp) {
-    if (lane_id() == 0) bwd_mma_role<HD, CAUSAL>(p, sh, sK, sV, sQ, sdO, sDS, tmem);
+    if (lane_id() == 0) bwd_mma_role<HD, CAUSAL, DQ>(p, sh, sK, sV, sQ, sdO, sDS, tmem);
   } else {
-    bwd_softmax_role<HD, CAUSAL>(p, sh, sDS, sLD, sDQ, tmem, wg);
+    bwd_softmax_role<HD, CAUSAL, DQ>(p, sh, sDS, sLD, sDQ, tmem, wg);
   }
 
   tc_fence_before_sync();
@@ -766,15 +747,16 @@ cudaError_t launch_pre_t(const BwdLaunch& a, cudaStream_t stream) {
   const long long rows = static_cast<long long>(a.BH) * a.Npad;
   constexpr int RPB = 8 * (32 / (HD / 8));  // rows per 256-thread block
   const long long blocks = (rows + RPB - 1) / RPB;
-  bwd_pre_kernel<HD><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a.o, a.dO, a.lse, a.D, a.lse2, a.dq_acc, a.sched,
+  bwd_pre_kernel<HD><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a.o, a.dO, a.lse, a.D, a.lse2,
+                                                                        a.deterministic ? nullptr : a.dq_acc, a.sched,
                                                                         a.N, a.Npad, rows);
   return cudaGetLastError();
 }
 
-template <int HD, bool CAUSAL>
+template <int HD, bool CAUSAL, bool DQ>
 cudaError_t launch_main_t(const BwdLaunch& a, cudaStream_t stream) {
   using C = BwdCfg<HD>;
-  auto kern = fa_bwd_kernel<HD, CAUSAL>;
+  auto kern = fa_bwd_kernel<HD, CAUSAL, DQ>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const int T = (a.N + 127) / 128;
@@ -788,7 +770,9 @@ cudaError_t launch_main_t(const BwdLaunch& a, cudaStream_t stream) {
 template <int HD>
 cudaError_t launch_post_t(const BwdLaunch& a, cudaStream_t stream) {
   const long long vec = static_cast<long long>(a.BH) * a.N * (HD / 8);
-  bwd_post_kernel<HD><<<static_cast<unsigned>((vec + 255) / 256), 256, 0, stream>>>(a.dq_acc, a.dq, a.N, a.Npad, vec);
+  if (!a.deterministic)  // the dQ kernel has written dq itself
+    bwd_post_kernel<HD><<<static_cast<unsigned>((vec + 255) / 256), 256, 0, stream>>>(a.dq_acc, a.dq, a.N, a.Npad,
+                                                                                     vec);
   if (a.chunks > 1) {
     const long long n8 = static_cast<long long>(a.BHkv) * a.N * HD / 8;
     bwd_kv_sum_kernel<<<static_cast<unsigned>((2 * n8 + 255) / 256), 256, 0, stream>>>(a.kv_part, a.dk, a.dv,
@@ -810,8 +794,14 @@ cudaError_t launch_bwd_pre(const BwdLaunch& a, cudaStream_t stream) {
 
 cudaError_t launch_bwd_main(const BwdLaunch& a, cudaStream_t stream) {
   switch (a.d) {
-    case 64: return a.causal ? launch_main_t<64, true>(a, stream) : launch_main_t<64, false>(a, stream);
-    case 128: return a.causal ? launch_main_t<128, true>(a, stream) : launch_main_t<128, false>(a, stream);
+    case 64:
+      if (a.deterministic)
+        return a.causal ? launch_main_t<64, true, false>(a, stream) : launch_main_t<64, false, false>(a, stream);
+      return a.causal ? launch_main_t<64, true, true>(a, stream) : launch_main_t<64, false, true>(a, stream);
+    case 128:
+      if (a.deterministic)
+        return a.causal ? launch_main_t<128, true, false>(a, stream) : launch_main_t<128, false, false>(a, stream);
+      return a.causal ? launch_main_t<128, true, true>(a, stream) : launch_main_t<128, false, true>(a, stream);
     case 256: return launch_bwd_main_d256(a, stream);
     default: return cudaErrorNotSupported;
   }

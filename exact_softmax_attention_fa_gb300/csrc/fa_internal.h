@@ -49,7 +49,8 @@ struct BwdLaunch {
   float* D;       // [BH][Npad]
   float* lse2;    // [BH][Npad], base-2 logsumexp (+inf on padding rows)
   float* dq_acc;  // [BH][Npad][d]
-  uint32_t* sched;  // [2]: next work item to hand out, CTAs done claiming
+  uint32_t* sched;  // [4]: main kernel's next work item and CTAs done claiming; the same for the dQ kernel
+  int deterministic; // 1: dQ from the separate dQ kernel (no atomics); the main kernel skips it
   uint32_t* status;
   int N, Npad, BH, d, causal;
   int BHkv, group;   // K/V heads (B * H_kv) and query heads per K/V head
@@ -68,6 +69,7 @@ cudaError_t launch_bwd_pre(const BwdLaunch& a, cudaStream_t stream);   // D, bas
 cudaError_t launch_bwd_main(const BwdLaunch& a, cudaStream_t stream);  // dK, dV; dQ into the accumulator
 cudaError_t launch_bwd_post(const BwdLaunch& a, cudaStream_t stream);  // dQ = bf16(accumulator)
 cudaError_t launch_bwd_main_d256(const BwdLaunch& a, cudaStream_t stream);  // fa_bwd256.cu
+cudaError_t launch_bwd_dq(const BwdLaunch& a, cudaStream_t stream);  // fa_bwd_dq.cu: dq without atomics
 cudaError_t launch_timeout_probe(uint32_t* status, uint64_t limit_ns, cudaStream_t stream);
 
 }  // namespace fa

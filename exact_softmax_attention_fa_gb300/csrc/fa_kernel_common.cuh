@@ -5,6 +5,7 @@
 #include <cstdint>
 
 #include "fa.h"
+#include "sm103_ptx.cuh"
 
 namespace fa {
 
@@ -29,5 +30,46 @@ __device__ __forceinline__ void red_add_f32(float* addr, float a) {
 }
 
 __device__ __forceinline__ float4 ldg_f4(const float* p) { return __ldg(reinterpret_cast<const float4*>(p)); }
+
+// ---------------------------------------------------------------------------
+// Work-item queue of a persistent kernel. CTA b starts on item b; afterwards
+// its producer thread claims item G + atomicAdd(ctr[0], 1) and publishes it
+// through kItemSlots smem slots (item_ring, item_full, item_empty of the
+// kernel's shared struct) to the CTA's consumer threads. An item >= the item
+// count ends every role's loop. ctr[1] counts CTAs done claiming; the last
+// one resets both words for the next launch.
+// ---------------------------------------------------------------------------
+constexpr int kItemSlots = 4;
+
+template <class Shared>
+__device__ __forceinline__ bool publish_item(Shared& sh, int u, int item, uint64_t lim) {
+  const int s = u % kItemSlots;
+  if (u >= kItemSlots && !mbar_wait(&sh.item_empty[s], ((u / kItemSlots) - 1) & 1, &sh.abort_flag, lim))
+    return false;
+  *reinterpret_cast<volatile int*>(&sh.item_ring[s]) = item;
+  mbar_arrive(&sh.item_full[s]);
+  return true;
+}
+
+// The u-th item of this CTA, or -1 if the wait timed out.
+template <class Shared>
+__device__ __forceinline__ int take_item(Shared& sh, int u, uint64_t lim) {
+  const int s = u % kItemSlots;
+  if (!mbar_wait(&sh.item_full[s], (u / kItemSlots) & 1, &sh.abort_flag, lim)) return -1;
+  const int item = *reinterpret_cast<volatile int*>(&sh.item_ring[s]);
+  mbar_arrive(&sh.item_empty[s]);
+  return item;
+}
+
+__device__ __forceinline__ int claim_item(uint32_t* ctr) {
+  return static_cast<int>(gridDim.x) + static_cast<int>(atomicAdd(ctr, 1u));
+}
+
+__device__ __forceinline__ void finish_claiming(uint32_t* ctr) {
+  if (atomicAdd(ctr + 1, 1u) == gridDim.x - 1) {
+    atomicExch(ctr, 0u);
+    atomicExch(ctr + 1, 0u);
+  }
+}
 
 }  // namespace fa

@@ -128,6 +128,26 @@ fa_status_t fa_bwd(const void* q, const void* k, const void* v, const void* o, c
  */
 size_t fa_bwd_gqa_workspace_size(int B, int Hq, int Hkv, int N, int d);
 
+/*
+ * Deterministic backward: the same results as fa_bwd / fa_bwd_gqa, but dq is
+ * bitwise reproducible too. The pages accumulate dQ_i += dS K_j across key
+ * blocks with atomic adds (reading note 5.3-5.4; paper-graph-ui summary, "The
+ * Backward Pass"), whose order varies run to run. Here a separate kernel owns
+ * each 128-row query tile, recomputes S, P, dP and dS for every key tile it
+ * sees and sums dQ_i on chip in key order; the main kernel then computes only
+ * dK and dV. Costs three more 128x128xd products per (query tile, key tile)
+ * pair than the atomic version.
+ *   Arguments, layouts and workspace as for fa_bwd / fa_bwd_gqa.
+ *   d must be 64 or 128 (d = 256: FA_ERR_UNSUPPORTED).
+ */
+fa_status_t fa_bwd_deterministic(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                                 const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal,
+                                 float scale, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+fa_status_t fa_bwd_gqa_deterministic(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                                     const void* dO, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N,
+                                     int d, int causal, float scale, void* workspace, size_t workspace_bytes,
+                                     cudaStream_t stream);
+
 fa_status_t fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const float* lse,
                        const void* dO, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N, int d,
                        int causal, float scale, void* workspace, size_t workspace_bytes, cudaStream_t stream);

@@ -90,6 +90,18 @@ def test_grouped_workspace_size(lib):
     assert lib.fa_bwd_gqa_workspace_size(1, 4, 0, 128, 64) == 0
 
 
+def test_deterministic_backward_checks(lib):
+    def det(d=64, Hq=4, Hkv=2, ws=P, ws_bytes=1 << 30, ptr=P):
+        return lib.fa_bwd_gqa_deterministic(ptr, ptr, ptr, ptr, P, ptr, ptr, ptr, ptr, 1, Hq, Hkv, 128, d, 0, 0.125,
+                                            ws, ws_bytes, None)
+    assert det(d=256) == UNSUPPORTED
+    assert det(d=96) == UNSUPPORTED
+    assert det(Hkv=3) == INVALID
+    assert det(ptr=0) == INVALID
+    assert det(ws=0) == WORKSPACE
+    assert lib.fa_bwd_deterministic(P, P, P, P, P, P, P, P, P, 1, 1, 128, 256, 0, 0.125, P, 1 << 30, None) == UNSUPPORTED
+
+
 def test_grouped_heads_other_checks(lib):
     assert fwd_gqa(lib, d=96) == UNSUPPORTED
     assert bwd_gqa(lib, scale=0.0) == INVALID

@@ -1,0 +1,100 @@
+"""GPU parity and bitwise reproducibility of the deterministic backward
+(fa_bwd_deterministic, fa_bwd_gqa_deterministic): dQ summed on chip per query
+tile in key order instead of with atomic adds."""
+
+import numpy as np
+import pytest
+
+import oracle
+from attn_inputs import BASE_SEED
+from gpu_util import TOL_GRAD_REL, inputs, scale_f32, to_device, to_host64
+
+pytestmark = pytest.mark.gpu
+
+
+def rel_err(got, ref):
+    return np.abs(got - ref).max() / max(np.abs(ref).max(), 1e-3)
+
+
+def grouped_inputs(B, Hq, Hkv, N, d, seed):
+    xq, fq = inputs(B, Hq, N, d, seed, tensors=("q", "do"))
+    xk, fk = inputs(B, Hkv, N, d, seed + 1, tensors=("k", "v"))
+    return {**xq, **xk}, {**fq, **fk}
+
+
+def run(x, causal, scale, deterministic=True):
+    import exact_softmax_attention_fa_gb300 as fa
+    q, k, v, do = (to_device(x[n]) for n in ("q", "k", "v", "do"))
+    o, lse = fa.forward(q, k, v, causal=causal, scale=scale)
+    grads = fa.backward(q, k, v, o, lse, do, causal=causal, scale=scale, deterministic=deterministic)
+    assert fa.fa_get_device_status() == 0
+    return grads
+
+
+def check(x, f, causal, d):
+    scale = scale_f32(d)
+    grads = run(x, causal, scale)
+    ref = oracle.attention_backward(f["q"], f["k"], f["v"], f["do"], causal, scale)
+    for name, g, r in zip(("dq", "dk", "dv"), grads, ref):
+        e = rel_err(to_host64(g), r)
+        assert e <= TOL_GRAD_REL, (name, e)
+    return grads
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [1, 65, 128, 129, 300, 1000])
+def test_deterministic_parity(d, causal, N):
+    x, f = inputs(2, 3, N, d, BASE_SEED + 600 + N)
+    check(x, f, causal, d)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Hq,Hkv", [(4, 2), (6, 1)])
+def test_deterministic_grouped_parity(d, causal, Hq, Hkv):
+    x, f = grouped_inputs(2, Hq, Hkv, 333, d, BASE_SEED + 650 + Hq)
+    check(x, f, causal, d)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bitwise_reproducible(d, causal):
+    import torch
+    x, _ = inputs(2, 4, 1500, d, BASE_SEED + 700)
+    a = run(x, causal, scale_f32(d))
+    b = run(x, causal, scale_f32(d))
+    for t1, t2 in zip(a, b):
+        assert torch.equal(t1, t2)
+
+
+def test_matches_atomic_backward():
+    x, _ = inputs(1, 4, 777, 128, BASE_SEED + 710)
+    det = run(x, True, scale_f32(128))
+    atomic = run(x, True, scale_f32(128), deterministic=False)
+    for a, b in zip(det, atomic):
+        assert rel_err(to_host64(a), to_host64(b)) <= 1e-2
+
+
+def test_several_thousand_rows_sampled_heads():
+    # the oracle computes only the sampled heads: compare those of every gradient
+    x, f = inputs(1, 4, 4096, 128, BASE_SEED + 720)
+    scale = scale_f32(128)
+    heads = [(0, 0), (0, 3)]
+    grads = run(x, True, scale)
+    ref = oracle.attention_backward(f["q"], f["k"], f["v"], f["do"], True, scale, heads=heads)
+    for name, g, r in zip(("dq", "dk", "dv"), grads, ref):
+        got = np.stack([to_host64(g)[b, h] for b, h in heads])
+        want = np.stack([r[b, h] for b, h in heads])
+        assert rel_err(got, want) <= TOL_GRAD_REL, name
+
+
+def test_head_dim_256_is_unsupported():
+    import exact_softmax_attention_fa_gb300 as fa
+    import torch
+    x, _ = inputs(1, 1, 64, 256, BASE_SEED + 730)
+    q, k, v, do = (to_device(x[n]) for n in ("q", "k", "v", "do"))
+    o, lse = fa.forward(q, k, v, causal=False)
+    with pytest.raises(fa.FAError):
+        fa.backward(q, k, v, o, lse, do, deterministic=True)
+    assert fa.fa_get_device_status() == 0
