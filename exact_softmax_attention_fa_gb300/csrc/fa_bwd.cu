@@ -119,8 +119,18 @@ struct BwdWork {
     nq = T - i0;
   }
   __device__ int n_iter() const { return gs * nq; }
-  __device__ int qbh(int n) const { return q0 + n / nq; }  // query head of step n
-  __device__ int qi(int n) const { return i0 + n % nq; }   // query tile of step n
+  // (query head, query tile) of a step of the query stream, advanced in order
+  // (no per-step division on the softmax warps' path)
+  struct Pos {
+    int bh, i;
+  };
+  __device__ Pos first() const { return Pos{q0, i0}; }
+  __device__ void advance(Pos& p) const {
+    if (++p.i == T) {
+      p.i = i0;
+      ++p.bh;
+    }
+  }
 };
 
 // Dynamic schedule (fa_kernel_common.cuh): items are claimed from sched[0..1]
@@ -274,7 +284,8 @@ __device__ void bwd_load_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sK, ui
     if (item >= total) break;
     const BwdWork<CAUSAL> wk(item, p.BHkv, p.N, p.group, p.chunks);
     const int n_iter = wk.n_iter();
-    if (!load_qdo(g, wk.qi(0), wk.qbh(0))) {
+    typename BwdWork<CAUSAL>::Pos pos = wk.first();
+    if (!load_qdo(g, pos.i, pos.bh)) {
       aborted = true;
       break;
     }
@@ -290,7 +301,8 @@ __device__ void bwd_load_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sK, ui
     }
     ++kv_issued;
     for (int n = 1; n < n_iter; ++n) {
-      if (!load_qdo(g + n, wk.qi(n), wk.qbh(n))) {
+      wk.advance(pos);
+      if (!load_qdo(g + n, pos.i, pos.bh)) {
         aborted = true;
         break;
       }
@@ -600,20 +612,18 @@ __device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS
     const int key = wk.j * 128 + r;
     const uint32_t t = tmem + lane_base + (w == 0 ? C::DK_COL : C::DV_COL);
     const size_t row = static_cast<size_t>(wk.bh) * p.N + key;
-    __nv_bfloat16* dst = (w == 0 ? p.dk : p.dv) + row * HD;
-    const size_t part_len = static_cast<size_t>(p.chunks) * p.BHkv * p.N * HD;
-    float* part = p.kv_part + (w == 0 ? 0 : part_len) + (static_cast<size_t>(wk.c) * p.BHkv * p.N + row) * HD;
+    if (p.chunks == 1) {
+      __nv_bfloat16* dst = (w == 0 ? p.dk : p.dv) + row * HD;
 #pragma unroll 1
-    for (int c = 0; c < HD; c += 32) {
-      uint32_t v[32];
-      tmem_ld32(t + c, v);
-      tmem_ld_wait();
-      if (c + 32 == HD) {  // both accumulators read: the next item may overwrite them
-        tc_fence_before_sync();
-        mbar_arrive(&sh.acc_free);
-      }
-      if (key < p.N) {
-        if (p.chunks == 1) {
+      for (int c = 0; c < HD; c += 32) {
+        uint32_t v[32];
+        tmem_ld32(t + c, v);
+        tmem_ld_wait();
+        if (c + 32 == HD) {  // both accumulators read: the next item may overwrite them
+          tc_fence_before_sync();
+          mbar_arrive(&sh.acc_free);
+        }
+        if (key < p.N) {
 #pragma unroll
           for (int u = 0; u < 4; ++u)
             *reinterpret_cast<uint4*>(dst + c + 8 * u) =
@@ -621,7 +631,21 @@ __device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS
                            pack_bf16x2(__uint_as_float(v[8 * u + 2]), __uint_as_float(v[8 * u + 3])),
                            pack_bf16x2(__uint_as_float(v[8 * u + 4]), __uint_as_float(v[8 * u + 5])),
                            pack_bf16x2(__uint_as_float(v[8 * u + 6]), __uint_as_float(v[8 * u + 7])));
-        } else {
+        }
+      }
+    } else {
+      const size_t part_len = static_cast<size_t>(p.chunks) * p.BHkv * p.N * HD;
+      float* part = p.kv_part + (w == 0 ? 0 : part_len) + (static_cast<size_t>(wk.c) * p.BHkv * p.N + row) * HD;
+#pragma unroll 1
+      for (int c = 0; c < HD; c += 32) {
+        uint32_t v[32];
+        tmem_ld32(t + c, v);
+        tmem_ld_wait();
+        if (c + 32 == HD) {
+          tc_fence_before_sync();
+          mbar_arrive(&sh.acc_free);
+        }
+        if (key < p.N) {
 #pragma unroll
           for (int u = 0; u < 8; ++u)
             *reinterpret_cast<uint4*>(part + c + 4 * u) = make_uint4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
@@ -629,6 +653,7 @@ __device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS
       }
     }
   };
+
 
   // The next work item, agreed on by the whole warpgroup: a warp whose wait
   // timed out makes every warp of the group leave the loop at the same point.
@@ -647,7 +672,7 @@ __device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS
   float ld = 0.f;
   if (item < total) {
     const BwdWork<CAUSAL> wk0(item, p.BHkv, p.N, p.group, p.chunks);
-    ld = fetch_ld(wk0.qbh(0), wk0.qi(0));
+    ld = fetch_ld(wk0.q0, wk0.i0);
   }
   while (item < total) {
     const BwdWork<CAUSAL> wk(item, p.BHkv, p.N, p.group, p.chunks);
@@ -655,23 +680,27 @@ __device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS
     if (items > 0) named_barrier_sync(bar_id, 128);  // the previous item's L2 / D reads are done
     sLD[w * 128 + r] = ld;
     named_barrier_sync(bar_id, 128);
-    phase_a(wk, wk.qi(0), g);
+    typename BwdWork<CAUSAL>::Pos cur = wk.first();
+    phase_a(wk, cur.i, g);
     for (int n = 0; n < n_iter; ++n) {
       const bool has_next = n + 1 < n_iter;
-      const float next_ld = has_next ? fetch_ld(wk.qbh(n + 1), wk.qi(n + 1)) : 0.f;  // lands during phase B
+      typename BwdWork<CAUSAL>::Pos nxt = cur;
+      wk.advance(nxt);
+      const float next_ld = has_next ? fetch_ld(nxt.bh, nxt.i) : 0.f;  // lands during phase B
       phase_b(g + n);
       if (has_next) {
         named_barrier_sync(bar_id, 128);  // every thread is done reading this tile's L2 / D
         sLD[w * 128 + r] = next_ld;
         named_barrier_sync(bar_id, 128);
-        phase_a(wk, wk.qi(n + 1), g + n + 1);
+        phase_a(wk, nxt.i, g + n + 1);
       }
-      if constexpr (DQ) drain(wk.qbh(n), wk.qi(n), g + n);
+      if constexpr (DQ) drain(cur.bh, cur.i, g + n);
+      cur = nxt;
     }
     const int item_next = next_item(items + 1);
     if (item_next < total) {
       const BwdWork<CAUSAL> wk1(item_next, p.BHkv, p.N, p.group, p.chunks);
-      ld = fetch_ld(wk1.qbh(0), wk1.qi(0));  // lands during the epilogue
+      ld = fetch_ld(wk1.q0, wk1.i0);  // lands during the epilogue
     }
     epilogue(wk, items);
     g += n_iter;

@@ -78,8 +78,17 @@ struct Work256 {
     g = group;
   }
   __device__ int n_iter() const { return g * nq; }
-  __device__ int qbh(int n) const { return bh * g + n / nq; }  // query head of step n
-  __device__ int qi(int n) const { return i0 + n % nq; }       // 64-row query tile of step n
+  // (query head, 64-row query tile) of a step, advanced in order
+  struct Pos {
+    int bh, i;
+  };
+  __device__ Pos first() const { return Pos{bh * g, i0}; }
+  __device__ void advance(Pos& p) const {
+    if (++p.i == T64) {
+      p.i = i0;
+      ++p.bh;
+    }
+  }
 };
 
 template <bool CAUSAL>
@@ -100,8 +109,9 @@ __device__ void load_role(const BwdLaunch& p, Shared256& sh, uint8_t* sK, uint8_
   const int n_iter = wk.n_iter();
   int q_issued = 0, do_issued = 0;
   bool aborted = false;
-  for (int n = 0; n < n_iter && !aborted; ++n) {
-    const int i = wk.qi(n), qbh = wk.qbh(n);
+  typename Work256<CAUSAL>::Pos pos = wk.first();
+  for (int n = 0; n < n_iter && !aborted; ++n, wk.advance(pos)) {
+    const int i = pos.i, qbh = pos.bh;
     if (n > 0 && !mbar_wait(&sh.q_empty, (n - 1) & 1, &sh.abort_flag, p.wait_limit_ns)) {
       aborted = true;
       break;
@@ -211,23 +221,26 @@ __device__ void softmax_role(const BwdLaunch& p, Shared256& sh, uint8_t* sDS, fl
   const uint32_t bar_id = 1 + w;
   bool alive = true;
 
-  // thread r < 32 holds L2 of query 32w + r of step n's tile, 32 <= r < 64 its scaled D
-  auto fetch_ld = [&](int n) -> float {
-    const size_t row = static_cast<size_t>(wk.qbh(n)) * p.Npad + wk.qi(n) * C::BQ + 32 * w;
+  // thread r < 32 holds L2 of query 32w + r of a step's tile, 32 <= r < 64 its scaled D
+  auto fetch_ld = [&](const typename Work256<CAUSAL>::Pos& q) -> float {
+    const size_t row = static_cast<size_t>(q.bh) * p.Npad + q.i * C::BQ + 32 * w;
     if (r < 32) return __ldg(p.lse2 + row + r);
     if (r < 64) return __ldg(p.D + row + (r - 32)) * sc;
     return 0.f;
   };
+  typename Work256<CAUSAL>::Pos cur = wk.first();
   {
-    const float v = fetch_ld(0);
+    const float v = fetch_ld(cur);
     if (r < 64) sLD[w * 64 + r] = v;
     named_barrier_sync(bar_id, 128);
   }
 
   for (int n = 0; n < n_iter; ++n) {
-    const int i = wk.qi(n);
+    const int i = cur.i;
     const bool has_next = n + 1 < n_iter;
-    const float next_ld = has_next ? fetch_ld(n + 1) : 0.f;
+    typename Work256<CAUSAL>::Pos nxt = cur;
+    wk.advance(nxt);
+    const float next_ld = has_next ? fetch_ld(nxt) : 0.f;
     const uint32_t tS = tmem + lane_base + C::REG_S + 32 * w;
     const uint32_t tDP = tmem + lane_base + C::REG_DP + 32 * w;
     // ---- phase A: P^T for this warpgroup's 32 queries, bf16 back into TMEM
@@ -298,7 +311,7 @@ __device__ void softmax_role(const BwdLaunch& p, Shared256& sh, uint8_t* sDS, fl
       tmem_ld_wait();
       tc_fence_before_sync();
       mbar_arrive(&sh.dq_free);
-      float* dst = p.dq_acc + (static_cast<size_t>(wk.qbh(n)) * p.Npad + i * C::BQ + 32 * w) * C::HD + 128 * wk.h + r;
+      float* dst = p.dq_acc + (static_cast<size_t>(cur.bh) * p.Npad + i * C::BQ + 32 * w) * C::HD + 128 * wk.h + r;
 #pragma unroll
       for (int c = 0; c < 32; ++c) red_add_f32(dst + static_cast<size_t>(c) * C::HD, __uint_as_float(v[c]));
     }
@@ -307,6 +320,7 @@ __device__ void softmax_role(const BwdLaunch& p, Shared256& sh, uint8_t* sDS, fl
       if (r < 64) sLD[w * 64 + r] = next_ld;
       named_barrier_sync(bar_id, 128);
     }
+    cur = nxt;
   }
 }
 
