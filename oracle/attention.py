@@ -47,8 +47,11 @@ variants agree to 1e-12; torch's float64 CPU attention plus autograd agrees to
 1e-12; central finite differences match the gradients. Grouped K/V heads:
 torch's float64 attention with enable_gqa plus autograd agrees; K/V repeated
 along the head axis give the same O, L, dQ and, summed over each group, dK and
-dV; the tiled variants and finite differences agree. Every function here is
-pinned by at least one of these.
+dV; the tiled variants and finite differences agree. Shorter query blocks
+(N_q < N_k, causal mask aligned to the last key): a single causal query equals
+the unmasked one; the block equals the last N_q rows of the square causal
+problem; torch's float64 attention with the explicit last-key-aligned mask
+agrees. Every function here is pinned by at least one of these.
 """
 
 from __future__ import annotations
@@ -59,12 +62,12 @@ _ROW_CHUNK = 256
 
 
 def _check(q, k, v=None):
-    """Promote to float64 and return (q, k, v, g): q is [B, H_q, N, d], k and v
-    are [B, H_kv, N, d] with H_q = g * H_kv ([note] §5.6)."""
+    """Promote to float64 and return (q, k, v, g): q is [B, H_q, N_q, d], k and v
+    are [B, H_kv, N_k, d] with H_q = g * H_kv ([note] §5.6)."""
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
-    if q.ndim != 4 or k.ndim != 4 or k.shape[0] != q.shape[0] or k.shape[2:] != q.shape[2:]:
-        raise ValueError("q must be [B, H_q, N, d] and k [B, H_kv, N, d]")
+    if q.ndim != 4 or k.ndim != 4 or k.shape[0] != q.shape[0] or k.shape[3] != q.shape[3]:
+        raise ValueError("q must be [B, H_q, N_q, d] and k [B, H_kv, N_k, d]")
     if k.shape[1] < 1 or q.shape[1] % k.shape[1] != 0:
         raise ValueError("H_q must be a multiple of H_kv")
     if v is not None:
@@ -80,12 +83,22 @@ def _kv_head(h, g):
 
 
 def _scores(q_rows, k, row_ids, causal, scale):
-    """S for the given query rows of one head: scale * q k^T, future keys -> -inf."""
+    """S for the given query rows of one head: scale * q k^T, future keys -> -inf.
+
+    row_ids are the rows' positions on the key axis: query i of N_q sits at
+    i + N_k - N_q, so a shorter query block is the last rows of the square
+    causal problem (the mask aligned to the last key).
+    """
     s = scale * (q_rows @ k.T)
     if causal:
         cols = np.arange(k.shape[0])
         s = np.where(cols[None, :] > row_ids[:, None], -np.inf, s)
     return s
+
+
+def _key_pos(rows, nq, nk):
+    """Positions on the key axis of query rows of an N_q-row block against N_k keys."""
+    return rows + (nk - nq)
 
 
 def softmax_rows(s):
@@ -102,8 +115,9 @@ def attention_probabilities(q, k, causal, scale):
     """The full P = softmax(S) as a [B, H, N, N] array (small inputs only)."""
     q, k, _, g = _check(q, k)
     B, H, N, _d = q.shape
-    out = np.zeros((B, H, N, N))
-    rows = np.arange(N)
+    Nk = k.shape[2]
+    out = np.zeros((B, H, N, Nk))
+    rows = _key_pos(np.arange(N), N, Nk)
     for b in range(B):
         for h in range(H):
             out[b, h], _ = softmax_rows(_scores(q[b, h], k[b, _kv_head(h, g)], rows, causal, scale))
@@ -111,7 +125,11 @@ def attention_probabilities(q, k, causal, scale):
 
 
 def attention_forward(q, k, v, causal, scale):
-    """O = softmax(S) V and L = logsumexp(S) per row; returns (O [B,H,N,d], L [B,H,N])."""
+    """O = softmax(S) V and L = logsumexp(S) per row; returns (O [B,H,N_q,d], L [B,H,N_q]).
+
+    K and V may hold N_k != N_q keys; under a causal mask query i then sees
+    keys j <= i + N_k - N_q.
+    """
     q, k, v, g = _check(q, k, v)
     B, H, N, d = q.shape
     o = np.zeros((B, H, N, d))
@@ -121,7 +139,8 @@ def attention_forward(q, k, v, causal, scale):
             hk = _kv_head(h, g)
             for r0 in range(0, N, _ROW_CHUNK):
                 rows = np.arange(r0, min(N, r0 + _ROW_CHUNK))
-                p, l_rows = softmax_rows(_scores(q[b, h, rows], k[b, hk], rows, causal, scale))
+                p, l_rows = softmax_rows(_scores(q[b, h, rows], k[b, hk], _key_pos(rows, N, k.shape[2]), causal,
+                                                 scale))
                 o[b, h, rows] = p @ v[b, hk]
                 lse[b, h, rows] = l_rows
     return o, lse
@@ -164,7 +183,7 @@ def attention_backward(q, k, v, do, causal, scale, heads=None):
         hk = _kv_head(h, g)
         for r0 in range(0, N, _ROW_CHUNK):
             rows = np.arange(r0, min(N, r0 + _ROW_CHUNK))
-            p, _ = softmax_rows(_scores(q[b, h, rows], k[b, hk], rows, causal, scale))
+            p, _ = softmax_rows(_scores(q[b, h, rows], k[b, hk], _key_pos(rows, N, k.shape[2]), causal, scale))
             do_rows = do[b, h, rows]
             dv[b, hk] += p.T @ do_rows
             dp = do_rows @ v[b, hk].T
@@ -208,6 +227,8 @@ def tiled_forward(q, k, v, causal, scale, block_rows, block_cols):
     """
     q, k, v, g = _check(q, k, v)
     B, H, N, d = q.shape
+    if k.shape[2] != N:
+        raise ValueError("the blocked variants take N_q = N_k")
     o = np.zeros((B, H, N, d))
     lse = np.zeros((B, H, N))
     for b in range(B):
@@ -253,6 +274,8 @@ def tiled_backward(q, k, v, o, lse, do, causal, scale, block_rows, block_cols):
     do = np.asarray(do, dtype=np.float64)
     lse = np.asarray(lse, dtype=np.float64)
     B, H, N, d = q.shape
+    if k.shape[2] != N:
+        raise ValueError("the blocked variants take N_q = N_k")
     dq = np.zeros_like(q)
     dk = np.zeros_like(k)
     dv = np.zeros_like(k)

@@ -381,3 +381,39 @@ def test_planted_wrong_group_mapping_is_caught(monkeypatch):
     monkeypatch.setattr(oa, "_kv_head", lambda h, g: h % Hkv)
     o_bad, _ = oracle.attention_forward(q, k, v, False, 0.5)
     assert not np.allclose(o_bad, o_r, atol=1e-6)
+
+
+# ---- query blocks shorter than the key sequence (decoding against a cache) ---
+
+def test_single_causal_query_sees_every_key():
+    # with the mask aligned to the last key, one query is the newest position
+    q = rand((2, 3, 1, 8), 100)
+    k, v = rand((2, 3, 37, 8), 101), rand((2, 3, 37, 8), 102)
+    oc, lc = oracle.attention_forward(q, k, v, True, 0.4)
+    on, ln = oracle.attention_forward(q, k, v, False, 0.4)
+    np.testing.assert_allclose(oc, on, rtol=0, atol=1e-15)
+    np.testing.assert_allclose(lc, ln, rtol=0, atol=1e-15)
+
+
+@pytest.mark.parametrize("nq", [1, 5, 16, 29])
+def test_short_causal_block_is_tail_of_square_problem(nq):
+    nk = 29
+    q, k, v = qkv(1, 2, nk, 6, 110)
+    o_full, l_full = oracle.attention_forward(q, k, v, True, 0.6)
+    o, l = oracle.attention_forward(q[:, :, nk - nq:], k, v, True, 0.6)
+    np.testing.assert_allclose(o, o_full[:, :, nk - nq:], rtol=0, atol=1e-14)
+    np.testing.assert_allclose(l, l_full[:, :, nk - nq:], rtol=0, atol=1e-14)
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(2, 2), (4, 1)])
+def test_short_block_torch_sdpa_with_last_key_mask(Hq, Hkv):
+    torch = pytest.importorskip("torch")
+    nq, nk = 7, 40
+    q = rand((2, Hq, nq, 8), 120)
+    k, v = rand((2, Hkv, nk, 8), 121), rand((2, Hkv, nk, 8), 122)
+    mask = torch.ones(nq, nk, dtype=torch.bool).tril(diagonal=nk - nq)
+    tq, tk, tv = (torch.tensor(x, dtype=torch.float64) for x in (q, k, v))
+    to = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, attn_mask=mask, scale=0.3,
+                                                          enable_gqa=Hq != Hkv)
+    o, _ = oracle.attention_forward(q, k, v, True, 0.3)
+    np.testing.assert_allclose(o, to.numpy(), rtol=0, atol=1e-12)
