@@ -15,7 +15,7 @@ import math
 
 from ._lib import load, check, FAError, header_functions, STATUS_NAMES  # noqa: F401
 
-__all__ = ["fa_fwd", "fa_bwd", "fa_fwd_gqa", "fa_bwd_gqa", "fa_bwd_deterministic", "fa_bwd_gqa_deterministic", "fa_bwd_workspace_size", "fa_bwd_gqa_workspace_size", "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_postprocess", "fa_bwd_noalloc", "fa_get_device_status", "fa_set_wait_limit_ns",
+__all__ = ["fa_fwd", "fa_bwd", "fa_fwd_gqa", "fa_bwd_gqa", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_size", "fa_bwd_deterministic", "fa_bwd_gqa_deterministic", "fa_bwd_workspace_size", "fa_bwd_gqa_workspace_size", "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_postprocess", "fa_bwd_noalloc", "fa_get_device_status", "fa_set_wait_limit_ns",
            "fa_debug_timeout_probe", "forward", "backward", "FAError", "flops"]
 
 _SUPPORTED_D = (64, 128, 256)
@@ -107,6 +107,32 @@ def fa_bwd_gqa(q, k, v, o, lse, do, dq, dk, dv, causal: bool, scale: float, work
                                        do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
                                        B, Hq, Hkv, N, d, int(bool(causal)), float(scale), *_ws(workspace),
                                        _stream_handle(stream)))
+
+
+def fa_fwd_splitkv_workspace_size(B: int, Hq: int, Nq: int, d: int, num_splits: int) -> int:
+    return int(load().fa_fwd_splitkv_workspace_size(B, Hq, Nq, d, num_splits))
+
+
+def fa_fwd_splitkv(q, k, v, o, lse, causal: bool, scale: float, num_splits: int = 0, workspace=None,
+                   stream=None) -> None:
+    """fa_fwd_splitkv of the C ABI: q, o [B, Hq, Nq, d]; k, v [B, Hkv, Nk, d]; lse [B, Hq, Nq].
+
+    Causal masks align to the last key (query i sees keys j <= i + Nk - Nq).
+    num_splits = 0 lets the library choose within `workspace` (a CUDA uint8
+    tensor, or None for no split).
+    """
+    B, Hq, Nq, d = _dims(q)
+    if k.dim() != 4 or k.shape[0] != B or k.shape[3] != d:
+        raise ValueError("k must be [B, Hkv, Nk, d] with q's B and d")
+    Hkv, Nk = int(k.shape[1]), int(k.shape[2])
+    for name, t, shape in (("q", q, (B, Hq, Nq, d)), ("k", k, (B, Hkv, Nk, d)), ("v", v, (B, Hkv, Nk, d)),
+                           ("o", o, (B, Hq, Nq, d))):
+        _check_bf16(name, t, shape)
+    _check_lse(lse, (B, Hq, Nq, d))
+    check("fa_fwd_splitkv", load().fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                                  lse.data_ptr(), B, Hq, Hkv, Nq, Nk, d, int(bool(causal)),
+                                                  float(scale), int(num_splits), *_ws(workspace),
+                                                  _stream_handle(stream)))
 
 
 def fa_bwd_deterministic(q, k, v, o, lse, do, dq, dk, dv, causal: bool, scale: float, workspace, stream=None) -> None:

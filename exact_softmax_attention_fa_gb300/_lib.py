@@ -31,6 +31,9 @@ _c_int, _c_float, _vp = ctypes.c_int, ctypes.c_float, ctypes.c_void_p
 _SIGNATURES = {
     "fa_fwd": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_float, _vp]),
     "fa_fwd_gqa": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_float, _vp]),
+    "fa_fwd_splitkv": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                _c_float, _c_int, _vp, ctypes.c_size_t, _vp]),
+    "fa_fwd_splitkv_workspace_size": (ctypes.c_size_t, [_c_int, _c_int, _c_int, _c_int, _c_int]),
     "fa_bwd_workspace_size": (ctypes.c_size_t, [_c_int, _c_int, _c_int, _c_int]),
     "fa_bwd_deterministic": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
                                       _c_int, _c_float, _vp, ctypes.c_size_t, _vp]),

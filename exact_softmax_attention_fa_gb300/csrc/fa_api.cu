@@ -171,6 +171,29 @@ BwdWorkspaceLayout bwd_layout(long long BH, int N, int d) {
   return w;
 }
 
+// Key ranges of the split-key forward: fp32 O and L partials per range.
+constexpr int kMaxSplits = 256;
+
+size_t splitkv_bytes(long long BH, int Nq, int d, int splits) {
+  return align_up(static_cast<size_t>(splits) * BH * Nq * d * 4, 256) +
+         align_up(static_cast<size_t>(splits) * BH * Nq * 4, 256);
+}
+
+// Automatic number of key ranges: enough items for about two per SM when the
+// query tiles alone are too few (short query blocks such as decoding), at
+// least one key tile per range, and no more ranges than the workspace holds.
+int auto_splits(long long BH, int Nq, int Nk, int d, int sms, size_t room) {
+  const long long tq = (Nq + 127) / 128;
+  const long long nt = d <= 128 ? 2 : 1;  // query tiles per CTA
+  const long long items = BH * ((tq + nt - 1) / nt);
+  const int Tk = (Nk + 127) / 128;
+  if (items >= sms || Tk < 2) return 1;
+  long long want = (2LL * sms + items - 1) / items;
+  want = std::min<long long>(want, std::min(Tk, kMaxSplits));
+  while (want > 1 && splitkv_bytes(BH, Nq, d, static_cast<int>(want)) > room) --want;
+  return static_cast<int>(std::max<long long>(want, 1));
+}
+
 // fp32 partial dK + dV of one chunk of a group, for every K/V head.
 size_t kv_part_bytes(long long BHkv, int N, int d) { return static_cast<size_t>(BHkv) * N * d * 4 * 2; }
 
@@ -240,35 +263,78 @@ void fa_set_wait_limit_ns(unsigned long long limit_ns) {
   g_wait_limit_ns.store(limit_ns == 0 ? kDefaultWaitLimitNs : limit_ns);
 }
 
-fa_status_t fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
-                       int N, int d, int causal, float scale, cudaStream_t stream) {
-  bool empty = false;
-  fa_status_t st = check_common(B, Hq, N, d, causal, scale, &empty);
+fa_status_t fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                           int Nq, int Nk, int d, int causal, float scale, int num_splits, void* workspace,
+                           size_t workspace_bytes, cudaStream_t stream) {
+  bool empty = false, empty_k = false;
+  fa_status_t st = check_common(B, Hq, Nq, d, causal, scale, &empty);
+  if (st != FA_OK) return st;
+  st = check_common(B, Hkv, Nk, d, causal, scale, &empty_k);
   if (st != FA_OK) return st;
   st = check_heads(Hq, Hkv);
   if (st != FA_OK) return st;
+  if (num_splits < 0 || num_splits > kMaxSplits) return FA_ERR_INVALID_ARG;
   if (empty) return FA_OK;
+  // every query row must see at least one key
+  if (Nk == 0 || (causal && Nq > Nk)) return FA_ERR_INVALID_ARG;
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
     return FA_ERR_MISALIGNED;
+  const int BH = B * Hq, BHkv = B * Hkv;
+  const int Tk = (Nk + 127) / 128;
+  int splits = num_splits;
+  if (splits == 0) {
+    DeviceState* ds0 = device_state(&st);
+    if (!ds0) return st;
+    splits = auto_splits(BH, Nq, Nk, d, ds0->num_sms, workspace ? workspace_bytes : 0);
+  }
+  int per = (Tk + splits - 1) / splits;  // key tiles per range; no range is empty
+  splits = (Tk + per - 1) / per;
+  if (splits > 1) {
+    if (!workspace || workspace_bytes < splitkv_bytes(BH, Nq, d, splits)) return FA_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return FA_ERR_MISALIGNED;
+  }
   DeviceState* ds = device_state(&st);
   if (!ds) return st;
   FwdLaunch a{};
-  const int BH = B * Hq, BHkv = B * Hkv;
-  if (!make_map(&a.tmQ, q, BH, N, d) || !make_map(&a.tmK, k, BHkv, N, d) || !make_map(&a.tmV, v, BHkv, N, d) ||
-      !make_map(&a.tmO, o, BH, N, d))
+  if (!make_map(&a.tmQ, q, BH, Nq, d) || !make_map(&a.tmK, k, BHkv, Nk, d) || !make_map(&a.tmV, v, BHkv, Nk, d) ||
+      !make_map(&a.tmO, o, BH, Nq, d))
     return FA_ERR_CUDA;
   a.lse = lse;
+  a.o = static_cast<__nv_bfloat16*>(o);
   a.status = ds->status;
-  a.N = N;
+  a.Nq = Nq;
+  a.Nk = Nk;
+  a.causal_off = Nk - Nq;
   a.BH = BH;
   a.d = d;
   a.causal = causal;
   a.group = Hq / Hkv;
+  a.splits = splits;
+  a.kv_per_split = per;
+  if (splits > 1) {
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    a.o_part = reinterpret_cast<float*>(ws);
+    a.lse_part = reinterpret_cast<float*>(ws + align_up(static_cast<size_t>(splits) * BH * Nq * d * 4, 256));
+  }
   a.scale_log2 = static_cast<float>(static_cast<double>(scale) * kLog2e);
   a.wait_limit_ns = g_wait_limit_ns.load();
   a.num_sms = ds->num_sms;
-  return from_cuda(launch_fwd(a, stream));
+  cudaError_t e = launch_fwd(a, stream);
+  if (e == cudaSuccess && splits > 1) e = launch_fwd_combine(a, stream);
+  return from_cuda(e);
+}
+
+size_t fa_fwd_splitkv_workspace_size(int B, int Hq, int Nq, int d, int num_splits) {
+  bool empty = false;
+  if (check_common(B, Hq, Nq, d, 0, 1.0f, &empty) != FA_OK || empty || num_splits < 2 || num_splits > kMaxSplits)
+    return 0;
+  return splitkv_bytes(static_cast<long long>(B) * Hq, Nq, d, num_splits);
+}
+
+fa_status_t fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                       int N, int d, int causal, float scale, cudaStream_t stream) {
+  return fa_fwd_splitkv(q, k, v, o, lse, B, Hq, Hkv, N, N, d, causal, scale, 1, nullptr, 0, stream);
 }
 
 fa_status_t fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,

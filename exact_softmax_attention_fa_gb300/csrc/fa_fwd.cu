@@ -82,32 +82,49 @@ struct FwdShared {
   int abort_flag;
 };
 
-// Work item: NT consecutive 128-row query tiles of head `bh`. Items are
-// numbered longest-first under a causal mask (the last query tiles see the
-// most keys); non-causal items of one head are adjacent (K/V reuse in L2).
+// Work item: NT consecutive 128-row query tiles of head `bh` and key range s
+// (key tiles kv0 .. kv0 + kv_per_split - 1; one range covers every key unless
+// the keys are split). Items are numbered longest-first under a causal mask
+// (the last query tiles see the most keys); non-causal items of one head are
+// adjacent (K/V reuse in L2). Key-tile indices inside an item are relative to
+// kv0.
 template <int NT, bool CAUSAL>
 struct FwdWork {
-  int bh;
+  int bh, s, kv0;
   int qt[NT];       // query tile indices
-  int last_kv[NT];  // last key tile each query tile needs; -1 if the tile is past the end
+  int last_kv[NT];  // last key tile each query tile needs in this range; -1: none (or past the end)
   int nkv;          // number of key tiles streamed
-  __device__ FwdWork(int item, int BH, int N) {
-    const int T = (N + 127) / 128;
-    const int n_w = (T + NT - 1) / NT;
+  __device__ FwdWork(int item, const FwdLaunch& p) {
+    const int Tq = (p.Nq + 127) / 128;
+    const int Tk = (p.Nk + 127) / 128;
+    const int n_w = (Tq + NT - 1) / NT;
     int w;
     if (CAUSAL) {
-      bh = item % BH;
-      w = n_w - 1 - item / BH;
+      const int u = item % (p.BH * p.splits);
+      w = n_w - 1 - item / (p.BH * p.splits);
+      bh = u / p.splits;
+      s = u - bh * p.splits;
     } else {
-      bh = item / n_w;
-      w = item % n_w;
+      bh = item / (n_w * p.splits);
+      const int rem = item - bh * (n_w * p.splits);
+      w = rem / p.splits;
+      s = rem - w * p.splits;
     }
+    kv0 = s * p.kv_per_split;
+    const int kv_end = min(Tk, kv0 + p.kv_per_split) - 1;
     nkv = 0;
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
       qt[t] = w * NT + t;
-      last_kv[t] = qt[t] < T ? (CAUSAL ? qt[t] : T - 1) : -1;
-      nkv = max(nkv, last_kv[t] + 1);
+      int last = -1;
+      if (qt[t] < Tq) {
+        int lim = kv_end;
+        // causal: the tile's last row sees keys up to its index + causal_off
+        if (CAUSAL) lim = min(lim, (min(qt[t] * 128 + 127, p.Nq - 1) + p.causal_off) / 128);
+        last = max(lim - kv0, -1);
+      }
+      last_kv[t] = last;
+      nkv = max(nkv, last + 1);
     }
   }
 };
@@ -118,9 +135,9 @@ struct FwdWork {
 // similar total.
 __device__ __forceinline__ int sched_item(int k, int b, int G) { return k * G + ((k & 1) ? G - 1 - b : b); }
 
-__device__ __forceinline__ int total_items(int BH, int N, int NT) {
-  const int T = (N + 127) / 128;
-  return BH * ((T + NT - 1) / NT);
+__device__ __forceinline__ int total_items(const FwdLaunch& p, int NT) {
+  const int Tq = (p.Nq + 127) / 128;
+  return p.BH * ((Tq + NT - 1) / NT) * p.splits;
 }
 
 // ---------------------------------------------------------------------------
@@ -133,7 +150,7 @@ __device__ void fwd_load_role(const FwdLaunch& p, FwdShared& sh, uint8_t* sQ, ui
   tma_prefetch_desc(&p.tmK);
   tma_prefetch_desc(&p.tmV);
   tma_prefetch_desc(&p.tmO);
-  const int total = total_items(p.BH, p.N, C::NT);
+  const int total = total_items(p, C::NT);
   const int G = gridDim.x;
   const uint64_t lim = p.wait_limit_ns;
   int kv = 0;     // running count of K/V tiles loaded by this CTA
@@ -143,7 +160,8 @@ __device__ void fwd_load_role(const FwdLaunch& p, FwdShared& sh, uint8_t* sQ, ui
   for (int k = 0; k * G < total && !aborted; ++k) {
     const int item = sched_item(k, blockIdx.x, G);
     if (item >= total) continue;
-    const FwdWork<C::NT, CAUSAL> wk(item, p.BH, p.N);
+    const FwdWork<C::NT, CAUSAL> wk(item, p);
+    if (wk.nkv == 0) continue;  // a key range with nothing to do (every role skips it)
     const int kv_bh = wk.bh / p.group;  // grouped K/V heads: query head bh reads K/V head bh / g
     // Q_t's smem was the previous item's O staging: wait until its store read
     // it. The item's first K/V tile is issued before that wait so it loads
@@ -178,7 +196,8 @@ __device__ void fwd_load_role(const FwdLaunch& p, FwdShared& sh, uint8_t* sQ, ui
       mbar_arrive_expect_tx(&sh.k_full[ks], C::TILE_BYTES);
 #pragma unroll
       for (int c = 0; c < C::CHUNKS; ++c)
-        tma_load_3d(sK + ks * C::TILE_BYTES + c * C::CHUNK_BYTES, &p.tmK, &sh.k_full[ks], c * 64, j * 128, kv_bh);
+        tma_load_3d(sK + ks * C::TILE_BYTES + c * C::CHUNK_BYTES, &p.tmK, &sh.k_full[ks], c * 64, (wk.kv0 + j) * 128,
+                    kv_bh);
       ++k_issued;
       if (j == 0 && !load_q()) {
         aborted = true;
@@ -192,7 +211,8 @@ __device__ void fwd_load_role(const FwdLaunch& p, FwdShared& sh, uint8_t* sQ, ui
       mbar_arrive_expect_tx(&sh.v_full[vs], C::TILE_BYTES);
 #pragma unroll
       for (int c = 0; c < C::CHUNKS; ++c)
-        tma_load_3d(sV + vs * C::TILE_BYTES + c * C::CHUNK_BYTES, &p.tmV, &sh.v_full[vs], c * 64, j * 128, kv_bh);
+        tma_load_3d(sV + vs * C::TILE_BYTES + c * C::CHUNK_BYTES, &p.tmV, &sh.v_full[vs], c * 64, (wk.kv0 + j) * 128,
+                    kv_bh);
       ++v_issued;
     }
     if (aborted) break;
@@ -221,7 +241,7 @@ __device__ void fwd_mma_role(const FwdLaunch& p, FwdShared& sh, uint8_t* sQ, uin
   constexpr uint32_t kIdescPV = make_idesc_bf16_f32(128, HD, false, true);
   const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV);
   const uint64_t lim = p.wait_limit_ns;
-  const int total = total_items(p.BH, p.N, C::NT);
+  const int total = total_items(p, C::NT);
   const int G = gridDim.x;
 
   auto issue_s = [&](int t, int g) {  // g: running K/V tile index
@@ -251,7 +271,8 @@ __device__ void fwd_mma_role(const FwdLaunch& p, FwdShared& sh, uint8_t* sQ, uin
   for (int k = 0; k * G < total; ++k) {
     const int item = sched_item(k, blockIdx.x, G);
     if (item >= total) continue;
-    const FwdWork<C::NT, CAUSAL> wk(item, p.BH, p.N);
+    const FwdWork<C::NT, CAUSAL> wk(item, p);
+    if (wk.nkv == 0) continue;
     if (!mbar_wait(&sh.q_full, items & 1, &sh.abort_flag, lim)) return fail();
     if (!mbar_wait(&sh.k_full[kv % C::KST], (kv / C::KST) & 1, &sh.abort_flag, lim)) return fail();
     tc_fence_after_sync();
@@ -325,22 +346,24 @@ __device__ void fwd_softmax_role(const FwdLaunch& p, FwdShared& sh, uint8_t* sQ,
   const uint32_t tS = tmem + lane_base + C::s_col(t);
   const uint32_t tP = tmem + lane_base + C::p_col(t);
   const uint32_t tO = tmem + lane_base + C::o_col(t);
-  const int N = p.N;
-  const int T = (N + 127) / 128;
+  const int Nq = p.Nq, Nk = p.Nk;
+  const int Tk = (Nk + 127) / 128;
   const float c2 = p.scale_log2;
   const uint64_t lim = p.wait_limit_ns;
-  const int total = total_items(p.BH, N, C::NT);
+  const int total = total_items(p, C::NT);
   const int G = gridDim.x;
   uint8_t* stage = sQ + t * C::TILE_BYTES;  // O staging: Q_t once its last S MMA is done
   // After a timed-out wait a warp stops working but keeps passing every named
   // barrier and arrival, so the warpgroup's barrier counts stay matched.
   bool alive = true;
-  int cnt = 0;  // running S / P count of this slot
+  int cnt = 0;    // running S / P count of this slot
+  int items = 0;  // items processed (those with work)
 
   for (int k = 0; k * G < total; ++k) {
     const int item = sched_item(k, blockIdx.x, G);
     if (item >= total) continue;
-    const FwdWork<C::NT, CAUSAL> wk(item, p.BH, N);
+    const FwdWork<C::NT, CAUSAL> wk(item, p);
+    if (wk.nkv == 0) continue;
     const int qt = wk.qt[t];
     const int last_kv = wk.last_kv[t];
     const int row = qt * 128 + r;
@@ -370,12 +393,14 @@ __device__ void fwd_softmax_role(const FwdLaunch& p, FwdShared& sh, uint8_t* sQ,
           s[96 + i] = __uint_as_float(d[i]);
         }
       }
-      // Element-wise mask only on the key-tail tile and the causal diagonal tile.
-      const bool mask_tail = (j == T - 1) && (N & 127);
-      const bool mask_diag = CAUSAL && (j == qt);
+      // Element-wise mask only on the key-tail tile and the tiles the causal
+      // boundary crosses (key > row + causal_off).
+      const int a = wk.kv0 + j;  // absolute key tile
+      const bool mask_tail = (a == Tk - 1) && (Nk & 127);
+      const bool mask_diag = CAUSAL && (a * 128 + 127 > qt * 128 + p.causal_off);
       if (mask_tail || mask_diag) {
-        int lim_col = N - 1 - j * 128;
-        if (CAUSAL) lim_col = min(lim_col, row - j * 128);
+        int lim_col = Nk - 1 - a * 128;
+        if (CAUSAL) lim_col = min(lim_col, row + p.causal_off - a * 128);
 #pragma unroll
         for (int i = 0; i < 128; ++i)
           if (i > lim_col) s[i] = -INFINITY;
@@ -448,8 +473,33 @@ __device__ void fwd_softmax_role(const FwdLaunch& p, FwdShared& sh, uint8_t* sQ,
       if (!alive) record_timeout(p.status, &sh.abort_flag, WHERE_FWD_SOFTMAX);
     }
     tc_fence_after_sync();
-    if (alive && active) {
-      const float inv_l = 1.f / l;
+    // A row that saw no key of this range (possible only when the keys are
+    // split) has l = 0: its partial is O = 0, L = -inf, and the combine step
+    // never reads it.
+    const float inv_l = l > 0.f ? 1.f / l : 0.f;
+    const float lse_row = l > 0.f ? (m2 + log2f(l)) * kLn2 : -INFINITY;
+    if (alive && active && p.splits > 1) {
+      // fp32 partial of this key range, straight from TMEM to the workspace
+      float* dst = p.o_part + ((static_cast<size_t>(wk.s) * p.BH + wk.bh) * Nq + row) * HD;
+#pragma unroll 1
+      for (int c = 0; c < HD; c += 32) {
+        uint32_t o[32];
+        tmem_ld32(tO + c, o);
+        tmem_ld_wait();
+        if (c + 32 >= HD) {
+          tc_fence_before_sync();
+          mbar_arrive(&sh.o_free[t]);
+        }
+        if (row < Nq) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            *reinterpret_cast<float4*>(dst + c + 4 * u) =
+                make_float4(__uint_as_float(o[4 * u]) * inv_l, __uint_as_float(o[4 * u + 1]) * inv_l,
+                            __uint_as_float(o[4 * u + 2]) * inv_l, __uint_as_float(o[4 * u + 3]) * inv_l);
+        }
+      }
+      if (row < Nq) p.lse_part[(static_cast<size_t>(wk.s) * p.BH + wk.bh) * Nq + row] = lse_row;
+    } else if (alive && active) {
       const uint32_t stage_addr = smem_u32(stage);
 #pragma unroll 1
       for (int c = 0; c < HD; c += 32) {
@@ -471,13 +521,21 @@ __device__ void fwd_softmax_role(const FwdLaunch& p, FwdShared& sh, uint8_t* sQ,
         }
       }
       fence_proxy_async_smem();
-      if (row < N) p.lse[static_cast<size_t>(wk.bh) * N + row] = (m2 + log2f(l)) * kLn2;
+      if (row < Nq) p.lse[static_cast<size_t>(wk.bh) * Nq + row] = lse_row;
     } else {
+      // No query tile in this slot: nothing waits for this warpgroup, so it
+      // first waits for the item's Q load. That keeps its q_free / o_free
+      // arrivals one item at a time (a warpgroup that ran two items ahead
+      // would complete a phase the load thread has not waited for yet).
+      if (alive) {
+        alive = __all_sync(0xffffffffu, mbar_wait(&sh.q_full, items & 1, &sh.abort_flag, lim));
+        if (!alive) record_timeout(p.status, &sh.abort_flag, WHERE_FWD_SOFTMAX);
+      }
       mbar_arrive(&sh.o_free[t]);
     }
     named_barrier_sync(1 + t, 128);
     if (r == 0) {
-      if (alive && active && !*reinterpret_cast<volatile int*>(&sh.abort_flag)) {
+      if (alive && active && p.splits == 1 && !*reinterpret_cast<volatile int*>(&sh.abort_flag)) {
 #pragma unroll
         for (int c = 0; c < C::CHUNKS; ++c)
           tma_store_3d(&p.tmO, stage + c * C::CHUNK_BYTES, c * 64, qt * 128, wk.bh);
@@ -487,6 +545,7 @@ __device__ void fwd_softmax_role(const FwdLaunch& p, FwdShared& sh, uint8_t* sQ,
       mbar_arrive(&sh.q_free[t]);
     }
     if (active) cnt += last_kv + 1;
+    ++items;
   }
   if (r == 0) tma_store_wait_all();  // O stores complete before the CTA can exit
 }
@@ -549,8 +608,8 @@ cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
   auto kern = fa_fwd_kernel<HD, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  const int T = (a.N + 127) / 128;
-  const long long items = static_cast<long long>(a.BH) * ((T + C::NT - 1) / C::NT);
+  const int Tq = (a.Nq + 127) / 128;
+  const long long items = static_cast<long long>(a.BH) * ((Tq + C::NT - 1) / C::NT) * a.splits;
   // Persistent: one CTA per SM (the smem footprint allows no more), each
   // looping over its share of the items.
   const long long grid = items < a.num_sms ? items : a.num_sms;
@@ -559,6 +618,79 @@ cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
 }
 
 }  // namespace
+
+namespace {
+
+// Merge of the key ranges' partials (reading note 5.2: the running max and
+// sum make softmax blocks combinable; the same identity merges whole ranges):
+// with L_s and O_s of range s, each normalised by its own sum,
+//   L = log sum_s e^{L_s},   O = sum_s e^{L_s - L} O_s.
+// One warp per query row, HD / 32 consecutive columns per lane; ranges that
+// hold no key the row sees are not read. HBM-bound.
+template <int HD>
+__global__ void __launch_bounds__(256) fwd_combine_kernel(const float* __restrict__ o_part,
+                                                          const float* __restrict__ lse_part,
+                                                          __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
+                                                          int BH, int Nq, int Nk, int causal, int causal_off,
+                                                          int splits, int keys_per_split) {
+  constexpr int PER = HD / 32;
+  const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (row >= static_cast<long long>(BH) * Nq) return;
+  const int i = static_cast<int>(row % Nq);
+  const int last_key = causal ? min(Nk - 1, i + causal_off) : Nk - 1;
+  const int n = min(splits, last_key / keys_per_split + 1);
+  const size_t plane = static_cast<size_t>(BH) * Nq;
+  float m = -INFINITY;
+  for (int s = 0; s < n; ++s) m = fmaxf(m, __ldg(lse_part + s * plane + row));
+  float acc[PER];
+#pragma unroll
+  for (int k = 0; k < PER; ++k) acc[k] = 0.f;
+  float sum = 0.f;
+  for (int s = 0; s < n; ++s) {
+    const float wgt = expf(__ldg(lse_part + s * plane + row) - m);
+    sum += wgt;
+    const float* src = o_part + (s * plane + row) * HD + lane * PER;
+#pragma unroll
+    for (int k = 0; k < PER; k += 2) {
+      const float2 v = __ldg(reinterpret_cast<const float2*>(src + k));
+      acc[k] = fmaf(wgt, v.x, acc[k]);
+      acc[k + 1] = fmaf(wgt, v.y, acc[k + 1]);
+    }
+  }
+  const float inv = 1.f / sum;
+  uint32_t packed[PER / 2];
+#pragma unroll
+  for (int k = 0; k < PER; k += 2) packed[k / 2] = pack_bf16x2(acc[k] * inv, acc[k + 1] * inv);
+  __nv_bfloat16* dst = o + row * HD + lane * PER;
+  if constexpr (PER == 2) {
+    *reinterpret_cast<uint32_t*>(dst) = packed[0];
+  } else if constexpr (PER == 4) {
+    *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0], packed[1]);
+  } else {
+    *reinterpret_cast<uint4*>(dst) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+  }
+  if (lane == 0) lse[row] = m + logf(sum);
+}
+
+template <int HD>
+cudaError_t launch_combine_t(const FwdLaunch& a, cudaStream_t stream) {
+  const long long threads = static_cast<long long>(a.BH) * a.Nq * 32;
+  fwd_combine_kernel<HD><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, stream>>>(
+      a.o_part, a.lse_part, a.o, a.lse, a.BH, a.Nq, a.Nk, a.causal, a.causal_off, a.splits, a.kv_per_split * 128);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_combine(const FwdLaunch& a, cudaStream_t stream) {
+  switch (a.d) {
+    case 64: return launch_combine_t<64>(a, stream);
+    case 128: return launch_combine_t<128>(a, stream);
+    case 256: return launch_combine_t<256>(a, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
 
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t stream) {
   switch (a.d) {

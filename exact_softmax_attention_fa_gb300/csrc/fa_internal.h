@@ -30,7 +30,13 @@ struct FwdLaunch {
   CUtensorMap tmQ, tmK, tmV, tmO;
   float* lse;
   uint32_t* status;
-  int N, BH, d, causal;
+  int Nq, Nk, BH, d, causal;
+  int causal_off;    // Nk - Nq: query i sees key j iff j <= i + causal_off (bottom-right alignment)
+  int splits;        // key ranges per query tile; > 1: partial results go to o_part / lse_part
+  int kv_per_split;  // 128-key tiles per range
+  float* o_part;     // splits > 1: fp32 O of each range [splits][BH][Nq][d], normalised by its own l
+  float* lse_part;   // splits > 1: [splits][BH][Nq], natural log; the combine kernel merges them
+  __nv_bfloat16* o;  // [BH][Nq][d]: written by the combine kernel (splits > 1)
   int group;         // query heads per K/V head: query head bh reads K/V head bh / group
   float scale_log2;  // scale * log2(e): scores are exponentiated in base 2
   uint64_t wait_limit_ns;
@@ -65,6 +71,7 @@ struct BwdLaunch {
 // Launchers (defined in the kernel translation units). Return cudaSuccess or
 // the launch error.
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t stream);
+cudaError_t launch_fwd_combine(const FwdLaunch& a, cudaStream_t stream);  // splits > 1: merge the partials
 cudaError_t launch_bwd_pre(const BwdLaunch& a, cudaStream_t stream);   // D, base-2 L, zero dQ accumulator
 cudaError_t launch_bwd_main(const BwdLaunch& a, cudaStream_t stream);  // dK, dV; dQ into the accumulator
 cudaError_t launch_bwd_post(const BwdLaunch& a, cudaStream_t stream);  // dQ = bf16(accumulator)

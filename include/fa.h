@@ -84,6 +84,31 @@ fa_status_t fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, flo
                        int N, int d, int causal, float scale, cudaStream_t stream);
 
 /*
+ * Forward pass over a key range split and/or a key sequence of its own
+ * length (a query block against a longer key/value cache, e.g. decoding):
+ *   q, o : bf16 [B][Hq][Nq][d];  lse : fp32 [B][Hq][Nq]
+ *   k, v : bf16 [B][Hkv][Nk][d]  (grouped heads as for fa_fwd_gqa)
+ *   causal : query i sees key j iff j <= i + (Nk - Nq), i.e. the mask is
+ *            aligned to the last key (for Nq = Nk the usual causal mask);
+ *            needs Nq <= Nk. Nk must be >= 1.
+ *   num_splits : the keys of each query tile are cut into this many ranges of
+ *            whole 128-key tiles, processed as separate work items, and the
+ *            partial results (O of each range normalised by its own sum, and
+ *            its logsumexp L_s) are merged by a combine kernel:
+ *              L = log sum_s e^{L_s},  O = sum_s e^{L_s - L} O_s
+ *            (reading note 5.2: the running max and sum make softmax blocks
+ *            combinable). 1: no split, no workspace. 0: the library chooses,
+ *            within the workspace given. At most 256; ranges beyond the keys
+ *            are dropped.
+ *   workspace : fa_fwd_splitkv_workspace_size(B, Hq, Nq, d, splits) bytes,
+ *            256-byte aligned, for any split count above 1.
+ */
+fa_status_t fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                           int Nq, int Nk, int d, int causal, float scale, int num_splits, void* workspace,
+                           size_t workspace_bytes, cudaStream_t stream);
+size_t fa_fwd_splitkv_workspace_size(int B, int Hq, int Nq, int d, int num_splits);
+
+/*
  * Bytes of device workspace fa_bwd needs: D and the base-2 logsumexp
  * (fp32 per query row) and the fp32 dQ accumulator, with every head padded
  * to a multiple of 128 rows, plus 256 bytes for the main kernel's work-item

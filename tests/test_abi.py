@@ -102,6 +102,28 @@ def test_deterministic_backward_checks(lib):
     assert lib.fa_bwd_deterministic(P, P, P, P, P, P, P, P, P, 1, 1, 128, 256, 0, 0.125, P, 1 << 30, None) == UNSUPPORTED
 
 
+def test_split_key_forward_checks(lib):
+    def fwd_split(Nq=64, Nk=256, causal=0, splits=1, ws=P, ws_bytes=1 << 30, Hq=2, Hkv=2, d=64, ptr=P):
+        return lib.fa_fwd_splitkv(ptr, ptr, ptr, ptr, P, 1, Hq, Hkv, Nq, Nk, d, causal, 0.125, splits, ws, ws_bytes,
+                                  None)
+    assert fwd_split(Nq=300, Nk=200, causal=1) == INVALID  # a causal block longer than the keys
+    assert fwd_split(Nk=0) == INVALID
+    assert fwd_split(Nk=-1) == INVALID
+    assert fwd_split(splits=-1) == INVALID
+    assert fwd_split(splits=257) == INVALID
+    assert fwd_split(Hkv=3) == INVALID
+    assert fwd_split(d=96) == UNSUPPORTED
+    assert fwd_split(splits=2, ws=0) == WORKSPACE
+    assert fwd_split(splits=2, ws_bytes=16) == WORKSPACE
+    assert fwd_split(splits=2, ws=P + 16) == MISALIGNED
+    assert fwd_split(ptr=P + 8) == MISALIGNED
+    assert fwd_split(Nq=0, ptr=0) == OK
+    need = lib.fa_fwd_splitkv_workspace_size(1, 2, 64, 64, 3)
+    assert need == 3 * 2 * 64 * 64 * 4 + ((3 * 2 * 64 * 4 + 255) // 256) * 256
+    assert lib.fa_fwd_splitkv_workspace_size(1, 2, 64, 64, 1) == 0
+    assert lib.fa_fwd_splitkv_workspace_size(1, 2, 64, 64, 300) == 0
+
+
 def test_grouped_heads_other_checks(lib):
     assert fwd_gqa(lib, d=96) == UNSUPPORTED
     assert bwd_gqa(lib, scale=0.0) == INVALID

@@ -112,3 +112,17 @@ def test_long_causal_peaked_sampled(cuda_lib):
 def test_wide_head_d256_sampled(cuda_lib):
     w = WORKLOADS["wide_head_d256"]
     check_sampled(cuda_lib, w["B"], w["H"], w["N"], w["d"], w["causal"], seed_for(w))
+
+
+def test_persistent_ctas_with_several_half_empty_items():
+    # N = 300 gives 3 query tiles per head, so every head's last item has an
+    # empty second tile slot; with 304 heads a CTA takes two such items in a
+    # row (causal items come longest first). The idle slot must not run ahead.
+    import exact_softmax_attention_fa_gb300 as fa
+    from attn_inputs import BASE_SEED
+    x, f = inputs(1, 304, 300, 64, BASE_SEED + 900, tensors=("q", "k", "v"))
+    o, lse = fa.forward(to_device(x["q"]), to_device(x["k"]), to_device(x["v"]), causal=True, scale=scale_f32(64))
+    assert fa.fa_get_device_status() == 0
+    o_ref, lse_ref = oracle.attention_forward(f["q"], f["k"], f["v"], True, scale_f32(64))
+    assert np.abs(to_host64(o) - o_ref).max() <= TOL_O
+    assert np.abs(lse.cpu().numpy().astype(np.float64) - lse_ref).max() <= TOL_LSE
