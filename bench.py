@@ -49,7 +49,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 KERNEL_SOURCES = {
     "fa_bwd_main": ["exact_softmax_attention_fa_gb300/csrc/fa_bwd.cu",
                     "exact_softmax_attention_fa_gb300/csrc/sm103_ptx.cuh"],
-    "fa_fwd": ["exact_softmax_attention_fa_gb300/csrc/fa_fwd.cu",
+    "fa_fwd": ["exact_softmax_attention_fa_gb300/csrc/fa_fwd_kernel.cuh",
                "exact_softmax_attention_fa_gb300/csrc/sm103_ptx.cuh"],
 }
 

@@ -106,12 +106,13 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 // [BH][N][d] bf16, boxes of 128 rows x 64 columns, 128-byte swizzle; rows
 // past N read as zero and are not written by stores.
-bool make_map(CUtensorMap* m, const void* base, int BH, int N, int d, unsigned box_rows = 128) {
+bool make_map(CUtensorMap* m, const void* base, int BH, int N, int d, unsigned box_rows = 128,
+              unsigned box_heads = 1) {
   auto enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
-  cuuint32_t box[3] = {64, box_rows, 1};
+  cuuint32_t box[3] = {64, box_rows, box_heads};
   cuuint32_t estr[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -182,10 +183,11 @@ size_t splitkv_bytes(long long BH, int Nq, int d, int splits) {
 // Automatic number of key ranges: enough items for about two per SM when the
 // query tiles alone are too few (short query blocks such as decoding), at
 // least one key tile per range, and no more ranges than the workspace holds.
-int auto_splits(long long BH, int Nq, int Nk, int d, int sms, size_t room) {
-  const long long tq = (Nq + 127) / 128;
+// units: query-head units (heads, or packed head groups), tq: query tiles per
+// unit; BH, Nq size the partials.
+int auto_splits(long long units, long long tq, int Nk, int d, int sms, long long BH, int Nq, size_t room) {
   const long long nt = d <= 128 ? 2 : 1;  // query tiles per CTA
-  const long long items = BH * ((tq + nt - 1) / nt);
+  const long long items = units * ((tq + nt - 1) / nt);
   const int Tk = (Nk + 127) / 128;
   if (items >= sms || Tk < 2) return 1;
   long long want = (2LL * sms + items - 1) / items;
@@ -282,11 +284,16 @@ fa_status_t fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o,
     return FA_ERR_MISALIGNED;
   const int BH = B * Hq, BHkv = B * Hkv;
   const int Tk = (Nk + 127) / 128;
+  // A query block shorter than a tile shares its tiles among the query heads
+  // of a K/V group (a power-of-two group of at most 128 heads).
+  const int g = Hq / Hkv;
+  const int pack = (Nq < 128 && g >= 2 && g <= 128 && (g & (g - 1)) == 0) ? g : 1;
   int splits = num_splits;
   if (splits == 0) {
     DeviceState* ds0 = device_state(&st);
     if (!ds0) return st;
-    splits = auto_splits(BH, Nq, Nk, d, ds0->num_sms, workspace ? workspace_bytes : 0);
+    splits = auto_splits(BH / pack, (Nq + 128 / pack - 1) / (128 / pack), Nk, d, ds0->num_sms, BH, Nq,
+                         workspace ? workspace_bytes : 0);
   }
   int per = (Tk + splits - 1) / splits;  // key tiles per range; no range is empty
   splits = (Tk + per - 1) / per;
@@ -297,11 +304,13 @@ fa_status_t fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o,
   DeviceState* ds = device_state(&st);
   if (!ds) return st;
   FwdLaunch a{};
-  if (!make_map(&a.tmQ, q, BH, Nq, d) || !make_map(&a.tmK, k, BHkv, Nk, d) || !make_map(&a.tmV, v, BHkv, Nk, d) ||
-      !make_map(&a.tmO, o, BH, Nq, d))
+  if (!make_map(&a.tmQ, q, BH, Nq, d, 128 / pack, pack) || !make_map(&a.tmK, k, BHkv, Nk, d) ||
+      !make_map(&a.tmV, v, BHkv, Nk, d) || !make_map(&a.tmO, o, BH, Nq, d, 128 / pack, pack))
     return FA_ERR_CUDA;
   a.lse = lse;
   a.o = static_cast<__nv_bfloat16*>(o);
+  a.pack = pack;
+  a.rph = 128 / pack;
   a.status = ds->status;
   a.Nq = Nq;
   a.Nk = Nk;

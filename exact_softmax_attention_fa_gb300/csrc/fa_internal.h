@@ -38,6 +38,8 @@ struct FwdLaunch {
   float* lse_part;   // splits > 1: [splits][BH][Nq], natural log; the combine kernel merges them
   __nv_bfloat16* o;  // [BH][Nq][d]: written by the combine kernel (splits > 1)
   int group;         // query heads per K/V head: query head bh reads K/V head bh / group
+  int pack;          // query heads sharing one 128-row tile (1, or the group when query blocks are short)
+  int rph;           // query positions per head in a tile: 128 / pack
   float scale_log2;  // scale * log2(e): scores are exponentiated in base 2
   uint64_t wait_limit_ns;
   int num_sms;
@@ -72,6 +74,7 @@ struct BwdLaunch {
 // the launch error.
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t stream);
 cudaError_t launch_fwd_combine(const FwdLaunch& a, cudaStream_t stream);  // splits > 1: merge the partials
+cudaError_t launch_fwd_packed(const FwdLaunch& a, cudaStream_t stream);   // fa_fwd_pack.cu: pack > 1
 cudaError_t launch_bwd_pre(const BwdLaunch& a, cudaStream_t stream);   // D, base-2 L, zero dQ accumulator
 cudaError_t launch_bwd_main(const BwdLaunch& a, cudaStream_t stream);  // dK, dV; dQ into the accumulator
 cudaError_t launch_bwd_post(const BwdLaunch& a, cudaStream_t stream);  // dQ = bf16(accumulator)

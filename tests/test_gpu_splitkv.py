@@ -93,3 +93,21 @@ def test_long_keys_many_splits_peaked():
     xq, fq = inputs(1, 2, 256, 128, BASE_SEED + 890, tensors=("q",), peaked_frac=0.01)
     xk, fk = inputs(1, 2, 16384, 128, BASE_SEED + 891, tensors=("k", "v"))
     check({**xq, **xk}, {**fq, **fk}, True, 128, 16)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Hq,Hkv", [(4, 2), (8, 1), (8, 2), (6, 2), (32, 1)])
+@pytest.mark.parametrize("Nq", [1, 5, 31, 32, 33, 127])
+def test_grouped_short_blocks_share_tiles(causal, Hq, Hkv, Nq):
+    # short query blocks pack the group's query heads into one tile (power-of-
+    # two groups); unsplit and split key ranges
+    Nk = 1500
+    x, f = make(2, Hq, Hkv, Nq, Nk, 128, BASE_SEED + 910 + Nq + Hq)
+    for splits in (1, 4):
+        check(x, f, causal, 128, splits)
+
+
+@pytest.mark.parametrize("d", [64, 256])
+def test_grouped_decode_other_head_dims(d):
+    x, f = make(2, 8, 2, 3, 2100, d, BASE_SEED + 960 + d)
+    check(x, f, True, d, 0, ws_splits=32)
