@@ -345,11 +345,11 @@ __device__ void bwd_mma_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sK, uin
 
   // D[tmem] = A (128 x HD, K-major) * B (128 x HD, K-major)^T
   auto issue_sq = [&](uint32_t d_col, uint32_t a_addr, uint32_t b_addr) {
+    const uint64_t ad = make_smem_desc_sw128(a_addr, 16, 1024), bd = make_smem_desc_sw128(b_addr, 16, 1024);
 #pragma unroll
     for (int ks = 0; ks < HD / 16; ++ks) {
       const uint32_t off = (ks >> 2) * C::CHUNK_BYTES + (ks & 3) * 32;
-      umma_ss(tmem + d_col, make_smem_desc_sw128(a_addr + off, 16, 1024), make_smem_desc_sw128(b_addr + off, 16, 1024),
-              kIdescSq, ks > 0 ? 1u : 0u);
+      umma_ss(tmem + d_col, desc_add(ad, off), desc_add(bd, off), kIdescSq, ks > 0 ? 1u : 0u);
     }
   };
   auto fail = [&]() { record_timeout(p.status, &sh.abort_flag, WHERE_BWD_MMA); };
@@ -384,10 +384,11 @@ __device__ void bwd_mma_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sK, uin
       if (n == 0 && items > 0 && !mbar_wait(&sh.acc_free, (items - 1) & 1, &sh.abort_flag, lim)) return fail();
       tc_fence_after_sync();
       // dV += P^T dO_n; P^T (bf16) sits in columns [0,32) and [64,96) of region A
+      const uint64_t dod = make_smem_desc_sw128(doa, C::CHUNK_BYTES, 1024);
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks)
-        umma_ts(tmem + C::DV_COL, tmem + C::REG_A + (ks >> 2) * 64 + (ks & 3) * 8,
-                make_smem_desc_sw128(doa + ks * 2048, C::CHUNK_BYTES, 1024), kIdescAcc, (n > 0 || ks > 0) ? 1u : 0u);
+        umma_ts(tmem + C::DV_COL, tmem + C::REG_A + (ks >> 2) * 64 + (ks & 3) * 8, desc_add(dod, ks * 2048), kIdescAcc,
+                (n > 0 || ks > 0) ? 1u : 0u);
       umma_commit(&sh.pv_done);
       if (has_next) {
         // S^T(n+1) overwrites P^T(n): wait until dV(n) has read it.
@@ -400,18 +401,21 @@ __device__ void bwd_mma_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sK, uin
       if (!mbar_wait(&sh.ds_ready, g & 1, &sh.abort_flag, lim)) return fail();
       tc_fence_after_sync();
       // dK += dS^T Q_n
+      const uint64_t dsk = make_smem_desc_sw128(ds_addr, 16, 1024), qmn = make_smem_desc_sw128(qa, C::CHUNK_BYTES, 1024);
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks)
-        umma_ss(tmem + C::DK_COL, make_smem_desc_sw128(ds_addr + (ks >> 2) * C::CHUNK_BYTES + (ks & 3) * 32, 16, 1024),
-                make_smem_desc_sw128(qa + ks * 2048, C::CHUNK_BYTES, 1024), kIdescAcc, (n > 0 || ks > 0) ? 1u : 0u);
+        umma_ss(tmem + C::DK_COL, desc_add(dsk, (ks >> 2) * C::CHUNK_BYTES + (ks & 3) * 32), desc_add(qmn, ks * 2048),
+                kIdescAcc, (n > 0 || ks > 0) ? 1u : 0u);
       if constexpr (DQ) {
         // dQ_n into region B. d = 128: dQ_n^T = K_j^T dS^T (head-dim columns on
         // the lanes, queries along the columns), so the drain's reductions
         // cover whole 128-byte lines. d = 64: dQ_n = dS K_j (queries on lanes).
+        const uint64_t dsm = make_smem_desc_sw128(ds_addr, C::CHUNK_BYTES, 1024);
+        const uint64_t kmn = make_smem_desc_sw128(k_addr, C::CHUNK_BYTES, 1024);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
-          const uint64_t ds_mn = make_smem_desc_sw128(ds_addr + ks * 2048, C::CHUNK_BYTES, 1024);
-          const uint64_t k_mn = make_smem_desc_sw128(k_addr + ks * 2048, C::CHUNK_BYTES, 1024);
+          const uint64_t ds_mn = desc_add(dsm, ks * 2048);
+          const uint64_t k_mn = desc_add(kmn, ks * 2048);
           if constexpr (C::DQ_T)
             umma_ss(tmem + C::REG_B, k_mn, ds_mn, kIdescDq, ks > 0 ? 1u : 0u);
           else

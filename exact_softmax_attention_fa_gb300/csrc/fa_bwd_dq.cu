@@ -13,16 +13,18 @@
 //
 // GB300 mapping: persistent, one CTA (320 threads) per SM taking items from a
 // counter in the workspace (causal: the query tiles that see the most keys
-// first). Warp 8 streams Q_i, dO_i once per item and K_j, V_j through a ring;
+// first). Warp 8 streams Q_i, dO_i once per item and K_j, V_j through two
+// rings (K deeper: K_j is read by S(j) and, late, by the dQ product);
 // warp 9 issues the MMAs (S and dP into TMEM, dQ accumulated in TMEM);
 // warpgroups 0 and 1 own key columns [64w, 64w + 64) of every tile, thread r
 // = query row r = TMEM lane r, so the row statistics L_r and D_r are
 // per-thread scalars. P (bf16, the rounding the dV product of the main kernel
-// uses) and dS stay row-major: dS goes to a 128-byte-swizzled smem tile that
-// is the K-major A operand of dQ += dS K_j, with K_j as the MN-major B
-// operand.
+// uses) stays in registers; dS (bf16) is written back into the columns of
+// its own tile's S buffer, already read, and is the TMEM A operand of
+// dQ += dS K_j, with K_j as the MN-major B operand.
 //
-// TMEM columns (512 allocated): S [0, 128), dP [128, 256), dQ [256, 256 + d).
+// TMEM columns (512 allocated): S buffers [0, 128) and [128, 256), dP
+// [256, 384), dQ [384, 384 + d).
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -44,17 +46,23 @@ struct DqCfg {
   static constexpr int CHUNKS = HD / 64;
   static constexpr int TILE_BYTES = 128 * HD * 2;
   static constexpr int CHUNK_BYTES = 128 * 128;
-  static constexpr int KST = HD == 64 ? 3 : 2;  // K_j / V_j ring stages
-  static constexpr int DS_BYTES = 128 * 128 * 2;
-  static constexpr uint32_t S_COL = 0, DP_COL = 128, DQ_COL = 256;
-  // smem: Q_i, dO_i, KST x (K_j, V_j), dS
-  static constexpr int SMEM_BYTES = (2 + 2 * KST) * TILE_BYTES + DS_BYTES + 1024;
+  // K_j is read by S(j) early and by the dQ product late; V_j only by dP(j).
+  // A deeper K ring lets S(j+1) start while K_j is still in use.
+  static constexpr int KST = HD == 64 ? 4 : 3;  // K_j ring stages
+  static constexpr int VST = 2;                 // V_j ring stages
+  // S is double-buffered (tile t in buffer t & 1), so S(t+1) is computed
+  // while the softmax still works on tile t.
+  static constexpr uint32_t S_COL = 0, DP_COL = 256, DQ_COL = 384;
+  __host__ __device__ static constexpr uint32_t s_col(int b) { return S_COL + 128u * uint32_t(b); }
+  // smem: Q_i, dO_i, KST x K_j, VST x V_j (dS lives in TMEM)
+  static constexpr int SMEM_BYTES = (2 + KST + VST) * TILE_BYTES + 1024;
 };
 
 struct DqShared {
   uint64_t q_full, q_free;
-  uint64_t kv_full[3], kv_empty[3];
-  uint64_t s_full, s_free, dp_full, dp_free, ds_ready, dq_done, acc_done, acc_free;
+  uint64_t k_full[4], k_empty[4], v_full[2], v_empty[2];
+  uint64_t s_full[2];  // per S buffer
+  uint64_t dp_full, dp_free, ds_ready, dq_done, acc_done, acc_free;
   uint64_t item_full[kItemSlots], item_empty[kItemSlots];
   int item_ring[kItemSlots];
   uint32_t tmem_base;
@@ -94,17 +102,20 @@ __device__ void dq_load_role(const BwdLaunch& p, DqShared& sh, uint8_t* sQ, uint
   const int T = (p.N + 127) / 128;
   const int total = p.BH * T;
   const uint64_t lim = p.wait_limit_ns;
-  int u = 0, kv = 0, q_issued = 0;
+  int u = 0, kv = 0, q_issued = 0;  // kv: K/V tiles loaded
   bool aborted = false;
   auto load_kv = [&](int j, int kvh) -> bool {
-    const int s = kv % C::KST;
-    if (kv >= C::KST && !mbar_wait(&sh.kv_empty[s], ((kv / C::KST) - 1) & 1, &sh.abort_flag, lim)) return false;
-    mbar_arrive_expect_tx(&sh.kv_full[s], 2 * C::TILE_BYTES);
+    const int ks = kv % C::KST, vs = kv % C::VST;
+    if (kv >= C::KST && !mbar_wait(&sh.k_empty[ks], ((kv / C::KST) - 1) & 1, &sh.abort_flag, lim)) return false;
+    mbar_arrive_expect_tx(&sh.k_full[ks], C::TILE_BYTES);
 #pragma unroll
-    for (int c = 0; c < C::CHUNKS; ++c) {
-      tma_load_3d(sK + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &p.tmK, &sh.kv_full[s], c * 64, j * 128, kvh);
-      tma_load_3d(sV + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &p.tmV, &sh.kv_full[s], c * 64, j * 128, kvh);
-    }
+    for (int c = 0; c < C::CHUNKS; ++c)
+      tma_load_3d(sK + ks * C::TILE_BYTES + c * C::CHUNK_BYTES, &p.tmK, &sh.k_full[ks], c * 64, j * 128, kvh);
+    if (kv >= C::VST && !mbar_wait(&sh.v_empty[vs], ((kv / C::VST) - 1) & 1, &sh.abort_flag, lim)) return false;
+    mbar_arrive_expect_tx(&sh.v_full[vs], C::TILE_BYTES);
+#pragma unroll
+    for (int c = 0; c < C::CHUNKS; ++c)
+      tma_load_3d(sV + vs * C::TILE_BYTES + c * C::CHUNK_BYTES, &p.tmV, &sh.v_full[vs], c * 64, j * 128, kvh);
     ++kv;
     return true;
   };
@@ -137,38 +148,64 @@ __device__ void dq_load_role(const BwdLaunch& p, DqShared& sh, uint8_t* sQ, uint
   const int zero = 0;
   if (aborted) {
     record_timeout(p.status, &sh.abort_flag, WHERE_BWD_LOAD);
-    for (int n = std::max(0, kv - C::KST); n < kv; ++n)
-      mbar_wait(&sh.kv_full[n % C::KST], (n / C::KST) & 1, &zero, lim);
+    // the K and V copies of the last tiles may still be in flight
+    for (int n = std::max(0, kv - C::KST); n < kv; ++n) mbar_wait(&sh.k_full[n % C::KST], (n / C::KST) & 1, &zero, lim);
+    for (int n = std::max(0, kv - C::VST); n < kv; ++n) mbar_wait(&sh.v_full[n % C::VST], (n / C::VST) & 1, &zero, lim);
   }
   if (q_issued > 0) mbar_wait(&sh.q_full, (q_issued - 1) & 1, &zero, lim);
 }
 
 // One thread issues every MMA. Per key tile j (global tile t):
-//   S(j+1)   after phase A(j) has read S(j)       (overlaps phases A, B of j)
-//   dQ += dS(j) K_j   after phase B(j)            (overlaps phase A(j+1))
-//   dP(j+1)  after phase B(j) has read dP(j)      (overlaps phase A(j+1))
+//   S(t+1)   into the other S buffer once K_{j+1} is in and the dQ product
+//            of tile t-1 (whose dS sat there) is done (overlaps A(t), B(t))
+//   dP(t+1)  once phase B(t) has read dP(t)        (overlaps the rest of B(t))
+//   dQ += dS(t) K_j   once phase B(t) wrote dS(t)  (overlaps phase A(t+1))
 template <int HD, bool CAUSAL>
 __device__ void dq_mma_role(const BwdLaunch& p, DqShared& sh, uint8_t* sQ, uint8_t* sdO, uint8_t* sK, uint8_t* sV,
-                            uint8_t* sDS, uint32_t tmem) {
+                            uint32_t tmem) {
   using C = DqCfg<HD>;
   constexpr uint32_t kIdescSq = make_idesc_bf16_f32(128, 128, false, false);  // S, dP: A, B K-major
-  constexpr uint32_t kIdescDq = make_idesc_bf16_f32(128, HD, false, true);    // A = dS K-major, B = K_j MN-major
-  const uint32_t q_addr = smem_u32(sQ), do_addr = smem_u32(sdO), k_addr = smem_u32(sK), v_addr = smem_u32(sV),
-                 ds_addr = smem_u32(sDS);
+  constexpr uint32_t kIdescDq = make_idesc_bf16_f32(128, HD, false, true);    // A = dS (TMEM), B = K_j MN-major
+  const uint32_t q_addr = smem_u32(sQ), do_addr = smem_u32(sdO), k_addr = smem_u32(sK), v_addr = smem_u32(sV);
   const uint64_t lim = p.wait_limit_ns;
   const int T = (p.N + 127) / 128;
   const int total = p.BH * T;
 
   // D[tmem] = A (128 x HD, K-major) * B (128 x HD, K-major)^T
   auto issue_sq = [&](uint32_t d_col, uint32_t a_addr, uint32_t b_addr) {
+    const uint64_t ad = make_smem_desc_sw128(a_addr, 16, 1024), bd = make_smem_desc_sw128(b_addr, 16, 1024);
 #pragma unroll
     for (int ks = 0; ks < HD / 16; ++ks) {
       const uint32_t off = (ks >> 2) * C::CHUNK_BYTES + (ks & 3) * 32;
-      umma_ss(tmem + d_col, make_smem_desc_sw128(a_addr + off, 16, 1024), make_smem_desc_sw128(b_addr + off, 16, 1024),
-              kIdescSq, ks > 0 ? 1u : 0u);
+      umma_ss(tmem + d_col, desc_add(ad, off), desc_add(bd, off), kIdescSq, ks > 0 ? 1u : 0u);
     }
   };
   auto fail = [&]() { record_timeout(p.status, &sh.abort_flag, WHERE_BWD_MMA); };
+
+  // S(t) into buffer t & 1, which tile t - 2 used.
+  // done_tile: the latest dQ product issued (tile t - 2 inside an item, t - 1
+  // at an item's start); its completion implies that of every earlier one,
+  // including the product of tile t - 2 whose dS sat in buffer t & 1.
+  auto issue_s = [&](int t, int kvi, int done_tile) -> bool {  // kvi: the tile's index in the K/V stream
+    const int stage = kvi % C::KST;
+    if (!mbar_wait(&sh.k_full[stage], (kvi / C::KST) & 1, &sh.abort_flag, lim)) return false;
+    if (t >= 2 && !mbar_wait(&sh.dq_done, done_tile & 1, &sh.abort_flag, lim)) return false;
+    tc_fence_after_sync();
+    issue_sq(C::s_col(t & 1), q_addr, k_addr + stage * C::TILE_BYTES);
+    umma_commit(&sh.s_full[t & 1]);
+    return true;
+  };
+  // dP(t) over dP(t - 1): wait until phase B(t - 1) loaded it.
+  auto issue_dp = [&](int t, int kvi) -> bool {
+    const int stage = kvi % C::VST;
+    if (!mbar_wait(&sh.v_full[stage], (kvi / C::VST) & 1, &sh.abort_flag, lim)) return false;
+    if (t >= 1 && !mbar_wait(&sh.dp_free, (t - 1) & 1, &sh.abort_flag, lim)) return false;
+    tc_fence_after_sync();
+    issue_sq(C::DP_COL, do_addr, v_addr + stage * C::TILE_BYTES);
+    umma_commit(&sh.dp_full);
+    umma_commit(&sh.v_empty[stage]);  // V_j is read by dP(j) only
+    return true;
+  };
 
   int u = 0, kv = 0, t = 0;
   while (true) {
@@ -176,52 +213,31 @@ __device__ void dq_mma_role(const BwdLaunch& p, DqShared& sh, uint8_t* sQ, uint8
     if (item < 0) return fail();
     if (item >= total) break;
     const DqWork<CAUSAL> wk(item, p.BH, p.N);
-    {
-      const int s = kv % C::KST;
-      if (!mbar_wait(&sh.q_full, u & 1, &sh.abort_flag, lim) ||
-          !mbar_wait(&sh.kv_full[s], (kv / C::KST) & 1, &sh.abort_flag, lim))
-        return fail();
-      if (t > 0 && !mbar_wait(&sh.s_free, (t - 1) & 1, &sh.abort_flag, lim)) return fail();
-      tc_fence_after_sync();
-      issue_sq(C::S_COL, q_addr, k_addr + s * C::TILE_BYTES);
-      umma_commit(&sh.s_full);
-      if (t > 0 && !mbar_wait(&sh.dp_free, (t - 1) & 1, &sh.abort_flag, lim)) return fail();
-      tc_fence_after_sync();
-      issue_sq(C::DP_COL, do_addr, v_addr + s * C::TILE_BYTES);
-      umma_commit(&sh.dp_full);
-      if (wk.nkv == 1) umma_commit(&sh.q_free);
-    }
+    if (!mbar_wait(&sh.q_full, u & 1, &sh.abort_flag, lim) || !issue_s(t, kv, t - 1) || !issue_dp(t, kv))
+      return fail();
+    if (wk.nkv == 1) umma_commit(&sh.q_free);
+    // Per tile t: S(t+1) as soon as its K tile is in, dP(t+1) once phase B(t)
+    // has read dP(t), dQ += dS(t) K once phase B(t) has written dS(t).
     for (int j = 0; j < wk.nkv; ++j, ++kv, ++t) {
       const int s = kv % C::KST;
-      const int s1 = (kv + 1) % C::KST;
-      const bool has_next = j + 1 < wk.nkv;
-      if (has_next) {
-        if (!mbar_wait(&sh.kv_full[s1], ((kv + 1) / C::KST) & 1, &sh.abort_flag, lim) ||
-            !mbar_wait(&sh.s_free, t & 1, &sh.abort_flag, lim))
-          return fail();
-        tc_fence_after_sync();
-        issue_sq(C::S_COL, q_addr, k_addr + s1 * C::TILE_BYTES);
-        umma_commit(&sh.s_full);
+      if (j + 1 < wk.nkv) {
+        if (!issue_s(t + 1, kv + 1, t - 1) || !issue_dp(t + 1, kv + 1)) return fail();
+        if (j + 2 == wk.nkv) umma_commit(&sh.q_free);  // the item's last S and dP are issued
       }
       if (!mbar_wait(&sh.ds_ready, t & 1, &sh.abort_flag, lim)) return fail();
       // the first dQ product of an item overwrites the accumulator: the
       // previous item's epilogue must have read it
       if (j == 0 && u > 0 && !mbar_wait(&sh.acc_free, (u - 1) & 1, &sh.abort_flag, lim)) return fail();
       tc_fence_after_sync();
+      // dS (bf16 pairs) sits in columns [0, 32) and [64, 96) of S buffer t & 1:
+      // keys 16 ks .. 16 ks + 15 are 8 columns at 64 (ks / 4) + 8 (ks % 4)
+      const uint64_t kd = make_smem_desc_sw128(k_addr + s * C::TILE_BYTES, C::CHUNK_BYTES, 1024);
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks)
-        umma_ss(tmem + C::DQ_COL, make_smem_desc_sw128(ds_addr + (ks >> 2) * C::CHUNK_BYTES + (ks & 3) * 32, 16, 1024),
-                make_smem_desc_sw128(k_addr + s * C::TILE_BYTES + ks * 2048, C::CHUNK_BYTES, 1024), kIdescDq,
-                (j > 0 || ks > 0) ? 1u : 0u);
+        umma_ts(tmem + C::DQ_COL, tmem + C::s_col(t & 1) + (ks >> 2) * 64 + (ks & 3) * 8, desc_add(kd, ks * 2048),
+                kIdescDq, (j > 0 || ks > 0) ? 1u : 0u);
       umma_commit(&sh.dq_done);
-      umma_commit(&sh.kv_empty[s]);
-      if (has_next) {
-        if (!mbar_wait(&sh.dp_free, t & 1, &sh.abort_flag, lim)) return fail();
-        tc_fence_after_sync();
-        issue_sq(C::DP_COL, do_addr, v_addr + s1 * C::TILE_BYTES);
-        umma_commit(&sh.dp_full);
-        if (j + 2 == wk.nkv) umma_commit(&sh.q_free);  // the item's last S and dP are issued
-      }
+      umma_commit(&sh.k_empty[s]);
     }
     umma_commit(&sh.acc_done);
     ++u;
@@ -233,16 +249,15 @@ __device__ void dq_mma_role(const BwdLaunch& p, DqShared& sh, uint8_t* sQ, uint8
 // registers). Phase B: dS = P o (dP scale - D_r scale) into the dS tile. At
 // the end of an item warpgroup w writes dQ columns [w d/2, (w+1) d/2).
 template <int HD, bool CAUSAL>
-__device__ void dq_softmax_role(const BwdLaunch& p, DqShared& sh, uint8_t* sDS, uint32_t tmem, int w) {
+__device__ void dq_softmax_role(const BwdLaunch& p, DqShared& sh, uint32_t tmem, int w) {
   using C = DqCfg<HD>;
   const int r = threadIdx.x & 127;
   const uint32_t lane_base = static_cast<uint32_t>((threadIdx.x >> 5) & 3) << 21;
   const float c2 = p.scale_log2;
   const float sc = p.scale;
   const uint64_t lim = p.wait_limit_ns;
-  const uint32_t tS = tmem + lane_base + C::S_COL + 64 * w;
+  const uint32_t tS0 = tmem + lane_base + C::S_COL + 64 * w;  // + 128 for buffer 1
   const uint32_t tDP = tmem + lane_base + C::DP_COL + 64 * w;
-  const uint32_t ds_chunk = smem_u32(sDS) + w * C::CHUNK_BYTES;  // keys 64w .. 64w+63 of the tile
   const uint32_t bar_id = 1 + w;
   const int T = (p.N + 127) / 128;
   const int total = p.BH * T;
@@ -275,10 +290,11 @@ __device__ void dq_softmax_role(const BwdLaunch& p, DqShared& sh, uint8_t* sDS, 
     const float dsc = __ldg(p.D + srow) * sc;
     for (int j = 0; j < wk.nkv; ++j, ++t) {
       // ---- phase A
-      wait_all(&sh.s_full, t & 1, WHERE_BWD_SOFTMAX);
+      wait_all(&sh.s_full[t & 1], (t >> 1) & 1, WHERE_BWD_SOFTMAX);
       if (alive) {
         float pv[64];
         {
+          const uint32_t tS = tS0 + 128u * uint32_t(t & 1);
           uint32_t a[32], b[32];
           tmem_ld32(tS, a);
           tmem_ld32(tS + 32, b);
@@ -289,8 +305,7 @@ __device__ void dq_softmax_role(const BwdLaunch& p, DqShared& sh, uint8_t* sDS, 
             pv[32 + c] = __uint_as_float(b[c]);
           }
         }
-        tc_fence_before_sync();
-        mbar_arrive(&sh.s_free);
+
         // key 128j + 64w + c is seen if it is < N and (causal) <= the query row
         const int kbase = j * 128 + 64 * w;
         int c_hi = std::min(64, p.N - kbase);
@@ -313,9 +328,11 @@ __device__ void dq_softmax_role(const BwdLaunch& p, DqShared& sh, uint8_t* sDS, 
           pk[c4 / 2 + 1] = pack_bf16x2(pv[c4 + 2], pv[c4 + 3]);
         }
       }
-      // ---- phase B
+      // ---- phase B: dS into the first 32 columns of this warpgroup's half of
+      // S buffer t & 1 (phase A has read them)
       wait_all(&sh.dp_full, t & 1, WHERE_BWD_SOFTMAX);
       if (alive) {
+        uint32_t ds[32];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           uint32_t dpv[32];
@@ -325,7 +342,6 @@ __device__ void dq_softmax_role(const BwdLaunch& p, DqShared& sh, uint8_t* sDS, 
             tc_fence_before_sync();
             mbar_arrive(&sh.dp_free);
           }
-          uint32_t ds[16];
 #pragma unroll
           for (int c4 = 0; c4 < 32; c4 += 4) {
             const float2 p01 = unpack_bf16x2(pk[16 * h + c4 / 2]);
@@ -334,27 +350,14 @@ __device__ void dq_softmax_role(const BwdLaunch& p, DqShared& sh, uint8_t* sDS, 
             const float2 g23 = ffma2_bcast(__uint_as_float(dpv[c4 + 2]), __uint_as_float(dpv[c4 + 3]), sc, -dsc);
             const float2 d01 = fmul2(p01, g01);
             const float2 d23 = fmul2(p23, g23);
-            ds[c4 / 2] = pack_bf16x2(d01.x, d01.y);
-            ds[c4 / 2 + 1] = pack_bf16x2(d23.x, d23.y);
+            ds[16 * h + c4 / 2] = pack_bf16x2(d01.x, d01.y);
+            ds[16 * h + c4 / 2 + 1] = pack_bf16x2(d23.x, d23.y);
           }
-          if (h == 0 && t > 0) {
-            // the previous dQ product has finished reading the dS tile
-            alive = __all_sync(0xffffffffu, mbar_wait(&sh.dq_done, (t - 1) & 1, &sh.abort_flag, lim));
-            if (!alive) {
-              record_timeout(p.status, &sh.abort_flag, WHERE_BWD_SOFTMAX);
-              break;
-            }
-          }
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            st_shared_v4(ds_chunk + sw128_offset(r, 4 * h + q), ds[4 * q], ds[4 * q + 1], ds[4 * q + 2],
-                         ds[4 * q + 3]);
         }
-        if (alive) {
-          fence_proxy_async_smem();
-          tc_fence_before_sync();
-          mbar_arrive(&sh.ds_ready);
-        }
+        tmem_st32(tS0 + 128u * uint32_t(t & 1), ds);
+        tmem_st_wait();
+        tc_fence_before_sync();
+        mbar_arrive(&sh.ds_ready);
       }
     }
     const int item_next = next_item(u + 1);
@@ -398,18 +401,20 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
   uint8_t* sdO = sQ + C::TILE_BYTES;
   uint8_t* sK = sdO + C::TILE_BYTES;
   uint8_t* sV = sK + C::KST * C::TILE_BYTES;
-  uint8_t* sDS = sV + C::KST * C::TILE_BYTES;
   const int warp = threadIdx.x >> 5;
 
   if (threadIdx.x == 0) {
     mbar_init(&sh.q_full, 1);
     mbar_init(&sh.q_free, 1);
-    for (int s = 0; s < 3; ++s) {
-      mbar_init(&sh.kv_full[s], 1);
-      mbar_init(&sh.kv_empty[s], 1);
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(&sh.k_full[s], 1);
+      mbar_init(&sh.k_empty[s], 1);
     }
-    mbar_init(&sh.s_full, 1);
-    mbar_init(&sh.s_free, 256);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&sh.v_full[s], 1);
+      mbar_init(&sh.v_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) mbar_init(&sh.s_full[b], 1);
     mbar_init(&sh.dp_full, 1);
     mbar_init(&sh.dp_free, 256);
     mbar_init(&sh.ds_ready, 256);
@@ -435,9 +440,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
   if (warp == kLoadWarp) {
     if (lane_id() == 0) dq_load_role<HD, CAUSAL>(p, sh, sQ, sdO, sK, sV);
   } else if (warp == kMmaWarp) {
-    if (lane_id() == 0) dq_mma_role<HD, CAUSAL>(p, sh, sQ, sdO, sK, sV, sDS, tmem);
+    if (lane_id() == 0) dq_mma_role<HD, CAUSAL>(p, sh, sQ, sdO, sK, sV, tmem);
   } else {
-    dq_softmax_role<HD, CAUSAL>(p, sh, sDS, tmem, warp >> 2);
+    dq_softmax_role<HD, CAUSAL>(p, sh, tmem, warp >> 2);
   }
 
   tc_fence_before_sync();

@@ -271,20 +271,20 @@ __device__ void fwd_mma_role(const FwdLaunch& p, FwdShared& sh, uint8_t* sQ, uin
   auto issue_s = [&](int t, int g) {  // g: running K/V tile index
     const uint32_t qa = q_addr + t * C::TILE_BYTES;
     const uint32_t ka = k_addr + (g % C::KST) * C::TILE_BYTES;
+    const uint64_t qd = make_smem_desc_sw128(qa, 16, 1024), kd = make_smem_desc_sw128(ka, 16, 1024);
 #pragma unroll
     for (int ks = 0; ks < HD / 16; ++ks) {
       const uint32_t off = (ks >> 2) * C::CHUNK_BYTES + (ks & 3) * 32;
-      umma_ss(tmem + C::s_col(t), make_smem_desc_sw128(qa + off, 16, 1024), make_smem_desc_sw128(ka + off, 16, 1024),
-              kIdescS, ks > 0 ? 1u : 0u);
+      umma_ss(tmem + C::s_col(t), desc_add(qd, off), desc_add(kd, off), kIdescS, ks > 0 ? 1u : 0u);
     }
     umma_commit(&sh.s_full[t]);
   };
   auto issue_pv = [&](int t, int g, bool first) {
-    const uint32_t va = v_addr + (g % C::VST) * C::TILE_BYTES;
+    const uint64_t vd = make_smem_desc_sw128(v_addr + (g % C::VST) * C::TILE_BYTES, C::CHUNK_BYTES, 1024);
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks)
-      umma_ts(tmem + C::o_col(t), tmem + C::p_col(t) + ks * 8, make_smem_desc_sw128(va + ks * 2048, C::CHUNK_BYTES, 1024),
-              kIdescPV, (!first || ks > 0) ? 1u : 0u);
+      umma_ts(tmem + C::o_col(t), tmem + C::p_col(t) + ks * 8, desc_add(vd, ks * 2048), kIdescPV,
+              (!first || ks > 0) ? 1u : 0u);
     umma_commit(&sh.pv_done[t]);
   };
   auto fail = [&]() { record_timeout(p.status, &sh.abort_flag, WHERE_FWD_MMA); };

@@ -192,6 +192,12 @@ __device__ __forceinline__ uint64_t make_smem_desc_sw128(uint32_t smem_addr, uin
   return d;
 }
 
+// A descriptor moved `bytes` further along its tile: the start-address field
+// (bits 0-13) holds address >> 4, and every shared address stays below
+// 256 KiB, so the move is one add on the low word with no carry out of the
+// field. Lets an MMA loop build each operand's descriptor once.
+__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
+
 // Instruction descriptor for kind::f16 with bf16 A/B and an fp32 accumulator.
 //   bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format
 //   (1 = bf16), bit 15 A is MN-major, bit 16 B is MN-major, bits 17-22 N >> 3,
