@@ -4,8 +4,9 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
 
 One step is one pass of the whole hot path over one batch of synthetic input:
-fa_fwd, then the backward's three phases (preprocess, main, postprocess), all
-through the C ABI. The default workload is the pages' microbenchmark shape at
+fa_fwd, then the three backward phases fa_bwd runs for this head dimension
+(d = 128: preprocess, dK/dV, per-query-tile dQ; d = 64, 256: preprocess,
+main with atomic dQ, postprocess), all through the C ABI. The default workload is the pages' microbenchmark shape at
 hidden size 2048 with d = 128 and N = 8192 (B = 16384 / N = 2, H = 16),
 non-causal: the configuration the headline "fwd+bwd TFLOP/s" figures are
 quoted on. FLOPs follow the pages' convention: forward 4 B H N^2 d (halved
@@ -14,8 +15,8 @@ when causal), backward 2.5x forward.
 Rank 0 prints one JSON line. `value` is fwd+bwd TFLOP/s over all ranks with
 inputs resident in HBM; `e2e` is the same metric with host->device copies of
 Q, K, V, dO and device->host copies of O, L, dQ, dK, dV inside the timed
-region; `roofline` is the dominant kernel (the backward main kernel) against
-the measured dense bf16 peak; `cpu_baseline` is the float64 CPU oracle timed on
+region; `roofline` is the dominant kernel against the measured dense bf16
+peak, with that kernel's own algorithmic FLOPs; `cpu_baseline` is the float64 CPU oracle timed on
 a bounded sample. `--impl reference` times that oracle alone as the reference
 arm (rank 0 only).
 """
@@ -49,6 +50,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 KERNEL_SOURCES = {
     "fa_bwd_main": ["exact_softmax_attention_fa_gb300/csrc/fa_bwd.cu",
                     "exact_softmax_attention_fa_gb300/csrc/sm103_ptx.cuh"],
+    "fa_bwd_dkdv": ["exact_softmax_attention_fa_gb300/csrc/fa_bwd.cu",
+                    "exact_softmax_attention_fa_gb300/csrc/sm103_ptx.cuh"],
+    "fa_bwd_dq": ["exact_softmax_attention_fa_gb300/csrc/fa_bwd_dq.cu",
+                  "exact_softmax_attention_fa_gb300/csrc/sm103_ptx.cuh"],
     "fa_fwd": ["exact_softmax_attention_fa_gb300/csrc/fa_fwd_kernel.cuh",
                "exact_softmax_attention_fa_gb300/csrc/sm103_ptx.cuh"],
 }
@@ -279,19 +284,26 @@ def run_ours(args, p: dict, name: str, world: int, rank: int, local: int) -> dic
     ws = torch.empty(fa.fa_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
 
+    # The backward phases fa_bwd runs for this head dimension (include/fa.h).
+    if d == 128:
+        bwd_names = ("bwd_pre", "bwd_dkdv", "bwd_dq")
+        bwd_calls = (lambda: fa.fa_bwd_preprocess(o, lse, do, ws, stream),
+                     lambda: fa.fa_bwd_dkdv(q, k, v, do, dk, dv, causal, scale, ws, stream),
+                     lambda: fa.fa_bwd_dq(q, k, v, do, dq, causal, scale, ws, stream))
+    else:
+        bwd_names = ("bwd_pre", "bwd_main", "bwd_post")
+        bwd_calls = (lambda: fa.fa_bwd_preprocess(o, lse, do, ws, stream),
+                     lambda: fa.fa_bwd_main(q, k, v, do, dk, dv, causal, scale, ws, stream),
+                     lambda: fa.fa_bwd_postprocess(dq, ws, stream))
+
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
         fa.fa_fwd(q, k, v, o, lse, causal, scale, stream)
-        if ev is not None:
-            ev[1].record(stream)
-        fa.fa_bwd_preprocess(o, lse, do, ws, stream)
-        if ev is not None:
-            ev[2].record(stream)
-        fa.fa_bwd_main(q, k, v, do, dk, dv, causal, scale, ws, stream)
-        if ev is not None:
-            ev[3].record(stream)
-        fa.fa_bwd_postprocess(dq, ws, stream)
+        for i, call in enumerate(bwd_calls):
+            if ev is not None:
+                ev[1 + i].record(stream)
+            call()
         if ev is not None:
             ev[4].record(stream)
 
@@ -353,11 +365,19 @@ def run_ours(args, p: dict, name: str, world: int, rank: int, local: int) -> dic
     value = aggregate_value(f_step * args.steps, world, max_s)
     fwd_tf = f_fwd / (phase_ms[0] / 1e3) / 1e12
     bwd_tf = f_bwd / (sum(phase_ms[1:]) / 1e3) / 1e12
-    main_tf = f_bwd / (phase_ms[2] / 1e3) / 1e12
     fwd_bwd_tf = f_step / (sum(phase_ms) / 1e3) / 1e12
+    # Per kernel: its phase time and its own algorithmic FLOPs. The backward's
+    # 10 N^2 d (2.5x forward) are its five 128x128xd products per tile pair;
+    # the dK/dV kernel computes four of them (S, dP, dV, dK), the dQ kernel
+    # three (S, dP, dQ).
+    if bwd_names[1] == "bwd_dkdv":
+        kernels = {"fa_fwd": (phase_ms[0], f_fwd), "fa_bwd_dkdv": (phase_ms[2], 0.8 * f_bwd),
+                   "fa_bwd_dq": (phase_ms[3], 0.6 * f_bwd)}
+    else:
+        kernels = {"fa_fwd": (phase_ms[0], f_fwd), "fa_bwd_main": (phase_ms[2], f_bwd)}
     # The dominant kernel (largest share of the step) gets the roofline entry.
-    kernels = {"fa_fwd": (phase_ms[0], f_fwd), "fa_bwd_main": (phase_ms[2], f_bwd)}
-    dom = max(kernels, key=lambda kk: kernels[kk][0])
+    ranked = sorted(kernels, key=lambda kk: -kernels[kk][0])
+    dom = ranked[0]
     dom_ms, dom_flops = kernels[dom]
     achieved = dom_flops / (dom_ms / 1e3) / 1e12
     # Each kernel is timed inside a long back-to-back step: sustained peak.
@@ -365,7 +385,7 @@ def run_ours(args, p: dict, name: str, world: int, rank: int, local: int) -> dic
                 "frac": achieved / sustained, "traffic": profiled_traffic(dom, name),
                 "peak_kind": f"{peak_kind} sustained dense bf16 (MEASURED_PEAKS.json)",
                 "avg_launch_ms": dom_ms}
-    other = "fa_fwd" if dom == "fa_bwd_main" else "fa_bwd_main"
+    other = ranked[1]
     o_ms, o_fl = kernels[other]
     roofline_other = {"bound": "tensor", "kernel": other, "achieved": o_fl / (o_ms / 1e3) / 1e12,
                       "peak": sustained, "unit": UNIT, "frac": o_fl / (o_ms / 1e3) / 1e12 / sustained,
@@ -379,10 +399,12 @@ def run_ours(args, p: dict, name: str, world: int, rank: int, local: int) -> dic
         "config": {"workload": name, "B": B, "H": H, "N": N, "d": d, "causal": causal,
                    "l2": "inputs larger than L2 (Q, K, V, dO and outputs exceed 129 MB per step)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf, "bwd_main_tflops": main_tf, "fwd_bwd_tflops": fwd_bwd_tf,
+        "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf, "fwd_bwd_tflops": fwd_bwd_tf,
+        "kernel_tflops": {kk: fl / (ms / 1e3) / 1e12 for kk, (ms, fl) in kernels.items()},
         "pct_of_peak": {"fwd": fwd_tf / burst, "fwd_bwd": fwd_bwd_tf / burst, "peak_tflops": burst,
                         "peak_kind": f"{peak_kind} burst dense bf16 (MEASURED_PEAKS.json)"},
-        "phase_ms": {"fwd": phase_ms[0], "bwd_pre": phase_ms[1], "bwd_main": phase_ms[2], "bwd_post": phase_ms[3]},
+        "phase_ms": {"fwd": phase_ms[0], bwd_names[0]: phase_ms[1], bwd_names[1]: phase_ms[2],
+                     bwd_names[2]: phase_ms[3]},
         "roofline": roofline, "roofline_secondary": roofline_other,
         "e2e": {"value": aggregate_value(f_step, world, e2e_s), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},

@@ -15,7 +15,7 @@ import math
 
 from ._lib import load, check, FAError, header_functions, STATUS_NAMES  # noqa: F401
 
-__all__ = ["fa_fwd", "fa_bwd", "fa_fwd_gqa", "fa_bwd_gqa", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_size", "fa_bwd_deterministic", "fa_bwd_gqa_deterministic", "fa_bwd_workspace_size", "fa_bwd_gqa_workspace_size", "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_postprocess", "fa_bwd_noalloc", "fa_get_device_status", "fa_set_wait_limit_ns",
+__all__ = ["fa_fwd", "fa_bwd", "fa_fwd_gqa", "fa_bwd_gqa", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_size", "fa_bwd_deterministic", "fa_bwd_gqa_deterministic", "fa_bwd_workspace_size", "fa_bwd_gqa_workspace_size", "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_postprocess", "fa_bwd_dkdv", "fa_bwd_dq", "fa_bwd_noalloc", "fa_get_device_status", "fa_set_wait_limit_ns",
            "fa_debug_timeout_probe", "forward", "backward", "FAError", "flops"]
 
 _SUPPORTED_D = (64, 128, 256)
@@ -215,6 +215,28 @@ def fa_bwd_main(q, k, v, do, dk, dv, causal: bool, scale: float, workspace, stre
     check("fa_bwd_main", load().fa_bwd_main(q.data_ptr(), k.data_ptr(), v.data_ptr(), do.data_ptr(), dk.data_ptr(),
                                             dv.data_ptr(), B, H, N, d, int(bool(causal)), float(scale),
                                             *_ws(workspace), _stream_handle(stream)))
+
+
+def fa_bwd_dkdv(q, k, v, do, dk, dv, causal: bool, scale: float, workspace, stream=None) -> None:
+    """Deterministic backward phase: dk, dv only (after fa_bwd_preprocess)."""
+    shape = _dims(q)
+    for name, t in (("q", q), ("k", k), ("v", v), ("do", do), ("dk", dk), ("dv", dv)):
+        _check_bf16(name, t, shape)
+    B, H, N, d = shape
+    check("fa_bwd_dkdv", load().fa_bwd_dkdv(q.data_ptr(), k.data_ptr(), v.data_ptr(), do.data_ptr(), dk.data_ptr(),
+                                            dv.data_ptr(), B, H, N, d, int(bool(causal)), float(scale),
+                                            *_ws(workspace), _stream_handle(stream)))
+
+
+def fa_bwd_dq(q, k, v, do, dq, causal: bool, scale: float, workspace, stream=None) -> None:
+    """Deterministic backward phase: dq summed per query tile on chip (after fa_bwd_preprocess)."""
+    shape = _dims(q)
+    for name, t in (("q", q), ("k", k), ("v", v), ("do", do), ("dq", dq)):
+        _check_bf16(name, t, shape)
+    B, H, N, d = shape
+    check("fa_bwd_dq", load().fa_bwd_dq(q.data_ptr(), k.data_ptr(), v.data_ptr(), do.data_ptr(), dq.data_ptr(),
+                                        B, H, N, d, int(bool(causal)), float(scale), *_ws(workspace),
+                                        _stream_handle(stream)))
 
 
 def fa_bwd_postprocess(dq, workspace, stream=None) -> None:

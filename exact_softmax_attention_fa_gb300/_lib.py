@@ -47,6 +47,10 @@ _SIGNATURES = {
     "fa_bwd_preprocess": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _vp, ctypes.c_size_t, _vp]),
     "fa_bwd_main": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_float, _vp,
                              ctypes.c_size_t, _vp]),
+    "fa_bwd_dkdv": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_float, _vp,
+                             ctypes.c_size_t, _vp]),
+    "fa_bwd_dq": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_float, _vp,
+                           ctypes.c_size_t, _vp]),
     "fa_bwd_postprocess": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _vp, ctypes.c_size_t, _vp]),
     "fa_bwd_noalloc": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int,
                                 _c_float, _vp]),

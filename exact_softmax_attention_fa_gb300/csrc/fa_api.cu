@@ -450,6 +450,12 @@ fa_status_t fa_bwd_gqa(const void* q, const void* k, const void* v, const void* 
   if (st != FA_OK) return st;
   if (empty) return FA_OK;
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  // d = 128: dQ from the per-query-tile kernel (measured faster than the
+  // atomic accumulation at this head dimension, and reproducible); d = 64,
+  // 256: atomic accumulation in the main kernel.
+  if (d == 128)
+    return fa_bwd_gqa_deterministic(q, k, v, o, lse, dO, dq, dk, dv, B, Hq, Hkv, N, d, causal, scale, workspace,
+                                    workspace_bytes, stream);
   BwdLaunch a;
   st = prepare_bwd(BwdTensors{q, k, v, o, dO, lse, dq, dk, dv}, B, Hq, Hkv, N, d, causal, scale, workspace,
                    workspace_bytes, &empty, &a);
@@ -525,6 +531,39 @@ fa_status_t fa_bwd_main(const void* q, const void* k, const void* v, const void*
                    workspace_bytes, &empty, &a);
   if (st != FA_OK || empty) return st;
   return from_cuda(launch_bwd_main(a, stream));
+}
+
+fa_status_t fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* dO, void* dk, void* dv, int B,
+                        int H, int N, int d, int causal, float scale, void* workspace, size_t workspace_bytes,
+                        cudaStream_t stream) {
+  bool empty = false;
+  fa_status_t st = check_common(B, H, N, d, causal, scale, &empty);
+  if (st != FA_OK) return st;
+  if (d == 256) return FA_ERR_UNSUPPORTED;
+  if (empty) return FA_OK;
+  if (!q || !k || !v || !dO || !dk || !dv) return FA_ERR_INVALID_ARG;
+  BwdLaunch a;
+  st = prepare_bwd(BwdTensors{q, k, v, nullptr, dO, nullptr, nullptr, dk, dv}, B, H, H, N, d, causal, scale,
+                   workspace, workspace_bytes, &empty, &a);
+  if (st != FA_OK || empty) return st;
+  a.deterministic = 1;
+  return from_cuda(launch_bwd_main(a, stream));
+}
+
+fa_status_t fa_bwd_dq(const void* q, const void* k, const void* v, const void* dO, void* dq, int B, int H, int N,
+                      int d, int causal, float scale, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  bool empty = false;
+  fa_status_t st = check_common(B, H, N, d, causal, scale, &empty);
+  if (st != FA_OK) return st;
+  if (d == 256) return FA_ERR_UNSUPPORTED;
+  if (empty) return FA_OK;
+  if (!q || !k || !v || !dO || !dq) return FA_ERR_INVALID_ARG;
+  BwdLaunch a;
+  st = prepare_bwd(BwdTensors{q, k, v, nullptr, dO, nullptr, dq, nullptr, nullptr}, B, H, H, N, d, causal, scale,
+                   workspace, workspace_bytes, &empty, &a);
+  if (st != FA_OK || empty) return st;
+  a.deterministic = 1;
+  return from_cuda(launch_bwd_dq(a, stream));
 }
 
 fa_status_t fa_bwd_postprocess(void* dq, int B, int H, int N, int d, void* workspace, size_t workspace_bytes,

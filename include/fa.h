@@ -127,8 +127,11 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d);
  *   dq, dk, dv : out, bf16 [B][H][N][d]
  *   workspace  : device scratch of at least fa_bwd_workspace_size() bytes,
  *                owned by the caller; its contents on entry do not matter.
- * dQ is accumulated in fp32 with atomic adds across key blocks, so dq is not
- * bitwise reproducible run to run; dk and dv are.
+ * dQ: for d = 64 and 256 it is accumulated in fp32 with atomic adds across
+ * key blocks (the pages' scheme), so dq is not bitwise reproducible run to
+ * run; for d = 128 fa_bwd runs the sequence of fa_bwd_deterministic, which
+ * measured faster at that head dimension, and dq is reproducible. dk and dv
+ * are always reproducible.
  */
 fa_status_t fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
                    void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal, float scale,
@@ -197,6 +200,20 @@ fa_status_t fa_bwd_preprocess(const void* o, const float* lse, const void* dO, i
 fa_status_t fa_bwd_main(const void* q, const void* k, const void* v, const void* dO, void* dk, void* dv, int B,
                         int H, int N, int d, int causal, float scale, void* workspace, size_t workspace_bytes,
                         cudaStream_t stream);
+/*
+ * The phases of the deterministic backward (d = 64, 128; d = 256:
+ * FA_ERR_UNSUPPORTED), run after fa_bwd_preprocess on the same workspace:
+ * fa_bwd_deterministic == preprocess, dkdv, dq.
+ * fa_bwd_dkdv: the block loops of reading note 5.3 without the dQ products:
+ *   writes dk and dv.
+ * fa_bwd_dq: per 128-row query tile, recomputes S, P, dP and dS for every key
+ *   tile it sees and sums dQ on chip in key order; writes dq.
+ */
+fa_status_t fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* dO, void* dk, void* dv, int B,
+                        int H, int N, int d, int causal, float scale, void* workspace, size_t workspace_bytes,
+                        cudaStream_t stream);
+fa_status_t fa_bwd_dq(const void* q, const void* k, const void* v, const void* dO, void* dq, int B, int H, int N,
+                      int d, int causal, float scale, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 fa_status_t fa_bwd_postprocess(void* dq, int B, int H, int N, int d, void* workspace, size_t workspace_bytes,
                                cudaStream_t stream);
 

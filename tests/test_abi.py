@@ -124,6 +124,15 @@ def test_split_key_forward_checks(lib):
     assert lib.fa_fwd_splitkv_workspace_size(1, 2, 64, 64, 300) == 0
 
 
+def test_deterministic_phase_checks(lib):
+    assert lib.fa_bwd_dkdv(P, P, P, P, P, P, 1, 1, 128, 256, 0, 0.125, P, 1 << 30, None) == UNSUPPORTED
+    assert lib.fa_bwd_dq(P, P, P, P, P, 1, 1, 128, 256, 0, 0.125, P, 1 << 30, None) == UNSUPPORTED
+    assert lib.fa_bwd_dkdv(P, P, P, P, 0, P, 1, 1, 128, 64, 0, 0.125, P, 1 << 30, None) == INVALID
+    assert lib.fa_bwd_dq(P, P, P, P, P, 1, 1, 128, 64, 0, 0.125, 0, 0, None) == WORKSPACE
+    assert lib.fa_bwd_dq(P, P, P, P, P, 1, 1, 128, 64, 2, 0.125, P, 1 << 30, None) == INVALID
+    assert lib.fa_bwd_dkdv(0, 0, 0, 0, 0, 0, 1, 1, 0, 64, 0, 0.125, 0, 0, None) == OK
+
+
 def test_grouped_heads_other_checks(lib):
     assert fwd_gqa(lib, d=96) == UNSUPPORTED
     assert bwd_gqa(lib, scale=0.0) == INVALID

@@ -98,3 +98,35 @@ def test_head_dim_256_is_unsupported():
     with pytest.raises(fa.FAError):
         fa.backward(q, k, v, o, lse, do, deterministic=True)
     assert fa.fa_get_device_status() == 0
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_phases_compose_to_the_deterministic_backward(d):
+    import exact_softmax_attention_fa_gb300 as fa
+    import torch
+    x, _ = inputs(1, 3, 700, d, BASE_SEED + 740)
+    q, k, v, do = (to_device(x[n]) for n in ("q", "k", "v", "do"))
+    scale = scale_f32(d)
+    o, lse = fa.forward(q, k, v, causal=True, scale=scale)
+    ws = torch.empty(fa.fa_bwd_workspace_size(1, 3, 700, d), dtype=torch.uint8, device="cuda")
+    a = [torch.empty_like(q) for _ in range(3)]
+    b = [torch.empty_like(q) for _ in range(3)]
+    fa.fa_bwd_deterministic(q, k, v, o, lse, do, *a, True, scale, ws)
+    fa.fa_bwd_preprocess(o, lse, do, ws)
+    fa.fa_bwd_dkdv(q, k, v, do, b[1], b[2], True, scale, ws)
+    fa.fa_bwd_dq(q, k, v, do, b[0], True, scale, ws)
+    assert fa.fa_get_device_status() == 0
+    for t1, t2 in zip(a, b):
+        assert torch.equal(t1, t2)
+
+
+def test_default_backward_at_d128_is_the_deterministic_one():
+    import exact_softmax_attention_fa_gb300 as fa
+    import torch
+    x, _ = inputs(2, 2, 555, 128, BASE_SEED + 750)
+    q, k, v, do = (to_device(x[n]) for n in ("q", "k", "v", "do"))
+    o, lse = fa.forward(q, k, v, causal=False, scale=0.1)
+    a = fa.backward(q, k, v, o, lse, do, causal=False, scale=0.1)
+    b = fa.backward(q, k, v, o, lse, do, causal=False, scale=0.1, deterministic=True)
+    for t1, t2 in zip(a, b):
+        assert torch.equal(t1, t2)
