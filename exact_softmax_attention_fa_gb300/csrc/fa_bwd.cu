@@ -501,24 +501,27 @@ __device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS
     const bool key_valid = wk.j * 128 + r < p.N;
     const bool masked = !key_valid || (CAUSAL && i == wk.j);
     const int c_lo = !key_valid ? 64 : ((CAUSAL && i == wk.j) ? r - 64 * w : 0);
+    // Three passes over the row (exponent arguments, exponentials, bf16
+    // pairs) give the scheduler long runs of independent instructions.
 #pragma unroll
     for (int c4 = 0; c4 < 64; c4 += 4) {
       const float4 l = *reinterpret_cast<const float4*>(ld_l2 + c4);
-      const float lv[4] = {l.x, l.y, l.z, l.w};
-      const float2 x01 = ffma2_bcast_mul(pv[c4], pv[c4 + 1], c2, -lv[0], -lv[1]);
-      const float2 x23 = ffma2_bcast_mul(pv[c4 + 2], pv[c4 + 3], c2, -lv[2], -lv[3]);
-      pv[c4] = ex2_approx(x01.x);
-      pv[c4 + 1] = ex2_approx(x01.y);
-      pv[c4 + 2] = ex2_approx(x23.x);
-      pv[c4 + 3] = ex2_approx(x23.y);
-      if (masked) {
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          if (c4 + u < c_lo) pv[c4 + u] = 0.f;
-      }
-      pk[c4 / 2] = pack_bf16x2(pv[c4], pv[c4 + 1]);
-      pk[c4 / 2 + 1] = pack_bf16x2(pv[c4 + 2], pv[c4 + 3]);
+      const float2 x01 = ffma2_bcast_mul(pv[c4], pv[c4 + 1], c2, -l.x, -l.y);
+      const float2 x23 = ffma2_bcast_mul(pv[c4 + 2], pv[c4 + 3], c2, -l.z, -l.w);
+      pv[c4] = x01.x;
+      pv[c4 + 1] = x01.y;
+      pv[c4 + 2] = x23.x;
+      pv[c4 + 3] = x23.y;
     }
+#pragma unroll
+    for (int c = 0; c < 64; ++c) pv[c] = ex2_approx(pv[c]);
+    if (masked) {
+#pragma unroll
+      for (int c = 0; c < 64; ++c)
+        if (c < c_lo) pv[c] = 0.f;
+    }
+#pragma unroll
+    for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(pv[2 * c], pv[2 * c + 1]);
     tmem_st32(tA, pk);  // columns [64w, 64w + 32): already read
     tmem_st_wait();
     tc_fence_before_sync();

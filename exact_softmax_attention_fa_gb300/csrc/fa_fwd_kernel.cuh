@@ -333,17 +333,13 @@ __device__ void fwd_mma_role(const FwdLaunch& p, FwdShared& sh, uint8_t* sQ, uin
         if (j == 0 && items > 0 && !mbar_wait(&sh.o_free[t], (items - 1) & 1, &sh.abort_flag, lim)) return fail();
         tc_fence_after_sync();
         issue_pv(t, g, j == 0);
-        if (!C::P_ALIAS && has_next && j + 1 <= wk.last_kv[t]) {
+        if (has_next && j + 1 <= wk.last_kv[t]) {
           if (!wait_k_next()) return fail();
-          issue_s(t, gn);
-        }
-      }
-      if (C::P_ALIAS && has_next) {
-#pragma unroll
-        for (int t = 0; t < C::NT; ++t) {
-          if (j + 1 > wk.last_kv[t]) continue;
-          // S_t(j+1) overwrites the TMEM columns P_t(j) is read from.
-          if (!wait_k_next() || !mbar_wait(&sh.pv_done[t], (cnt[t] + j) & 1, &sh.abort_flag, lim)) return fail();
+          // d = 128: S_t(j+1) overwrites the TMEM columns P_t(j) is read
+          // from, so it follows PV_t(j) directly, before the other tile's PV:
+          // tile t's products then run while the other tile is in its
+          // softmax (the two tiles alternate instead of moving in lockstep).
+          if (C::P_ALIAS && !mbar_wait(&sh.pv_done[t], (cnt[t] + j) & 1, &sh.abort_flag, lim)) return fail();
           tc_fence_after_sync();
           issue_s(t, gn);
         }
