@@ -461,6 +461,7 @@ __device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS
   const int T = (p.N + 127) / 128;
   const int total = p.BHkv * p.chunks * T;
   bool alive = true;
+  constexpr bool kPrefetchStats = !DQ && HD == 128;
   // P^T of the current tile as the bf16 pairs written to TMEM, kept from
   // phase A to phase B: dS uses the same rounded P as the dV MMA.
   uint32_t pk[32];
@@ -482,6 +483,16 @@ __device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS
   // stops working but still passes every named barrier, so the warpgroup's
   // barrier counts stay matched.
   auto phase_a = [&](const BwdWork<CAUSAL>& wk, int i, int g) {
+    // The 64 base-2 logsumexps of this warpgroup's queries, read from smem
+    // while S^T is still being computed (read in the loop they sit on the
+    // phase's critical path: measured ~800 of ~1600 cycles at d = 128). Only
+    // where the registers allow it (d = 128 without dQ); elsewhere they are
+    // read in the loop.
+    float4 lv[kPrefetchStats ? 16 : 1];
+    if constexpr (kPrefetchStats) {
+#pragma unroll
+      for (int c = 0; c < 16; ++c) lv[c] = *reinterpret_cast<const float4*>(ld_l2 + 4 * c);
+    }
     wait_all(&sh.s_full, g & 1, WHERE_BWD_SOFTMAX);
     if (!alive) return;
     float pv[64];
@@ -505,7 +516,7 @@ __device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS
     // pairs) give the scheduler long runs of independent instructions.
 #pragma unroll
     for (int c4 = 0; c4 < 64; c4 += 4) {
-      const float4 l = *reinterpret_cast<const float4*>(ld_l2 + c4);
+      const float4 l = kPrefetchStats ? lv[kPrefetchStats ? c4 / 4 : 0] : *reinterpret_cast<const float4*>(ld_l2 + c4);
       const float2 x01 = ffma2_bcast_mul(pv[c4], pv[c4 + 1], c2, -l.x, -l.y);
       const float2 x23 = ffma2_bcast_mul(pv[c4 + 2], pv[c4 + 3], c2, -l.z, -l.w);
       pv[c4] = x01.x;
@@ -530,6 +541,13 @@ __device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS
 
   // ---- phase B: dS^T = P^T o (dP^T - D) * scale -> smem (bf16, swizzled)
   auto phase_b = [&](int g) {
+    // the scaled D values, read from smem while dP^T is still being computed
+    // (as the logsumexps in phase A)
+    float4 dvv[kPrefetchStats ? 16 : 1];
+    if constexpr (kPrefetchStats) {
+#pragma unroll
+      for (int c = 0; c < 16; ++c) dvv[c] = *reinterpret_cast<const float4*>(ld_d + 4 * c);
+    }
     wait_all(&sh.dp_full, g & 1, WHERE_BWD_SOFTMAX);
     if (!alive) return;
 #pragma unroll
@@ -540,7 +558,8 @@ __device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS
       uint32_t dk[16];
 #pragma unroll
       for (int c4 = 0; c4 < 32; c4 += 4) {
-        const float4 dd = *reinterpret_cast<const float4*>(ld_d + 32 * h + c4);
+        const float4 dd = kPrefetchStats ? dvv[kPrefetchStats ? (32 * h + c4) / 4 : 0]
+                                         : *reinterpret_cast<const float4*>(ld_d + 32 * h + c4);
         const float dv4[4] = {dd.x, dd.y, dd.z, dd.w};
         const float2 p01 = unpack_bf16x2(pk[16 * h + c4 / 2]);
         const float2 p23 = unpack_bf16x2(pk[16 * h + c4 / 2 + 1]);
