@@ -44,6 +44,20 @@ cudaError_t launch_timeout_probe(uint32_t* status, uint64_t limit_ns, cudaStream
   return cudaGetLastError();
 }
 
+// Argument checks shared by every entry point (the conventions of fa.h).
+fa_status_t check_common(int B, int H, int N, int d, int causal, float scale, bool* empty) {
+  if (B < 0 || H < 0 || N < 0) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
+  // [BH] is a TMA coordinate (int32) and the tensor byte size must fit.
+  const long long bh = static_cast<long long>(B) * H;
+  if (bh > INT32_MAX) return FA_ERR_INVALID_ARG;
+  if (bh * N > (1ll << 40)) return FA_ERR_INVALID_ARG;
+  *empty = (bh * N == 0);
+  return FA_OK;
+}
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -133,18 +147,6 @@ bool make_map_f32_acc(CUtensorMap* m, void* base, int BH, int Npad, int d) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-fa_status_t check_common(int B, int H, int N, int d, int causal, float scale, bool* empty) {
-  if (B < 0 || H < 0 || N < 0) return FA_ERR_INVALID_ARG;
-  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
-  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
-  if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
-  // [BH] is a TMA coordinate (int32) and the tensor byte size must fit.
-  const long long bh = static_cast<long long>(B) * H;
-  if (bh > INT32_MAX) return FA_ERR_INVALID_ARG;
-  if (bh * N > (1ll << 40)) return FA_ERR_INVALID_ARG;
-  *empty = (bh * N == 0);
-  return FA_OK;
-}
 
 // Grouped K/V heads: Hkv >= 1 dividing Hq (nothing to check when Hq == 0).
 fa_status_t check_heads(int Hq, int Hkv) {

@@ -70,6 +70,10 @@ struct BwdLaunch {
   int num_sms;
 };
 
+// Checks of the sizes, flag and scale common to every entry point; *empty is
+// set when the problem has no rows (fa_api.cu).
+fa_status_t check_common(int B, int H, int N, int d, int causal, float scale, bool* empty);
+
 // Launchers (defined in the kernel translation units). Return cudaSuccess or
 // the launch error.
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t stream);

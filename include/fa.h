@@ -33,7 +33,9 @@
  *   - Device-side failures (a pipeline wait that exceeded its time limit) are
  *     recorded in a per-device status word that fa_get_device_status() reads.
  *   - The library allocates no device memory; it keeps only cached device
- *     attributes in process-wide state. Entry points are thread-safe.
+ *     attributes in process-wide state (plus, once fa_fwd_bwd_host has run
+ *     on a device, two copy streams and ten events for that device).
+ *     Entry points are thread-safe.
  */
 #ifndef FA_GB300_H
 #define FA_GB300_H
@@ -249,6 +251,40 @@ fa_status_t fa_bwd_postprocess(void* dq, int B, int H, int N, int d, void* works
 fa_status_t fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
                            const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal,
                            float scale, cudaStream_t stream);
+
+/*
+ * Forward and backward pass of a problem held in HOST memory (the forward of
+ * reading note 5.1-5.2 and the backward of 5.3, as fa_fwd and fa_bwd), with
+ * the host<->device copies overlapped with the kernels.
+ *   q, k, v, dO     : in,  HOST bf16 [B][H][N][d]
+ *   o               : out, HOST bf16 [B][H][N][d]
+ *   lse             : out, HOST fp32 [B][H][N]
+ *   dq, dk, dv      : out, HOST bf16 [B][H][N][d]
+ *   device_buffer   : DEVICE memory of at least
+ *                     fa_fwd_bwd_host_device_bytes(B, H, N, d) bytes,
+ *                     256-byte aligned, owned by the caller; it receives the
+ *                     device copies and the backward workspace, and its
+ *                     contents are undefined afterwards.
+ * Host buffers may have any alignment. The copies overlap the kernels only
+ * when the host buffers are page-locked (cudaHostAlloc / cudaHostRegister);
+ * pageable buffers give the same results with serialised copies.
+ * The call queues, in order after the work already on `stream`: the uploads of
+ * Q, K, V in four chunks of heads and of dO on a library-owned copy stream;
+ * the forward per chunk as soon as its inputs are on the device; the backward
+ * phases fa_bwd runs for this d; the read-back of O and L after the forward,
+ * of dK and dV after their kernel and of dQ after its kernel, on a second
+ * copy stream. Work queued on `stream` after the call, and a synchronisation
+ * of `stream`, see every output in host memory. Only equal-head problems
+ * (one K/V head per query head).
+ * Errors: those of fa_fwd / fa_bwd, checked before any work is queued;
+ * FA_ERR_WORKSPACE if device_buffer is null or too small, FA_ERR_MISALIGNED
+ * if it is not 256-byte aligned, FA_ERR_CUDA if a copy or an event call
+ * fails (the outputs are then undefined).
+ */
+size_t fa_fwd_bwd_host_device_bytes(int B, int H, int N, int d); /* 0 for invalid or empty problems */
+fa_status_t fa_fwd_bwd_host(const void* q, const void* k, const void* v, const void* dO, void* o, float* lse,
+                            void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal, float scale,
+                            void* device_buffer, size_t device_bytes, cudaStream_t stream);
 
 /* Static, human-readable name of a status code. */
 const char* fa_status_string(fa_status_t status);

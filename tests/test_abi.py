@@ -193,3 +193,27 @@ def test_noalloc_backward_validation(lib):
     # 16 heads x 8192 rows at d=128 need ~68 MB of scratch, beyond the compiled 16 MiB
     assert lib.fa_bwd_workspace_size(1, 16, 8192, 128) > (16 << 20)
     assert call(B=1, H=16, N=8192, d=128) == WORKSPACE
+
+
+def test_host_entry_checks(lib):
+    """fa_fwd_bwd_host: size formula and argument errors (all before any CUDA call)."""
+    def call(ptr=P, lse=P, buf=P, nbytes=1 << 34, B=1, H=2, N=128, d=64, causal=0, scale=0.125):
+        return lib.fa_fwd_bwd_host(ptr, ptr, ptr, ptr, ptr, lse, ptr, ptr, ptr, B, H, N, d, causal, scale, buf,
+                                   nbytes, None)
+    a = lambda n: (n + 255) // 256 * 256
+    for B, H, N, d in ((1, 2, 128, 64), (2, 3, 1000, 128), (1, 1, 1, 256)):
+        rows = B * H * N
+        need = 8 * a(rows * d * 2) + a(rows * 4) + a(lib.fa_bwd_workspace_size(B, H, N, d))
+        assert lib.fa_fwd_bwd_host_device_bytes(B, H, N, d) == need
+    need = lib.fa_fwd_bwd_host_device_bytes(1, 2, 128, 64)
+    assert lib.fa_fwd_bwd_host_device_bytes(1, 2, 0, 64) == 0
+    assert lib.fa_fwd_bwd_host_device_bytes(1, 2, 128, 96) == 0
+    assert call(d=96) == UNSUPPORTED
+    assert call(scale=0.0) == INVALID
+    assert call(causal=3) == INVALID
+    assert call(ptr=0) == INVALID
+    assert call(lse=0) == INVALID
+    assert call(buf=0) == WORKSPACE
+    assert call(nbytes=need - 1) == WORKSPACE
+    assert call(buf=P + 16, nbytes=need) == MISALIGNED
+    assert call(N=0, ptr=0, lse=0, buf=0, nbytes=0) == OK
