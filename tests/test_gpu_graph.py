@@ -1,0 +1,153 @@
+"""CUDA graphs and concurrent callers: the forward + backward step captured
+once into a CUDA graph and replayed on new inputs gives the outputs of eager
+calls, through the device-buffer entry points and through the host-buffer
+entry point (whose library-owned copy streams join the capture through its
+events); and two host threads driving fa_fwd_bwd_host on their own streams
+get the results of serial calls."""
+
+import threading
+
+import numpy as np
+import pytest
+
+from attn_inputs import BASE_SEED
+from gpu_util import inputs, scale_f32, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+def bf16_host(bits, pinned=True):
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+    return t.pin_memory() if pinned else t.clone()
+
+
+@pytest.mark.parametrize("d,causal", [(128, False), (128, True), (64, False)])
+def test_device_step_graph_replay(d, causal):
+    import torch
+    import exact_softmax_attention_fa_gb300 as fa
+    B, H, N = 1, 3, 700
+    scale = scale_f32(d)
+    xs = [inputs(B, H, N, d, BASE_SEED + 1100 + i)[0] for i in range(3)]
+    q, k, v, do = (to_device(xs[0][n]) for n in ("q", "k", "v", "do"))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    ws = torch.empty(fa.fa_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device="cuda")
+
+    def step():
+        fa.fa_fwd(q, k, v, o, lse, causal, scale)
+        fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, causal, scale, ws)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()  # warm-up outside the capture (kernel attributes, tensor maps)
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for x in xs[1:]:
+        for t, n in ((q, "q"), (k, "k"), (v, "v"), (do, "do")):
+            t.copy_(to_device(x[n]))
+        g.replay()
+        torch.cuda.synchronize()
+        assert fa.fa_get_device_status() == 0
+        got = [t.clone() for t in (o, lse, dq, dk, dv)]
+        step()
+        torch.cuda.synchronize()
+        for name, a, b in zip(("o", "lse", "dq", "dk", "dv"), got, (o, lse, dq, dk, dv)):
+            if name == "dq" and d != 128:  # atomic dQ: the order of the adds varies
+                rel = (a.float() - b.float()).abs().max() / b.float().abs().max()
+                assert rel.item() < 1e-2, name
+            else:
+                assert torch.equal(a, b), name
+
+
+def test_host_step_graph_replay():
+    import torch
+    import exact_softmax_attention_fa_gb300 as fa
+    B, H, N, d, causal = 1, 4, 512, 128, True
+    scale = scale_f32(d)
+    xs = [inputs(B, H, N, d, BASE_SEED + 1150 + i)[0] for i in range(3)]
+    hin = {n: bf16_host(xs[0][n]) for n in ("q", "k", "v", "do")}
+    hout = [torch.empty((B, H, N, d), dtype=torch.bfloat16).pin_memory() for _ in range(4)]
+    hlse = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    buf = torch.empty(fa.fa_fwd_bwd_host_device_bytes(B, H, N, d), dtype=torch.uint8, device="cuda")
+
+    def step(outs, lse):
+        fa.fa_fwd_bwd_host(hin["q"], hin["k"], hin["v"], hin["do"], outs[0], lse, outs[1], outs[2], outs[3],
+                           causal, scale, buf)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step(hout, hlse)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step(hout, hlse)
+    for x in xs[1:]:
+        for n in ("q", "k", "v", "do"):
+            hin[n].copy_(bf16_host(x[n], pinned=False))
+        g.replay()
+        torch.cuda.synchronize()
+        assert fa.fa_get_device_status() == 0
+        ref = [torch.empty_like(t) for t in hout]
+        ref_lse = torch.empty_like(hlse)
+        step(ref, ref_lse)
+        torch.cuda.synchronize()
+        for name, a, b in zip(("o", "lse", "dq", "dk", "dv"), (hout[0], hlse, *hout[1:]), (ref[0], ref_lse, *ref[1:])):
+            assert torch.equal(a, b), name
+
+
+def test_host_step_from_two_threads():
+    import torch
+    import exact_softmax_attention_fa_gb300 as fa
+    B, H, N, d = 1, 2, 640, 128
+    scale = scale_f32(d)
+    xs = [inputs(B, H, N, d, BASE_SEED + 1200 + i)[0] for i in range(2)]
+
+    def make(x):
+        ins = [bf16_host(x[n]) for n in ("q", "k", "v", "do")]
+        outs = [torch.empty((B, H, N, d), dtype=torch.bfloat16).pin_memory() for _ in range(4)]
+        lse = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+        buf = torch.empty(fa.fa_fwd_bwd_host_device_bytes(B, H, N, d), dtype=torch.uint8, device="cuda")
+        return ins, outs, lse, buf
+
+    def call(state, stream):
+        ins, outs, lse, buf = state
+        fa.fa_fwd_bwd_host(*ins, outs[0], lse, outs[1], outs[2], outs[3], False, scale, buf, stream)
+
+    # serial reference
+    refs = []
+    for x in xs:
+        st = make(x)
+        call(st, torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        refs.append([t.clone() for t in (st[1][0], st[2], *st[1][1:])])
+    states = [make(x) for x in xs]
+    streams = [torch.cuda.Stream() for _ in xs]
+    errors = []
+
+    def worker(i):
+        try:
+            torch.cuda.set_device(0)
+            for _ in range(5):
+                call(states[i], streams[i])
+            streams[i].synchronize()
+        except Exception as e:  # reported below
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == 0
+    for st, ref in zip(states, refs):
+        for name, a, b in zip(("o", "lse", "dq", "dk", "dv"), (st[1][0], st[2], *st[1][1:]), ref):
+            assert torch.equal(a, b), name
