@@ -4,9 +4,12 @@
 // caller's stream with events, so the copies overlap the kernels:
 //
 //   h2d:    Q,K,V heads chunk 0 | chunk 1 | ... | chunk C-1 | dO
-//   stream:          fwd chunk 0 | fwd chunk 1 | ... | fwd C-1 | D, L2 | dK,dV | dQ
-//   d2h:                                                  O, L | dK, dV   | dQ
+//   stream:          fwd chunk 0 | fwd chunk 1 | ... | fwd C-1 | D, L2 | dK,dV | dQ part 0 | dQ part 1
+//   d2h:                                                  O, L | dK, dV   | dQ part 0 | dQ part 1
 //
+// d = 128: the dQ kernel runs in two launches over the first three quarters
+// and the last quarter of the heads, so only the last quarter of dQ is read
+// back after the last kernel.
 // The forward runs per chunk of heads as soon as that chunk is on the device
 // (rows of different heads are independent problems, and a head's result does
 // not depend on which launch computes it). The backward needs every head's
@@ -25,7 +28,7 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr int kFwdChunks = 4;
 
-enum : int { EV_START, EV_DO, EV_FWD, EV_DKDV, EV_BWD, EV_DONE, EV_IN0, EV_COUNT = EV_IN0 + kFwdChunks };
+enum : int { EV_START, EV_DO, EV_FWD, EV_DKDV, EV_DQ0, EV_BWD, EV_DONE, EV_IN0, EV_COUNT = EV_IN0 + kFwdChunks };
 
 struct CopyState {
   std::once_flag once;
@@ -164,14 +167,26 @@ fa_status_t fa_fwd_bwd_host(const void* q, const void* k, const void* v, const v
   ok(cudaStreamWaitEvent(cs->d2h, cs->ev[EV_DKDV], 0));
   ok(cudaMemcpyAsync(dk, dKd, all_bytes, D2H, cs->d2h));
   ok(cudaMemcpyAsync(dv, dVd, all_bytes, D2H, cs->d2h));
+  long long dq_first = BH;  // heads whose dQ is read back while the rest is computed
   if (d == 128) {
-    run(fa_bwd_dq(Qd, Kd, Vd, dOd, dQd, B, H, N, d, causal, scale, ws, L.ws_bytes, stream));
+    dq_first = BH >= 4 ? BH - (BH + 3) / 4 : BH;
+    run(bwd_dq_heads(Qd, Kd, Vd, dOd, dQd, B, H, N, d, causal, scale, ws, L.ws_bytes, 0, static_cast<int>(dq_first),
+                     stream));
+    if (dq_first < BH) {
+      ok(cudaEventRecord(cs->ev[EV_DQ0], stream));
+      ok(cudaStreamWaitEvent(cs->d2h, cs->ev[EV_DQ0], 0));
+      ok(cudaMemcpyAsync(dq, dQd, dq_first * head_bytes, D2H, cs->d2h));
+      run(bwd_dq_heads(Qd, Kd, Vd, dOd, dQd, B, H, N, d, causal, scale, ws, L.ws_bytes, static_cast<int>(dq_first),
+                       static_cast<int>(BH - dq_first), stream));
+    }
   } else {
     run(fa_bwd_postprocess(dQd, B, H, N, d, ws, L.ws_bytes, stream));
   }
+  const long long dq_rest = d == 128 && dq_first < BH ? dq_first : 0;  // heads already read back
   ok(cudaEventRecord(cs->ev[EV_BWD], stream));
   ok(cudaStreamWaitEvent(cs->d2h, cs->ev[EV_BWD], 0));
-  ok(cudaMemcpyAsync(dq, dQd, all_bytes, D2H, cs->d2h));
+  ok(cudaMemcpyAsync(static_cast<uint8_t*>(dq) + dq_rest * head_bytes, dQd + dq_rest * head_bytes,
+                     (BH - dq_rest) * head_bytes, D2H, cs->d2h));
 
   // Work queued on `stream` after this call sees the outputs in host memory.
   ok(cudaEventRecord(cs->ev[EV_DONE], cs->d2h));

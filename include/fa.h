@@ -34,7 +34,7 @@
  *     recorded in a per-device status word that fa_get_device_status() reads.
  *   - The library allocates no device memory; it keeps only cached device
  *     attributes in process-wide state (plus, once fa_fwd_bwd_host has run
- *     on a device, two copy streams and ten events for that device).
+ *     on a device, two copy streams and eleven events for that device).
  *     Entry points are thread-safe.
  */
 #ifndef FA_GB300_H
@@ -271,9 +271,11 @@ fa_status_t fa_bwd_noalloc(const void* q, const void* k, const void* v, const vo
  * The call queues, in order after the work already on `stream`: the uploads of
  * Q, K, V in four chunks of heads and of dO on a library-owned copy stream;
  * the forward per chunk as soon as its inputs are on the device; the backward
- * phases fa_bwd runs for this d; the read-back of O and L after the forward,
- * of dK and dV after their kernel and of dQ after its kernel, on a second
- * copy stream. Work queued on `stream` after the call, and a synchronisation
+ * phases fa_bwd runs for this d (d = 128: the dQ kernel in two launches, over
+ * the first three quarters and the last quarter of the B*H heads); the
+ * read-back of O and L after the forward, of dK and dV after their kernel
+ * and of each part of dQ after the launch that wrote it, on a second copy
+ * stream. Work queued on `stream` after the call, and a synchronisation
  * of `stream`, see every output in host memory. Only equal-head problems
  * (one K/V head per query head).
  * Errors: those of fa_fwd / fa_bwd, checked before any work is queued;
