@@ -48,6 +48,7 @@ DEFAULT_WORKLOAD = "sweep_d128_N8192_full"
 # non-causal, 16k tokens, hidden 2048): context only, another machine.
 PAGES_FWD_BWD_TFLOPS = {"sweep_d128_N8192_full": 201.0}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+NOMINAL_BF16_TFLOPS = 2250.0  # GB300 datasheet dense bf16 (without 2:4 sparsity), for context
 KERNEL_SOURCES = {
     "fa_bwd_main": ["exact_softmax_attention_fa_gb300/csrc/fa_bwd.cu",
                     "exact_softmax_attention_fa_gb300/csrc/sm103_ptx.cuh"],
@@ -364,6 +365,8 @@ def run_ours(args, p: dict, name: str, world: int, rank: int, local: int) -> dic
     peaks, peak_kind = load_peaks()
     burst, sustained = peaks["bf16_tflops"], peaks["bf16_tflops_sustained"]
     f_fwd, f_bwd, f_step = flops(p, "fwd"), flops(p, "bwd"), flops(p, "fwd_bwd")
+    n_pad = (N + 127) // 128 * 128
+    pre_bytes = B * H * (2 * N * d * 2 + N * 4 + 2 * n_pad * 4 + (0 if bwd_names[1] == "bwd_dkdv" else n_pad * d * 4))
     value = aggregate_value(f_step * args.steps, world, max_s)
     fwd_tf = f_fwd / (phase_ms[0] / 1e3) / 1e12
     bwd_tf = f_bwd / (sum(phase_ms[1:]) / 1e3) / 1e12
@@ -404,10 +407,21 @@ def run_ours(args, p: dict, name: str, world: int, rank: int, local: int) -> dic
         "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf, "fwd_bwd_tflops": fwd_bwd_tf,
         "kernel_tflops": {kk: fl / (ms / 1e3) / 1e12 for kk, (ms, fl) in kernels.items()},
         "pct_of_peak": {"fwd": fwd_tf / burst, "fwd_bwd": fwd_bwd_tf / burst, "peak_tflops": burst,
-                        "peak_kind": f"{peak_kind} burst dense bf16 (MEASURED_PEAKS.json)"},
+                        "peak_kind": f"{peak_kind} burst dense bf16 (MEASURED_PEAKS.json)",
+                        "vs_sustained": {"fwd": fwd_tf / sustained, "fwd_bwd": fwd_bwd_tf / sustained,
+                                         "peak_tflops": sustained},
+                        "vs_nominal": {"fwd": fwd_tf / NOMINAL_BF16_TFLOPS, "fwd_bwd": fwd_bwd_tf / NOMINAL_BF16_TFLOPS,
+                                       "peak_tflops": NOMINAL_BF16_TFLOPS}},
         "phase_ms": {"fwd": phase_ms[0], bwd_names[0]: phase_ms[1], bwd_names[1]: phase_ms[2],
                      bwd_names[2]: phase_ms[3]},
         "roofline": roofline, "roofline_secondary": roofline_other,
+        # The preprocess kernel is HBM-bound: it reads O, dO (bf16) and L,
+        # writes D and the base-2 L (fp32) per padded row, and on the atomic
+        # path zeroes the fp32 dQ accumulator.
+        "roofline_hbm": {"bound": "hbm", "kernel": "bwd_pre", "unit": "GB/s", "peak": peaks["hbm_gbs"],
+                         "achieved": pre_bytes / (phase_ms[1] / 1e3) / 1e9,
+                         "frac": pre_bytes / (phase_ms[1] / 1e3) / 1e9 / peaks["hbm_gbs"],
+                         "bytes": pre_bytes, "avg_launch_ms": phase_ms[1]},
         "e2e": {"value": aggregate_value(f_step, world, e2e_s), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "gpu_launches": 4 * args.steps,
