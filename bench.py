@@ -366,6 +366,8 @@ def run_ours(args, p: dict, name: str, world: int, rank: int, local: int) -> dic
     burst, sustained = peaks["bf16_tflops"], peaks["bf16_tflops_sustained"]
     f_fwd, f_bwd, f_step = flops(p, "fwd"), flops(p, "bwd"), flops(p, "fwd_bwd")
     n_pad = (N + 127) // 128 * 128
+    clock_mhz = clk.get("sm_mhz") or clk.get("sm_max_mhz") or 2070.0
+    num_sms = torch.cuda.get_device_properties(device).multi_processor_count
     pre_bytes = B * H * (2 * N * d * 2 + N * 4 + 2 * n_pad * 4 + (0 if bwd_names[1] == "bwd_dkdv" else n_pad * d * 4))
     value = aggregate_value(f_step * args.steps, world, max_s)
     fwd_tf = f_fwd / (phase_ms[0] / 1e3) / 1e12
@@ -418,6 +420,13 @@ def run_ours(args, p: dict, name: str, world: int, rank: int, local: int) -> dic
         # The preprocess kernel is HBM-bound: it reads O, dO (bf16) and L,
         # writes D and the base-2 L (fp32) per padded row, and on the atomic
         # path zeroes the fp32 dQ accumulator.
+        # The forward's second bound: one 2^x per score on the special-function
+        # unit, measured at 4 cycles per warp instruction per sub-partition
+        # (32 results per clock per SM) on this GPU; peak at the sampled clock.
+        "roofline_exp": {"bound": "alu", "kernel": "fa_fwd", "unit": "Gexp/s",
+                         "achieved": f_fwd / (4 * d) / (phase_ms[0] / 1e3) / 1e9,
+                         "peak": 32 * num_sms * clock_mhz * 1e6 / 1e9,
+                         "frac": (f_fwd / (4 * d) / (phase_ms[0] / 1e3)) / (32 * num_sms * clock_mhz * 1e6)},
         "roofline_hbm": {"bound": "hbm", "kernel": "bwd_pre", "unit": "GB/s", "peak": peaks["hbm_gbs"],
                          "achieved": pre_bytes / (phase_ms[1] / 1e3) / 1e9,
                          "frac": pre_bytes / (phase_ms[1] / 1e3) / 1e9 / peaks["hbm_gbs"],
