@@ -113,7 +113,7 @@ def profiled_traffic(kernel: str, workload: str):
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,power.limit")
     REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
     def __init__(self, gpu_index: int):
@@ -143,7 +143,7 @@ class ClockSampler:
         rows = [r.split(",") for r in self.out.read().strip().splitlines() if r.strip()]
         self.out.close()
         os.unlink(self.out.name)
-        sm, mx, reasons = [], [], set()
+        sm, mx, pw, lim, reasons = [], [], [], [], set()
         for r in rows:
             r = [x.strip() for x in r]
             if len(r) < 9:
@@ -153,11 +153,17 @@ class ClockSampler:
                 mx.append(float(r[2]))
             except ValueError:
                 continue
+            for lst, idx in ((pw, 3), (lim, 9)):
+                try:
+                    lst.append(float(r[idx]))
+                except (ValueError, IndexError):
+                    pass
             for name, val in zip(self.REASONS, r[5:9]):
                 if val.lower().startswith("active"):
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w": statistics.median(pw) if pw else None, "power_limit_w": max(lim) if lim else None}
 
 
 # ---------------------------------------------------------------------------
