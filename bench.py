@@ -362,6 +362,24 @@ def run_ours(args, p: dict, name: str, world: int, rank: int, local: int) -> dic
     e1.record(stream)
     torch.cuda.synchronize(device)
     e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3 / e2e_steps, device if world > 1 else None)
+    # The forward alone through fa_fwd_host (inference callers): Q, K, V up,
+    # O and L back, pipelined over head chunks.
+    fwd_buf = torch.empty(fa.fa_fwd_host_device_bytes(B, H, N, d), dtype=torch.uint8, device=device)
+
+    def e2e_fwd_step():
+        fa.fa_fwd_host(pinned["q"], pinned["k"], pinned["v"], out_host["o"], out_host["lse"], causal, scale, fwd_buf,
+                       stream)
+
+    for _ in range(2):
+        e2e_fwd_step()
+    torch.cuda.synchronize(device)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_fwd_step()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    e2e_fwd_s = max_over_ranks(e0.elapsed_time(e1) / 1e3 / e2e_steps, device if world > 1 else None)
+    del fwd_buf
     h2d = sum(t.numel() * t.element_size() for t in (q, k, v, do))
     d2h = sum(t.numel() * t.element_size() for t in (o, lse, dq, dk, dv))
 
@@ -439,6 +457,10 @@ def run_ours(args, p: dict, name: str, world: int, rank: int, local: int) -> dic
                          "bytes": pre_bytes, "avg_launch_ms": phase_ms[1]},
         "e2e": {"value": aggregate_value(f_step, world, e2e_s), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "e2e_fwd": {"value": aggregate_value(f_fwd, world, e2e_fwd_s), "unit": UNIT,
+                    "h2d_bytes_per_step": 3 * q.numel() * q.element_size(),
+                    "d2h_bytes_per_step": o.numel() * o.element_size() + lse.numel() * lse.element_size(),
+                    "steps": e2e_steps, "entry": "fa_fwd_host"},
         "gpu_launches": 4 * args.steps,
         "clocks": clk,
     }

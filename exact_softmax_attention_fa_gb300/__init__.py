@@ -15,7 +15,7 @@ import math
 
 from ._lib import load, check, FAError, header_functions, STATUS_NAMES  # noqa: F401
 
-__all__ = ["fa_fwd", "fa_bwd", "fa_fwd_gqa", "fa_bwd_gqa", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_size", "fa_bwd_deterministic", "fa_bwd_gqa_deterministic", "fa_bwd_workspace_size", "fa_bwd_gqa_workspace_size", "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_postprocess", "fa_bwd_dkdv", "fa_bwd_dq", "fa_bwd_noalloc", "fa_fwd_bwd_host", "fa_fwd_bwd_host_device_bytes", "fa_get_device_status", "fa_set_wait_limit_ns",
+__all__ = ["fa_fwd", "fa_bwd", "fa_fwd_gqa", "fa_bwd_gqa", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_size", "fa_bwd_deterministic", "fa_bwd_gqa_deterministic", "fa_bwd_workspace_size", "fa_bwd_gqa_workspace_size", "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_postprocess", "fa_bwd_dkdv", "fa_bwd_dq", "fa_bwd_noalloc", "fa_fwd_bwd_host", "fa_fwd_bwd_host_device_bytes", "fa_fwd_host", "fa_fwd_host_device_bytes", "fa_get_device_status", "fa_set_wait_limit_ns",
            "fa_debug_timeout_probe", "forward", "backward", "FAError", "flops"]
 
 _SUPPORTED_D = (64, 128, 256)
@@ -304,6 +304,31 @@ def fa_fwd_bwd_host(q, k, v, do, o, lse, dq, dk, dv, causal: bool, scale: float,
         q.data_ptr(), k.data_ptr(), v.data_ptr(), do.data_ptr(), o.data_ptr(), lse.data_ptr(), dq.data_ptr(),
         dk.data_ptr(), dv.data_ptr(), B, H, N, d, int(bool(causal)), float(scale), device_buffer.data_ptr(),
         device_buffer.numel(), _stream_handle(stream)))
+
+
+def fa_fwd_host_device_bytes(B: int, H: int, N: int, d: int) -> int:
+    """Device buffer size fa_fwd_host needs (0 for invalid or empty problems)."""
+    return int(load().fa_fwd_host_device_bytes(B, H, N, d))
+
+
+def fa_fwd_host(q, k, v, o, lse, causal: bool, scale: float, device_buffer, stream=None) -> None:
+    """fa_fwd_host of the C ABI: the forward of CPU tensors, pipelined over head chunks.
+
+    q, k, v (in) and o (out) are contiguous bf16 CPU tensors [B, H, N, d], lse
+    a float32 CPU tensor [B, H, N]; device_buffer a CUDA uint8 tensor of at
+    least fa_fwd_host_device_bytes(B, H, N, d) bytes. Asynchronous on `stream`.
+    """
+    import torch
+    shape = _dims(q)
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o)):
+        _check_host(name, t, shape, torch.bfloat16)
+    _check_host("lse", lse, shape[:3], torch.float32)
+    if not device_buffer.is_cuda or device_buffer.dtype != torch.uint8:
+        raise ValueError("device_buffer must be a CUDA uint8 tensor")
+    B, H, N, d = shape
+    check("fa_fwd_host", load().fa_fwd_host(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d, int(bool(causal)),
+        float(scale), device_buffer.data_ptr(), device_buffer.numel(), _stream_handle(stream)))
 
 
 def fa_get_device_status(stream=None) -> int:

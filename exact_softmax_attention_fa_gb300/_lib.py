@@ -55,6 +55,9 @@ _SIGNATURES = {
     "fa_bwd_noalloc": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int,
                                 _c_float, _vp]),
     "fa_fwd_bwd_host_device_bytes": (ctypes.c_size_t, [_c_int, _c_int, _c_int, _c_int]),
+    "fa_fwd_host_device_bytes": (ctypes.c_size_t, [_c_int, _c_int, _c_int, _c_int]),
+    "fa_fwd_host": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_float, _vp,
+                             ctypes.c_size_t, _vp]),
     "fa_fwd_bwd_host": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
                                  _c_int, _c_float, _vp, ctypes.c_size_t, _vp]),
     "fa_status_string": (ctypes.c_char_p, [_c_int]),

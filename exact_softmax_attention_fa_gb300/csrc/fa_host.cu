@@ -30,11 +30,14 @@ constexpr int kFwdChunks = 4;
 
 enum : int { EV_START, EV_DO, EV_FWD, EV_DKDV, EV_DQ0, EV_BWD, EV_DONE, EV_IN0, EV_COUNT = EV_IN0 + kFwdChunks };
 
+constexpr int kFwdOnlyChunks = 8;  // fa_fwd_host: uploads, forwards and read-backs pipelined over 8 head chunks
+
 struct CopyState {
   std::once_flag once;
   cudaError_t error = cudaSuccess;
   cudaStream_t h2d = nullptr, d2h = nullptr;
   cudaEvent_t ev[EV_COUNT] = {};
+  cudaEvent_t fwd_in[kFwdOnlyChunks] = {}, fwd_out[kFwdOnlyChunks] = {};
   std::mutex mu;  // one call at a time per device enqueues on the shared streams and events
 };
 CopyState g_copy[kMaxDevices];
@@ -45,6 +48,10 @@ CopyState* copy_state(int dev) {
     cudaError_t e = cudaStreamCreateWithFlags(&cs.h2d, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&cs.d2h, cudaStreamNonBlocking);
     for (int i = 0; i < EV_COUNT && e == cudaSuccess; ++i) e = cudaEventCreateWithFlags(&cs.ev[i], cudaEventDisableTiming);
+    for (int i = 0; i < kFwdOnlyChunks && e == cudaSuccess; ++i) {
+      e = cudaEventCreateWithFlags(&cs.fwd_in[i], cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&cs.fwd_out[i], cudaEventDisableTiming);
+    }
     cs.error = e;
   });
   return cs.error == cudaSuccess ? &cs : nullptr;
@@ -75,10 +82,97 @@ HostLayout host_layout(int B, int H, int N, int d) {
   return L;
 }
 
+// fa_fwd_host's device buffer: q, k, v, o (bf16), lse (fp32).
+struct FwdHostLayout {
+  size_t q, k, v, o, lse, total;
+};
+
+FwdHostLayout fwd_host_layout(int B, int H, int N, int d) {
+  FwdHostLayout L{};
+  const size_t rows = static_cast<size_t>(B) * H * N;
+  const size_t tb = align256(rows * d * 2);
+  L.q = 0;
+  L.k = tb;
+  L.v = 2 * tb;
+  L.o = 3 * tb;
+  L.lse = 4 * tb;
+  L.total = 4 * tb + align256(rows * 4);
+  return L;
+}
+
 }  // namespace
 }  // namespace fa
 
 extern "C" {
+
+size_t fa_fwd_host_device_bytes(int B, int H, int N, int d) {
+  bool empty = false;
+  if (fa::check_common(B, H, N, d, 0, 1.0f, &empty) != FA_OK || empty) return 0;
+  return fa::fwd_host_layout(B, H, N, d).total;
+}
+
+// Forward of host tensors, pipelined over chunks of heads: chunk c uploads
+// while chunk c - 1 computes and chunk c - 2 is read back.
+fa_status_t fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                        int causal, float scale, void* device_buffer, size_t device_bytes, cudaStream_t stream) {
+  using namespace fa;
+  bool empty = false;
+  fa_status_t st = check_common(B, H, N, d, causal, scale, &empty);
+  if (st != FA_OK) return st;
+  if (empty) return FA_OK;
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  const FwdHostLayout L = fwd_host_layout(B, H, N, d);
+  if (!device_buffer || device_bytes < L.total) return FA_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(device_buffer) % 256 != 0) return FA_ERR_MISALIGNED;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+  CopyState* cs = copy_state(dev);
+  if (!cs) return FA_ERR_CUDA;
+
+  uint8_t* base = static_cast<uint8_t*>(device_buffer);
+  uint8_t *Qd = base + L.q, *Kd = base + L.k, *Vd = base + L.v, *Od = base + L.o;
+  float* Ld = reinterpret_cast<float*>(base + L.lse);
+  const long long BH = static_cast<long long>(B) * H;
+  const size_t head_bytes = static_cast<size_t>(N) * d * 2, head_lse = static_cast<size_t>(N) * 4;
+  const auto* hq = static_cast<const uint8_t*>(q);
+  const auto* hk = static_cast<const uint8_t*>(k);
+  const auto* hv = static_cast<const uint8_t*>(v);
+  auto* ho = static_cast<uint8_t*>(o);
+  auto* hl = reinterpret_cast<uint8_t*>(lse);
+
+  std::lock_guard<std::mutex> lock(cs->mu);
+  cudaError_t e = cudaSuccess;
+  auto ok = [&e](cudaError_t x) {
+    if (e == cudaSuccess) e = x;
+  };
+  ok(cudaEventRecord(cs->ev[EV_START], stream));
+  ok(cudaStreamWaitEvent(cs->h2d, cs->ev[EV_START], 0));
+  const int chunks = static_cast<int>(std::min<long long>(kFwdOnlyChunks, BH));
+  for (int c = 0; c < chunks; ++c) {
+    const long long h0 = BH * c / chunks, h1 = BH * (c + 1) / chunks;
+    const size_t off = h0 * head_bytes, n = (h1 - h0) * head_bytes;
+    ok(cudaMemcpyAsync(Qd + off, hq + off, n, cudaMemcpyHostToDevice, cs->h2d));
+    ok(cudaMemcpyAsync(Kd + off, hk + off, n, cudaMemcpyHostToDevice, cs->h2d));
+    ok(cudaMemcpyAsync(Vd + off, hv + off, n, cudaMemcpyHostToDevice, cs->h2d));
+    ok(cudaEventRecord(cs->fwd_in[c], cs->h2d));
+  }
+  for (int c = 0; c < chunks; ++c) {
+    const long long h0 = BH * c / chunks, h1 = BH * (c + 1) / chunks;
+    const size_t off = h0 * head_bytes, n = (h1 - h0) * head_bytes;
+    ok(cudaStreamWaitEvent(stream, cs->fwd_in[c], 0));
+    if (st == FA_OK && e == cudaSuccess)
+      st = fa_fwd(Qd + off, Kd + off, Vd + off, Od + off, Ld + h0 * N, 1, static_cast<int>(h1 - h0), N, d, causal,
+                  scale, stream);
+    ok(cudaEventRecord(cs->fwd_out[c], stream));
+    ok(cudaStreamWaitEvent(cs->d2h, cs->fwd_out[c], 0));
+    ok(cudaMemcpyAsync(ho + off, Od + off, n, cudaMemcpyDeviceToHost, cs->d2h));
+    ok(cudaMemcpyAsync(hl + h0 * head_lse, Ld + h0 * N, (h1 - h0) * head_lse, cudaMemcpyDeviceToHost, cs->d2h));
+  }
+  ok(cudaEventRecord(cs->ev[EV_DONE], cs->d2h));
+  ok(cudaStreamWaitEvent(stream, cs->ev[EV_DONE], 0));
+  if (st != FA_OK) return st;
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
 
 size_t fa_fwd_bwd_host_device_bytes(int B, int H, int N, int d) {
   bool empty = false;

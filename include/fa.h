@@ -33,9 +33,9 @@
  *   - Device-side failures (a pipeline wait that exceeded its time limit) are
  *     recorded in a per-device status word that fa_get_device_status() reads.
  *   - The library allocates no device memory; it keeps only cached device
- *     attributes in process-wide state (plus, once fa_fwd_bwd_host has run
- *     on a device, two copy streams and eleven events for that device).
- *     Entry points are thread-safe.
+ *     attributes in process-wide state (plus, once fa_fwd_bwd_host or
+ *     fa_fwd_host has run on a device, two copy streams and 27 events for
+ *     that device). Entry points are thread-safe.
  */
 #ifndef FA_GB300_H
 #define FA_GB300_H
@@ -287,6 +287,22 @@ size_t fa_fwd_bwd_host_device_bytes(int B, int H, int N, int d); /* 0 for invali
 fa_status_t fa_fwd_bwd_host(const void* q, const void* k, const void* v, const void* dO, void* o, float* lse,
                             void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal, float scale,
                             void* device_buffer, size_t device_bytes, cudaStream_t stream);
+
+/*
+ * Forward pass of a problem held in HOST memory (as fa_fwd), pipelined over
+ * eight chunks of heads: while chunk c is on the tensor cores, chunk c + 1
+ * uploads and chunk c - 1 is read back.
+ *   q, k, v         : in,  HOST bf16 [B][H][N][d]
+ *   o               : out, HOST bf16 [B][H][N][d]
+ *   lse             : out, HOST fp32 [B][H][N]
+ *   device_buffer   : DEVICE memory of at least
+ *                     fa_fwd_host_device_bytes(B, H, N, d) bytes, 256-byte
+ *                     aligned, owned by the caller (undefined afterwards).
+ * Host buffers, streams, ordering and errors as for fa_fwd_bwd_host.
+ */
+size_t fa_fwd_host_device_bytes(int B, int H, int N, int d); /* 0 for invalid or empty problems */
+fa_status_t fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                        int causal, float scale, void* device_buffer, size_t device_bytes, cudaStream_t stream);
 
 /* Static, human-readable name of a status code. */
 const char* fa_status_string(fa_status_t status);

@@ -217,3 +217,23 @@ def test_host_entry_checks(lib):
     assert call(nbytes=need - 1) == WORKSPACE
     assert call(buf=P + 16, nbytes=need) == MISALIGNED
     assert call(N=0, ptr=0, lse=0, buf=0, nbytes=0) == OK
+
+
+def test_forward_host_entry_checks(lib):
+    """fa_fwd_host: size formula and argument errors (all before any CUDA call)."""
+    def call(ptr=P, lse=P, buf=P, nbytes=1 << 34, B=1, H=2, N=128, d=64, causal=0, scale=0.125):
+        return lib.fa_fwd_host(ptr, ptr, ptr, ptr, lse, B, H, N, d, causal, scale, buf, nbytes, None)
+    a = lambda n: (n + 255) // 256 * 256
+    for B, H, N, d in ((1, 2, 128, 64), (2, 3, 1000, 128), (1, 1, 1, 256)):
+        rows = B * H * N
+        assert lib.fa_fwd_host_device_bytes(B, H, N, d) == 4 * a(rows * d * 2) + a(rows * 4)
+    need = lib.fa_fwd_host_device_bytes(1, 2, 128, 64)
+    assert lib.fa_fwd_host_device_bytes(0, 2, 128, 64) == 0
+    assert call(d=32) == UNSUPPORTED
+    assert call(scale=float("nan")) == INVALID
+    assert call(ptr=0) == INVALID
+    assert call(lse=0) == INVALID
+    assert call(buf=0) == WORKSPACE
+    assert call(nbytes=need - 1) == WORKSPACE
+    assert call(buf=P + 64, nbytes=need) == MISALIGNED
+    assert call(H=0, ptr=0, lse=0, buf=0, nbytes=0) == OK

@@ -151,3 +151,38 @@ def test_host_step_from_two_threads():
     for st, ref in zip(states, refs):
         for name, a, b in zip(("o", "lse", "dq", "dk", "dv"), (st[1][0], st[2], *st[1][1:]), ref):
             assert torch.equal(a, b), name
+
+
+def test_forward_host_graph_replay():
+    import torch
+    import exact_softmax_attention_fa_gb300 as fa
+    B, H, N, d, causal = 2, 5, 384, 128, False
+    scale = scale_f32(d)
+    xs = [inputs(B, H, N, d, BASE_SEED + 1250 + i)[0] for i in range(3)]
+    hin = {n: bf16_host(xs[0][n]) for n in ("q", "k", "v")}
+    ho = torch.empty((B, H, N, d), dtype=torch.bfloat16).pin_memory()
+    hl = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    buf = torch.empty(fa.fa_fwd_host_device_bytes(B, H, N, d), dtype=torch.uint8, device="cuda")
+
+    def step(o, lse):
+        fa.fa_fwd_host(hin["q"], hin["k"], hin["v"], o, lse, causal, scale, buf)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step(ho, hl)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step(ho, hl)
+    for x in xs[1:]:
+        for n in ("q", "k", "v"):
+            hin[n].copy_(bf16_host(x[n], pinned=False))
+        g.replay()
+        torch.cuda.synchronize()
+        assert fa.fa_get_device_status() == 0
+        ro, rl = torch.empty_like(ho), torch.empty_like(hl)
+        step(ro, rl)
+        torch.cuda.synchronize()
+        assert torch.equal(ho, ro) and torch.equal(hl, rl)

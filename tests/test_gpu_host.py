@@ -106,3 +106,26 @@ def test_host_entry_back_to_back_calls_reuse_the_buffer():
         want = run_device(x, False, scale)
         for name, s, t in zip(("o", "lse", "dq", "dk", "dv"), got, want):
             assert torch.equal(s, t), name
+
+
+@pytest.mark.parametrize("B,H,N,d,causal", [(1, 3, 1000, 128, False), (2, 5, 640, 128, True), (1, 9, 300, 64, True),
+                                            (1, 2, 257, 256, False), (1, 1, 65, 64, False)])
+def test_forward_host_entry_matches_device_path(B, H, N, d, causal):
+    """fa_fwd_host (8 head chunks; fewer when B*H < 8) equals fa_fwd bit for bit."""
+    import torch
+    import exact_softmax_attention_fa_gb300 as fa
+    x, f = inputs(B, H, N, d, BASE_SEED + 1300 + N + d)
+    scale = scale_f32(d)
+    hq, hk, hv = (host_bf16(x[n], True) for n in ("q", "k", "v"))
+    o = torch.full((B, H, N, d), float("nan"), dtype=torch.bfloat16).pin_memory()
+    lse = torch.full((B, H, N), float("nan"), dtype=torch.float32).pin_memory()
+    buf = torch.empty(fa.fa_fwd_host_device_bytes(B, H, N, d), dtype=torch.uint8, device="cuda")
+    fa.fa_fwd_host(hq, hk, hv, o, lse, causal, scale, buf)
+    assert fa.fa_get_device_status() == 0
+    q, k, v = (to_device(x[n]) for n in ("q", "k", "v"))
+    od, ld = fa.forward(q, k, v, causal=causal, scale=scale)
+    assert torch.equal(o, od.cpu())
+    assert torch.equal(lse, ld.cpu())
+    ref_o, ref_l = oracle.attention_forward(f["q"], f["k"], f["v"], causal, scale)
+    assert np.abs(to_host64(o) - ref_o).max() <= TOL_O
+    assert np.abs(lse.double().numpy() - ref_l).max() <= TOL_LSE
