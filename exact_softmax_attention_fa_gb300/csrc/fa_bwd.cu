@@ -10,7 +10,8 @@
 //   note 5.4), dK_j += dS^T Q_i.
 //
 // GB300 mapping (our design):
-//   Three kernels on the caller's stream:
+//   Three kernels on the caller's stream (the deterministic backward runs
+//   the first, the second without dQ, and the dQ kernel of fa_bwd_dq.cu):
 //   1. bwd_pre_kernel (HBM-bound): D from the stored bf16 O and dO, the
 //      base-2 logsumexp L*log2(e), and zeroes the fp32 dQ accumulator. Every
 //      head is padded to a multiple of 128 rows; padding rows get D = 0 and
@@ -30,11 +31,15 @@
 //          drain it into the fp32 accumulator with reductions (d = 128:
 //          scalar reductions that cover whole 128-byte lines; d = 64: TMA
 //          reduce-adds of a swizzled smem staging tile).
-//      Two 128-column TMEM regions alternate: S^T(i) and then P^T(i) use
-//      one, dP^T(i) and then dQ_i the other; S^T(i+1) reuses the P^T region
-//      once dV(i) is done and dP^T(i+1) reuses the dQ region once it was
-//      drained. dK, dV (fp32, TMEM) are written once per item, straight from
-//      TMEM to global memory, while the MMA warp starts the next item.
+//      Two 128-column TMEM regions with fixed roles: region 0 holds S^T(i)
+//      and then P^T(i), region 1 dP^T(i) and then dQ_i; S^T(i+1) reuses
+//      region 0 once dV(i) is done and dP^T(i+1) reuses region 1 once dQ_i
+//      was drained. dK, dV (fp32, TMEM) are written once per item, straight
+//      from TMEM to global memory (or, when a group's query heads are split
+//      into chunks, as fp32 partials that bwd_kv_sum_kernel adds in chunk
+//      order), while the MMA warp starts the next item.
+//      The DQ = false instantiation skips the dQ product and drain: the
+//      deterministic backward (fa_bwd at d = 128) forms dQ in fa_bwd_dq.cu.
 //   3. bwd_post_kernel (HBM-bound): dQ = bf16(accumulator).
 //
 // TMEM columns (512 allocated): dK [0, d), dV [d, 2d), region 0 [256, 384),
