@@ -440,28 +440,6 @@ fa_status_t prepare_bwd(const BwdTensors& t, int B, int H, int Hkv, int N, int d
 
 }  // namespace
 
-// The dQ kernel over a range of query heads; fa_bwd_dq runs it over all of
-// them, the host-buffer entry point in two parts.
-fa_status_t fa::bwd_dq_heads(const void* q, const void* k, const void* v, const void* dO, void* dq, int B, int H,
-                             int N, int d, int causal, float scale, void* workspace, size_t workspace_bytes, int bh0,
-                             int nbh, cudaStream_t stream) {
-  bool empty = false;
-  fa_status_t st = check_common(B, H, N, d, causal, scale, &empty);
-  if (st != FA_OK) return st;
-  if (d == 256) return FA_ERR_UNSUPPORTED;
-  if (empty) return FA_OK;
-  if (!q || !k || !v || !dO || !dq) return FA_ERR_INVALID_ARG;
-  if (bh0 < 0 || nbh < 1 || static_cast<long long>(bh0) + nbh > static_cast<long long>(B) * H) return FA_ERR_INVALID_ARG;
-  BwdLaunch a;
-  st = prepare_bwd(BwdTensors{q, k, v, nullptr, dO, nullptr, dq, nullptr, nullptr}, B, H, H, N, d, causal, scale,
-                   workspace, workspace_bytes, &empty, &a);
-  if (st != FA_OK || empty) return st;
-  a.deterministic = 1;
-  a.dq_bh0 = bh0;
-  a.BH = nbh;
-  return from_cuda(launch_bwd_dq(a, stream));
-}
-
 extern "C" {
 
 fa_status_t fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -576,9 +554,18 @@ fa_status_t fa_bwd_dkdv(const void* q, const void* k, const void* v, const void*
 
 fa_status_t fa_bwd_dq(const void* q, const void* k, const void* v, const void* dO, void* dq, int B, int H, int N,
                       int d, int causal, float scale, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
-  const long long bh = static_cast<long long>(B) * H;
-  return fa::bwd_dq_heads(q, k, v, dO, dq, B, H, N, d, causal, scale, workspace, workspace_bytes, 0,
-                          bh > INT32_MAX || bh < 0 ? -1 : static_cast<int>(bh), stream);
+  bool empty = false;
+  fa_status_t st = check_common(B, H, N, d, causal, scale, &empty);
+  if (st != FA_OK) return st;
+  if (d == 256) return FA_ERR_UNSUPPORTED;
+  if (empty) return FA_OK;
+  if (!q || !k || !v || !dO || !dq) return FA_ERR_INVALID_ARG;
+  BwdLaunch a;
+  st = prepare_bwd(BwdTensors{q, k, v, nullptr, dO, nullptr, dq, nullptr, nullptr}, B, H, H, N, d, causal, scale,
+                   workspace, workspace_bytes, &empty, &a);
+  if (st != FA_OK || empty) return st;
+  a.deterministic = 1;
+  return from_cuda(launch_bwd_dq(a, stream));
 }
 
 fa_status_t fa_bwd_postprocess(void* dq, int B, int H, int N, int d, void* workspace, size_t workspace_bytes,

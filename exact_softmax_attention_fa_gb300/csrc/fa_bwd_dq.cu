@@ -76,7 +76,7 @@ struct DqShared {
 template <bool CAUSAL>
 struct DqWork {
   int bh, i, nkv;
-  __device__ DqWork(int item, int BH, int N, int bh0) {
+  __device__ DqWork(int item, int BH, int N) {
     const int T = (N + 127) / 128;
     if (CAUSAL) {
       i = T - 1 - item / BH;
@@ -87,7 +87,6 @@ struct DqWork {
       i = item % T;
       nkv = T;
     }
-    bh += bh0;
   }
 };
 
@@ -128,7 +127,7 @@ __device__ void dq_load_role(const BwdLaunch& p, DqShared& sh, uint8_t* sQ, uint
       break;
     }
     if (item >= total) break;
-    const DqWork<CAUSAL> wk(item, p.BH, p.N, p.dq_bh0);
+    const DqWork<CAUSAL> wk(item, p.BH, p.N);
     const int kvh = wk.bh / p.group;  // grouped K/V heads
     // The first K/V tile loads while the previous item still reads Q_i, dO_i.
     if (!load_kv(0, kvh) || (u > 0 && !mbar_wait(&sh.q_free, (u - 1) & 1, &sh.abort_flag, lim))) {
@@ -214,7 +213,7 @@ __device__ void dq_mma_role(const BwdLaunch& p, DqShared& sh, uint8_t* sQ, uint8
     const int item = take_item(sh, u, lim);
     if (item < 0) return fail();
     if (item >= total) break;
-    const DqWork<CAUSAL> wk(item, p.BH, p.N, p.dq_bh0);
+    const DqWork<CAUSAL> wk(item, p.BH, p.N);
     if (!mbar_wait(&sh.q_full, u & 1, &sh.abort_flag, lim) || !issue_s(t, kv, t - 1) || !issue_dp(t, kv))
       return fail();
     if (wk.nkv == 1) umma_commit(&sh.q_free);
@@ -285,7 +284,7 @@ __device__ void dq_softmax_role(const BwdLaunch& p, DqShared& sh, uint32_t tmem,
   int u = 0, t = 0;
   int item = next_item(0);
   while (item < total) {
-    const DqWork<CAUSAL> wk(item, p.BH, p.N, p.dq_bh0);
+    const DqWork<CAUSAL> wk(item, p.BH, p.N);
     const int row = wk.i * 128 + r;
     const size_t srow = static_cast<size_t>(wk.bh) * p.Npad + row;
     const float l2 = __ldg(p.lse2 + srow);  // +inf on padding rows: their P is 0

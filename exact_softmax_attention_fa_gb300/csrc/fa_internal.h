@@ -59,7 +59,6 @@ struct BwdLaunch {
   float* dq_acc;  // [BH][Npad][d]
   uint32_t* sched;  // [4]: main kernel's next work item and CTAs done claiming; the same for the dQ kernel
   int deterministic; // 1: dQ from the separate dQ kernel (no atomics); the main kernel skips it
-  int dq_bh0;        // dQ kernel: its BH query heads are dq_bh0 .. dq_bh0 + BH - 1 (a head range of the problem)
   uint32_t* status;
   int N, Npad, BH, d, causal;
   int BHkv, group;   // K/V heads (B * H_kv) and query heads per K/V head
@@ -75,11 +74,6 @@ struct BwdLaunch {
 // set when the problem has no rows (fa_api.cu).
 fa_status_t check_common(int B, int H, int N, int d, int causal, float scale, bool* empty);
 
-// The dQ kernel over query heads [bh0, bh0 + nbh) of a B x H problem whose
-// workspace the preprocess kernel filled for all heads (fa_api.cu).
-fa_status_t bwd_dq_heads(const void* q, const void* k, const void* v, const void* dO, void* dq, int B, int H, int N,
-                         int d, int causal, float scale, void* workspace, size_t workspace_bytes, int bh0, int nbh,
-                         cudaStream_t stream);
 
 // Launchers (defined in the kernel translation units). Return cudaSuccess or
 // the launch error.

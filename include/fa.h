@@ -34,8 +34,9 @@
  *     recorded in a per-device status word that fa_get_device_status() reads.
  *   - The library allocates no device memory; it keeps only cached device
  *     attributes in process-wide state (plus, once fa_fwd_bwd_host or
- *     fa_fwd_host has run on a device, two copy streams and 27 events for
- *     that device). Entry points are thread-safe.
+ *     fa_fwd_host has run on a device, twelve streams and 50 events for
+ *     that device; they serve one call at a time). Entry points are
+ *     thread-safe.
  */
 #ifndef FA_GB300_H
 #define FA_GB300_H
@@ -268,16 +269,20 @@ fa_status_t fa_bwd_noalloc(const void* q, const void* k, const void* v, const vo
  * Host buffers may have any alignment. The copies overlap the kernels only
  * when the host buffers are page-locked (cudaHostAlloc / cudaHostRegister);
  * pageable buffers give the same results with serialised copies.
- * The call queues, in order after the work already on `stream`: the uploads of
- * Q, K, V in four chunks of heads and of dO on a library-owned copy stream;
- * the forward per chunk as soon as its inputs are on the device; the backward
- * phases fa_bwd runs for this d (d = 128: the dQ kernel in two launches, over
- * the first three quarters and the last quarter of the B*H heads); the
- * read-back of O and L after the forward, of dK and dV after their kernel
- * and of each part of dQ after the launch that wrote it, on a second copy
- * stream. Work queued on `stream` after the call, and a synchronisation
- * of `stream`, see every output in host memory. Only equal-head problems
- * (one K/V head per query head).
+ * The call splits the B*H heads into up to four groups (by default an eighth
+ * of the heads, two groups holding the rest halved, and another eighth) and
+ * queues, in order after the work already on `stream`: the uploads of each
+ * group's Q, K, V (the middle groups' in two chunks of heads) and dO on a
+ * library-owned copy stream; the forward per chunk as soon as its inputs are
+ * on the device, on two library-owned streams at the greatest priority; per
+ * group, on its own library-owned streams and its own part of device_buffer,
+ * the backward phases fa_bwd runs for this d (d = 128: the dK/dV and dQ
+ * kernels side by side); the read-back of O and L, dK and dV, and dQ of each
+ * group as soon as each is final, on a second copy stream. Later groups'
+ * uploads thus overlap earlier groups' kernels, and one launch's last,
+ * partly empty round fills with another's work. Work queued on `stream`
+ * after the call, and a synchronisation of `stream`, see every output in
+ * host memory. Only equal-head problems (one K/V head per query head).
  * Errors: those of fa_fwd / fa_bwd, checked before any work is queued;
  * FA_ERR_WORKSPACE if device_buffer is null or too small, FA_ERR_MISALIGNED
  * if it is not 256-byte aligned, FA_ERR_CUDA if a copy or an event call
@@ -291,7 +296,9 @@ fa_status_t fa_fwd_bwd_host(const void* q, const void* k, const void* v, const v
 /*
  * Forward pass of a problem held in HOST memory (as fa_fwd), pipelined over
  * eight chunks of heads: while chunk c is on the tensor cores, chunk c + 1
- * uploads and chunk c - 1 is read back.
+ * uploads and chunk c - 1 is read back. The chunks' launches alternate
+ * between two library-owned streams, so one fills the last round of the
+ * one before.
  *   q, k, v         : in,  HOST bf16 [B][H][N][d]
  *   o               : out, HOST bf16 [B][H][N][d]
  *   lse             : out, HOST fp32 [B][H][N]

@@ -201,9 +201,20 @@ def test_host_entry_checks(lib):
         return lib.fa_fwd_bwd_host(ptr, ptr, ptr, ptr, ptr, lse, ptr, ptr, ptr, B, H, N, d, causal, scale, buf,
                                    nbytes, None)
     a = lambda n: (n + 255) // 256 * 256
-    for B, H, N, d in ((1, 2, 128, 64), (2, 3, 1000, 128), (1, 1, 1, 256)):
+
+    def groups(BH):
+        """Head counts of the plan the header states: an eighth of the heads,
+        the rest (less another eighth) in two halves, then that eighth."""
+        g0 = (BH + 7) // 8
+        last = (BH + 7) // 8 if BH - g0 >= 2 else BH - g0
+        mid = BH - g0 - last
+        return [h for h in (g0, mid // 2, mid - mid // 2, last) if h > 0]
+
+    assert groups(32) == [4, 12, 12, 4] and groups(3) == [1, 1, 1] and groups(2) == [1, 1] and groups(1) == [1]
+    for B, H, N, d in ((1, 2, 128, 64), (2, 3, 1000, 128), (1, 1, 1, 256), (2, 16, 8192, 128), (1, 5, 300, 64)):
         rows = B * H * N
-        need = 8 * a(rows * d * 2) + a(rows * 4) + a(lib.fa_bwd_workspace_size(B, H, N, d))
+        need = 8 * a(rows * d * 2) + a(rows * 4)
+        need += sum(a(lib.fa_bwd_workspace_size(1, h, N, d)) for h in groups(B * H))
         assert lib.fa_fwd_bwd_host_device_bytes(B, H, N, d) == need
     need = lib.fa_fwd_bwd_host_device_bytes(1, 2, 128, 64)
     assert lib.fa_fwd_bwd_host_device_bytes(1, 2, 0, 64) == 0

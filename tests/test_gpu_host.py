@@ -74,6 +74,23 @@ def test_host_entry_matches_device_path(B, H, N, d, causal):
         assert e <= TOL_GRAD_REL, (name, e)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_host_entry_groups_at_full_tile_count_match_device_path(causal):
+    """B*H = 8 heads of N = 8192 at d = 128: the heads flow through four
+    groups (1, 3, 3 and 1 heads; the middle ones' forward in two launches),
+    each group's dK/dV and dQ kernels run side by side on their own streams
+    and workspace, and launches of different groups overlap. Every output
+    equals the device path's bit for bit (no atomics at d = 128)."""
+    import torch
+    B, H, N, d = 1, 8, 8192, 128
+    x, _ = inputs(B, H, N, d, BASE_SEED + 980 + int(causal))
+    scale = scale_f32(d)
+    host = run_host(x, causal, scale)
+    dev = run_device(x, causal, scale)
+    for name, a, b in zip(("o", "lse", "dq", "dk", "dv"), host, dev):
+        assert torch.equal(a, b), name
+
+
 def test_host_entry_pageable_buffers():
     """Pageable host tensors give the same outputs (the copies just do not overlap)."""
     import torch
