@@ -15,7 +15,7 @@ import math
 
 from ._lib import load, check, FAError, header_functions, STATUS_NAMES  # noqa: F401
 
-__all__ = ["fa_fwd", "fa_bwd", "fa_fwd_gqa", "fa_bwd_gqa", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_size", "fa_bwd_deterministic", "fa_bwd_gqa_deterministic", "fa_bwd_workspace_size", "fa_bwd_gqa_workspace_size", "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_postprocess", "fa_bwd_dkdv", "fa_bwd_dq", "fa_bwd_noalloc", "fa_fwd_bwd_host", "fa_fwd_bwd_host_device_bytes", "fa_fwd_host", "fa_fwd_host_device_bytes", "fa_get_device_status", "fa_set_wait_limit_ns",
+__all__ = ["fa_fwd", "fa_bwd", "fa_fwd_gqa", "fa_bwd_gqa", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_size", "fa_bwd_deterministic", "fa_bwd_gqa_deterministic", "fa_bwd_workspace_size", "fa_bwd_gqa_workspace_size", "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_postprocess", "fa_bwd_dkdv", "fa_bwd_dq", "fa_bwd_noalloc", "fa_fwd_bwd_host", "fa_fwd_bwd_host_device_bytes", "fa_fwd_host", "fa_fwd_host_device_bytes", "fa_get_device_status", "fa_get_device_status_detail", "fa_set_wait_limit_ns",
            "fa_debug_timeout_probe", "forward", "backward", "FAError", "flops"]
 
 _SUPPORTED_D = (64, 128, 256)
@@ -334,6 +334,17 @@ def fa_fwd_host(q, k, v, o, lse, causal: bool, scale: float, device_buffer, stre
 def fa_get_device_status(stream=None) -> int:
     """Synchronise the stream; return and clear the device status (0 = FA_OK)."""
     return int(load().fa_get_device_status(_stream_handle(stream)))
+
+
+def fa_get_device_status_detail(stream=None) -> tuple:
+    """Synchronise the stream; return and clear the whole device status word:
+    (code, role of the first wait that gave up, its block, its thread)."""
+    import ctypes
+    word = (ctypes.c_uint * 4)()
+    st = int(load().fa_get_device_status_detail(ctypes.addressof(word), _stream_handle(stream)))
+    if st == 7:  # FA_ERR_CUDA: the synchronisation failed, the word was not read
+        check("fa_get_device_status_detail", st)
+    return tuple(int(x) for x in word)
 
 
 def fa_set_wait_limit_ns(limit_ns: int) -> None:

@@ -62,6 +62,7 @@ _SIGNATURES = {
                                  _c_int, _c_float, _vp, ctypes.c_size_t, _vp]),
     "fa_status_string": (ctypes.c_char_p, [_c_int]),
     "fa_get_device_status": (_c_int, [_vp]),
+    "fa_get_device_status_detail": (_c_int, [_vp, _vp]),
     "fa_set_wait_limit_ns": (None, [ctypes.c_ulonglong]),
     "fa_debug_timeout_probe": (_c_int, [ctypes.c_ulonglong, _vp]),
     "fa_version": (_c_int, []),

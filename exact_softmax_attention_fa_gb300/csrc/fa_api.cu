@@ -582,18 +582,25 @@ fa_status_t fa_bwd_postprocess(void* dq, int B, int H, int N, int d, void* works
   return from_cuda(launch_bwd_post(a, stream));
 }
 
-fa_status_t fa_get_device_status(cudaStream_t stream) {
+fa_status_t fa_get_device_status_detail(unsigned int* word, cudaStream_t stream) {
+  if (!word) return FA_ERR_INVALID_ARG;
   fa_status_t st = FA_OK;
   DeviceState* ds = device_state(&st);
   if (!ds) return st;
   if (cudaStreamSynchronize(stream) != cudaSuccess) return FA_ERR_CUDA;
-  uint32_t word[4] = {0, 0, 0, 0};
-  if (cudaMemcpy(word, ds->status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
-  if (word[0] != 0) {
+  uint32_t w[4] = {0, 0, 0, 0};
+  if (cudaMemcpy(w, ds->status, sizeof(w), cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
+  if (w[0] != 0) {
     const uint32_t zero[4] = {0, 0, 0, 0};
     if (cudaMemcpy(ds->status, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_CUDA;
   }
-  return static_cast<fa_status_t>(word[0]);
+  for (int i = 0; i < 4; ++i) word[i] = w[i];
+  return static_cast<fa_status_t>(w[0]);
+}
+
+fa_status_t fa_get_device_status(cudaStream_t stream) {
+  unsigned int word[4];
+  return fa_get_device_status_detail(word, stream);
 }
 
 fa_status_t fa_debug_timeout_probe(unsigned long long limit_ns, cudaStream_t stream) {

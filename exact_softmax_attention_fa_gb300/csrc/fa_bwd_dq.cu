@@ -63,7 +63,13 @@ struct DqShared {
   uint64_t q_full, q_free;
   uint64_t k_full[4], k_empty[4], v_full[2], v_empty[2];
   uint64_t s_full[2];  // per S buffer
-  uint64_t dp_full, dp_free, ds_ready, dq_done, acc_done, acc_free;
+  // ds_ready[t & 1]: dS(t) is in TMEM. Two barriers, because the softmax can
+  // finish tile t+1 (it needs only dP(t+1), issued before the MMA thread
+  // waits for dS(t)) before that wait starts: on one barrier the wait would
+  // then see two completed phases and take the pending third for its own.
+  // Tile t+2 needs dP(t+2), issued after the wait, so one barrier per tile
+  // parity can be at most one phase ahead of its waiter.
+  uint64_t dp_full, dp_free, ds_ready[2], dq_done, acc_done, acc_free;
   uint64_t item_full[kItemSlots], item_empty[kItemSlots];
   int item_ring[kItemSlots];
   uint32_t tmem_base;
@@ -225,7 +231,7 @@ __device__ void dq_mma_role(const BwdLaunch& p, DqShared& sh, uint8_t* sQ, uint8
         if (!issue_s(t + 1, kv + 1, t - 1) || !issue_dp(t + 1, kv + 1)) return fail();
         if (j + 2 == wk.nkv) umma_commit(&sh.q_free);  // the item's last S and dP are issued
       }
-      if (!mbar_wait(&sh.ds_ready, t & 1, &sh.abort_flag, lim)) return fail();
+      if (!mbar_wait(&sh.ds_ready[t & 1], (t >> 1) & 1, &sh.abort_flag, lim)) return fail();
       // the first dQ product of an item overwrites the accumulator: the
       // previous item's epilogue must have read it
       if (j == 0 && u > 0 && !mbar_wait(&sh.acc_free, (u - 1) & 1, &sh.abort_flag, lim)) return fail();
@@ -358,7 +364,7 @@ __device__ void dq_softmax_role(const BwdLaunch& p, DqShared& sh, uint32_t tmem,
         tmem_st32(tS0 + 128u * uint32_t(t & 1), ds);
         tmem_st_wait();
         tc_fence_before_sync();
-        mbar_arrive(&sh.ds_ready);
+        mbar_arrive(&sh.ds_ready[t & 1]);
       }
     }
     const int item_next = next_item(u + 1);
@@ -418,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
     for (int b = 0; b < 2; ++b) mbar_init(&sh.s_full[b], 1);
     mbar_init(&sh.dp_full, 1);
     mbar_init(&sh.dp_free, 256);
-    mbar_init(&sh.ds_ready, 256);
+    for (int b = 0; b < 2; ++b) mbar_init(&sh.ds_ready[b], 256);
     mbar_init(&sh.dq_done, 1);
     mbar_init(&sh.acc_done, 1);
     mbar_init(&sh.acc_free, 256);

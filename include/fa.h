@@ -322,6 +322,17 @@ const char* fa_status_string(fa_status_t status);
 fa_status_t fa_get_device_status(cudaStream_t stream);
 
 /*
+ * As fa_get_device_status, and also copies the whole status word into
+ * word[4] (host memory, owned by the caller): word[0] the status code,
+ * word[1] the role of the thread whose wait gave up first (1-3: forward
+ * load / MMA / softmax; 11-14: backward load / MMA / softmax / dQ drain;
+ * 99: the self-test probe), word[2] its block index, word[3] its thread
+ * index; all zero when no wait gave up. Returns FA_ERR_INVALID_ARG for a
+ * null word.
+ */
+fa_status_t fa_get_device_status_detail(unsigned int* word, cudaStream_t stream);
+
+/*
  * Time limit, in nanoseconds, of every device-side pipeline wait in later
  * launches (default 4e9). A wait that exceeds it records FA_ERR_TIMEOUT and
  * the kernel returns early with its outputs undefined.

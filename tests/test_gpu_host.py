@@ -91,6 +91,38 @@ def test_host_entry_groups_at_full_tile_count_match_device_path(causal):
         assert torch.equal(a, b), name
 
 
+def test_host_entry_back_to_back_calls_never_stall():
+    """40 back-to-back calls at B=1, H=16, N=16384, d=128 with a 250 ms limit
+    on every device-side wait. The host-buffer step overlaps copies and
+    kernels of different head groups, which shifts the relative speed of the
+    warps inside a CTA; every pipeline wait must still complete (a waiter two
+    barrier phases behind its producer would stall until the limit). The
+    outputs of the last call equal the device path's."""
+    import torch
+    import exact_softmax_attention_fa_gb300 as fa
+    B, H, N, d = 1, 16, 16384, 128
+    x, _ = inputs(B, H, N, d, BASE_SEED + 1400)
+    scale = scale_f32(d)
+    hq, hk, hv, hdo = (host_bf16(x[n], True) for n in ("q", "k", "v", "do"))
+    outs = [torch.empty((B, H, N, d), dtype=torch.bfloat16).pin_memory() for _ in range(4)]
+    lse = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    buf = torch.empty(fa.fa_fwd_bwd_host_device_bytes(B, H, N, d), dtype=torch.uint8, device="cuda")
+    fa.fa_set_wait_limit_ns(250_000_000)
+    try:
+        stalls = []
+        for i in range(40):
+            fa.fa_fwd_bwd_host(hq, hk, hv, hdo, outs[0], lse, outs[1], outs[2], outs[3], False, scale, buf)
+            word = fa.fa_get_device_status_detail()
+            if word[0] != 0:
+                stalls.append((i, word))
+    finally:
+        fa.fa_set_wait_limit_ns(0)
+    assert not stalls, stalls
+    dev = run_device(x, False, scale)
+    for name, a, b in zip(("o", "lse", "dq", "dk", "dv"), (outs[0], lse, outs[1], outs[2], outs[3]), dev):
+        assert torch.equal(a, b), name
+
+
 def test_host_entry_pageable_buffers():
     """Pageable host tensors give the same outputs (the copies just do not overlap)."""
     import torch

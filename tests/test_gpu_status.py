@@ -26,6 +26,16 @@ def test_bounded_wait_reports_timeout_and_context_survives(cuda_lib):
     assert np.abs(to_host64(o) - o_ref).max() <= TOL_O
 
 
+def test_status_detail_names_the_waiting_role(cuda_lib):
+    """The whole status word: code, role (99 = the probe), block, thread; read and cleared."""
+    import exact_softmax_attention_fa_gb300 as fa
+    assert fa.fa_get_device_status_detail() == (0, 0, 0, 0)
+    fa.fa_debug_timeout_probe(2_000_000)
+    code, role, block, _thread = fa.fa_get_device_status_detail()
+    assert (code, role, block) == (FA_ERR_TIMEOUT, 99, 0)
+    assert fa.fa_get_device_status_detail() == (0, 0, 0, 0)
+
+
 def test_probe_rejects_bad_limits(cuda_lib):
     import exact_softmax_attention_fa_gb300 as fa
     with pytest.raises(fa.FAError):
