@@ -79,7 +79,7 @@ struct FwdCfg {
 };
 
 struct FwdShared {
-  uint64_t q_full, q_free[2];
+  uint64_t q_full[2], q_free[2];  // per query-tile slot
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
   uint64_t s_full[2], p_full[2], pv_done[2], o_free[2];
   uint32_t tmem_base;
@@ -164,6 +164,13 @@ __device__ __forceinline__ int total_items(const FwdLaunch& p, int NT) {
   return (p.BH / heads_per_tile<PACK>(p)) * ((Tq + NT - 1) / NT) * p.splits;
 }
 
+// Fetch one tile of a tensor map into L2 (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // TMA producer (one thread)
 // ---------------------------------------------------------------------------
@@ -180,6 +187,8 @@ __device__ void fwd_load_role(const FwdLaunch& p, FwdShared& sh, uint8_t* sQ, ui
   int kv = 0;     // running count of K/V tiles loaded by this CTA
   int items = 0;  // items started
   int k_issued = 0, v_issued = 0;
+  int q_item = -1;      // the latest item whose Q loads were issued ...
+  unsigned q_mask = 0;  // ... and its slots
   bool aborted = false;
   for (int k = 0; k * G < total && !aborted; ++k) {
     const int item = sched_item(k, blockIdx.x, G);
@@ -189,25 +198,26 @@ __device__ void fwd_load_role(const FwdLaunch& p, FwdShared& sh, uint8_t* sQ, ui
     const int kv_bh = wk.bh / p.group;  // grouped K/V heads: query head bh reads K/V head bh / g
     // Q_t's smem was the previous item's O staging: wait until its store read
     // it. The item's first K/V tile is issued before that wait so it loads
-    // while the previous epilogue runs.
+    // while the previous epilogue runs. Each slot has its own q_full, and the
+    // two warpgroups' epilogues end at different times, so Q_0 (and with it
+    // S_0(0)) does not wait for slot 1's epilogue. An empty slot's q_full
+    // still completes one phase per item (an arrival without bytes).
     auto load_q = [&]() -> bool {
-      if (items > 0) {
-#pragma unroll
-        for (int t = 0; t < C::NT; ++t)
-          if (!mbar_wait(&sh.q_free[t], (items - 1) & 1, &sh.abort_flag, lim)) return false;
-      }
-      uint32_t qbytes = 0;
-#pragma unroll
-      for (int t = 0; t < C::NT; ++t)
-        if (wk.last_kv[t] >= 0) qbytes += C::TILE_BYTES;
-      mbar_arrive_expect_tx(&sh.q_full, qbytes);
+      q_mask = 0;
 #pragma unroll
       for (int t = 0; t < C::NT; ++t) {
-        if (wk.last_kv[t] < 0) continue;
+        if (items > 0 && !mbar_wait(&sh.q_free[t], (items - 1) & 1, &sh.abort_flag, lim)) return false;
+        if (wk.last_kv[t] < 0) {
+          mbar_arrive(&sh.q_full[t]);
+          continue;
+        }
+        mbar_arrive_expect_tx(&sh.q_full[t], C::TILE_BYTES);
 #pragma unroll
         for (int c = 0; c < C::CHUNKS; ++c)
-          tma_load_3d(sQ + t * C::TILE_BYTES + c * C::CHUNK_BYTES, &p.tmQ, &sh.q_full, c * 64, wk.qt[t] * rows_per_head<PACK>(p),
-                      wk.bh);
+          tma_load_3d(sQ + t * C::TILE_BYTES + c * C::CHUNK_BYTES, &p.tmQ, &sh.q_full[t], c * 64,
+                      wk.qt[t] * rows_per_head<PACK>(p), wk.bh);
+        q_item = items;
+        q_mask |= 1u << t;
       }
       return true;
     };
@@ -223,9 +233,26 @@ __device__ void fwd_load_role(const FwdLaunch& p, FwdShared& sh, uint8_t* sQ, ui
         tma_load_3d(sK + ks * C::TILE_BYTES + c * C::CHUNK_BYTES, &p.tmK, &sh.k_full[ks], c * 64, (wk.kv0 + j) * 128,
                     kv_bh);
       ++k_issued;
-      if (j == 0 && !load_q()) {
-        aborted = true;
-        break;
+      if (j == 0) {
+        if (!load_q()) {
+          aborted = true;
+          break;
+        }
+        // The next item's Q tiles come from HBM (each query tile is read
+        // once) and are loaded only after this item's epilogue: fetch them
+        // into L2 now, so that load is an L2 hit. It matters for short
+        // sequences, whose items hold only a few key tiles.
+        const int next = (k + 1) * G < total ? sched_item(k + 1, blockIdx.x, G) : total;
+        if (next < total) {
+          const FwdWork<C::NT, CAUSAL, PACK> wn(next, p);
+#pragma unroll
+          for (int t = 0; t < C::NT; ++t) {
+            if (wn.nkv == 0 || wn.last_kv[t] < 0) continue;
+#pragma unroll
+            for (int c = 0; c < C::CHUNKS; ++c)
+              tma_prefetch_l2_3d(&p.tmQ, c * 64, wn.qt[t] * rows_per_head<PACK>(p), wn.bh);
+          }
+        }
       }
       const int vs = kv % C::VST;
       if (kv >= C::VST && !mbar_wait(&sh.v_empty[vs], ((kv / C::VST) - 1) & 1, &sh.abort_flag, lim)) {
@@ -250,7 +277,8 @@ __device__ void fwd_load_role(const FwdLaunch& p, FwdShared& sh, uint8_t* sQ, ui
       mbar_wait(&sh.k_full[jj % C::KST], (jj / C::KST) & 1, &zero, lim);
     for (int jj = max(0, v_issued - C::VST); jj < v_issued; ++jj)
       mbar_wait(&sh.v_full[jj % C::VST], (jj / C::VST) & 1, &zero, lim);
-    if (items > 0 || k_issued > 0) mbar_wait(&sh.q_full, items & 1, &zero, lim);
+    for (int t = 0; t < C::NT; ++t)
+      if (q_mask >> t & 1) mbar_wait(&sh.q_full[t], q_item & 1, &zero, lim);
   }
 }
 
@@ -297,7 +325,6 @@ __device__ void fwd_mma_role(const FwdLaunch& p, FwdShared& sh, uint8_t* sQ, uin
     if (item >= total) continue;
     const FwdWork<C::NT, CAUSAL, PACK> wk(item, p);
     if (wk.nkv == 0) continue;
-    if (!mbar_wait(&sh.q_full, items & 1, &sh.abort_flag, lim)) return fail();
     if (!mbar_wait(&sh.k_full[kv % C::KST], (kv / C::KST) & 1, &sh.abort_flag, lim)) return fail();
     tc_fence_after_sync();
 #pragma unroll
@@ -306,6 +333,7 @@ __device__ void fwd_mma_role(const FwdLaunch& p, FwdShared& sh, uint8_t* sQ, uin
       // S_t(0) overwrites S_t / P~_t of the previous item: its last PV must be done.
       if (C::P_ALIAS && cnt[t] > 0 && !mbar_wait(&sh.pv_done[t], (cnt[t] - 1) & 1, &sh.abort_flag, lim))
         return fail();
+      if (!mbar_wait(&sh.q_full[t], items & 1, &sh.abort_flag, lim)) return fail();
       tc_fence_after_sync();
       issue_s(t, kv);
     }
@@ -551,7 +579,7 @@ __device__ void fwd_softmax_role(const FwdLaunch& p, FwdShared& sh, uint8_t* sQ,
       // arrivals one item at a time (a warpgroup that ran two items ahead
       // would complete a phase the load thread has not waited for yet).
       if (alive) {
-        alive = __all_sync(0xffffffffu, mbar_wait(&sh.q_full, items & 1, &sh.abort_flag, lim));
+        alive = __all_sync(0xffffffffu, mbar_wait(&sh.q_full[t], items & 1, &sh.abort_flag, lim));
         if (!alive) record_timeout(p.status, &sh.abort_flag, WHERE_FWD_SOFTMAX);
       }
       mbar_arrive(&sh.o_free[t]);
@@ -585,7 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   const int warp = threadIdx.x >> 5;
 
   if (threadIdx.x == 0) {
-    mbar_init(&sh.q_full, 1);
+    for (int t = 0; t < 2; ++t) mbar_init(&sh.q_full[t], 1);
     for (int i = 0; i < 4; ++i) {
       mbar_init(&sh.k_full[i], 1);
       mbar_init(&sh.k_empty[i], 1);
