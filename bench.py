@@ -351,7 +351,7 @@ def run_ours(args, p: dict, name: str, world: int, rank: int, local: int) -> dic
         fa.fa_fwd_bwd_host(pinned["q"], pinned["k"], pinned["v"], pinned["do"], out_host["o"], out_host["lse"],
                            out_host["dq"], out_host["dk"], out_host["dv"], causal, scale, host_buf, stream)
 
-    for _ in range(2):
+    for _ in range(max(3, min(args.warmup, 5))):
         e2e_step()
     torch.cuda.synchronize(device)
     barrier(device)
@@ -370,7 +370,7 @@ def run_ours(args, p: dict, name: str, world: int, rank: int, local: int) -> dic
         fa.fa_fwd_host(pinned["q"], pinned["k"], pinned["v"], out_host["o"], out_host["lse"], causal, scale, fwd_buf,
                        stream)
 
-    for _ in range(2):
+    for _ in range(max(3, min(args.warmup, 5))):
         e2e_fwd_step()
     torch.cuda.synchronize(device)
     e0.record(stream)
