@@ -211,7 +211,9 @@ def test_host_entry_checks(lib):
         return [h for h in (g0, mid // 2, mid - mid // 2, last) if h > 0]
 
     assert groups(32) == [4, 12, 12, 4] and groups(3) == [1, 1, 1] and groups(2) == [1, 1] and groups(1) == [1]
-    for B, H, N, d in ((1, 2, 128, 64), (2, 3, 1000, 128), (1, 1, 1, 256), (2, 16, 8192, 128), (1, 5, 300, 64)):
+    shapes = [(1, 2, 128, 64), (2, 3, 1000, 128), (1, 1, 1, 256), (2, 16, 8192, 128), (1, 5, 300, 64)]
+    shapes += [(1, bh, 640, 128) for bh in range(1, 41)]  # every group split up to 40 heads
+    for B, H, N, d in shapes:
         rows = B * H * N
         need = 8 * a(rows * d * 2) + a(rows * 4)
         need += sum(a(lib.fa_bwd_workspace_size(1, h, N, d)) for h in groups(B * H))
