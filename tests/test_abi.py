@@ -36,6 +36,11 @@ def test_status_strings(lib):
     assert lib.fa_version() >= 100
 
 
+def test_status_detail_rejects_a_null_word(lib):
+    """The argument check comes before any device access (no GPU needed)."""
+    assert lib.fa_get_device_status_detail(None, None) == INVALID
+
+
 def fwd(lib, q=P, k=P, v=P, o=P, lse=P, B=1, H=1, N=128, d=64, causal=0, scale=0.125):
     return lib.fa_fwd(q, k, v, o, lse, B, H, N, d, causal, scale, None)
 
