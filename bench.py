@@ -247,7 +247,119 @@ def calibrate_rows(p: dict, x: dict, target_s: float) -> int:
 # arms
 # ---------------------------------------------------------------------------
 def host_inputs(p: dict, rank: int):
-    return make_inputs(p["B"], p["H"], p["N"], p["d"], seed_for(p) + rank)
+    return make_inputs(p["B"], p["H"], p["N"], p["d"], seed_for(p) + rank, peaked_frac=p.get("peaked_frac", 0.0))
+
+
+def backward_phases(fa, d, t, causal, scale, ws, stream):
+    """The backward phases fa_bwd runs for this head dimension (include/fa.h):
+    names and calls, in order."""
+    q, k, v, o, lse, do, dq, dk, dv = (t[n] for n in ("q", "k", "v", "o", "lse", "do", "dq", "dk", "dv"))
+    if d == 128:
+        return (("bwd_pre", "bwd_dkdv", "bwd_dq"),
+                (lambda: fa.fa_bwd_preprocess_stats(o, lse, do, ws, stream),
+                 lambda: fa.fa_bwd_dkdv(q, k, v, do, dk, dv, causal, scale, ws, stream),
+                 lambda: fa.fa_bwd_dq(q, k, v, do, dq, causal, scale, ws, stream)))
+    return (("bwd_pre", "bwd_main", "bwd_post"),
+            (lambda: fa.fa_bwd_preprocess(o, lse, do, ws, stream),
+             lambda: fa.fa_bwd_main(q, k, v, do, dk, dv, causal, scale, ws, stream),
+             lambda: fa.fa_bwd_postprocess(dq, ws, stream)))
+
+
+def device_buffers(fa, p: dict, x: dict, device):
+    """Device copies of the inputs and the outputs and workspace of one step."""
+    import numpy as np
+    import torch
+    B, H, N, d = p["B"], p["H"], p["N"], p["d"]
+    t = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).to(device) for k, v in x.items()}
+    t["o"] = torch.empty_like(t["q"])
+    t["lse"] = torch.empty((B, H, N), dtype=torch.float32, device=device)
+    for n in ("dq", "dk", "dv"):
+        t[n] = torch.empty_like(t["q"])
+    ws = torch.empty(fa.fa_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=device)
+    return t, ws
+
+
+def time_device_step(fa, p: dict, t: dict, ws, stream, steps: int, warmup: int, on_timed=None):
+    """Time `steps` back-to-back steps (fa_fwd, then the backward phases) with
+    CUDA events on `stream`; returns (total ms, per-phase mean ms, phase names).
+    `on_timed` = (start, stop) callbacks bracketing the timed region."""
+    import numpy as np
+    import torch
+    causal, d = p["causal"], p["d"]
+    scale = float(np.float32(1.0 / np.sqrt(d)))
+    names, calls = backward_phases(fa, d, t, causal, scale, ws, stream)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        fa.fa_fwd(t["q"], t["k"], t["v"], t["o"], t["lse"], causal, scale, stream)
+        for i, call in enumerate(calls):
+            if ev is not None:
+                ev[1 + i].record(stream)
+            call()
+        if ev is not None:
+            ev[4].record(stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(stream.device)
+    if fa.fa_get_device_status(stream) != 0:
+        raise RuntimeError("device status reports a timed-out pipeline wait during warm-up")
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+    if on_timed:
+        on_timed[0]()
+    for s_ in range(steps):
+        step(events[s_])
+    torch.cuda.synchronize(stream.device)
+    if on_timed:
+        on_timed[1]()
+    status = fa.fa_get_device_status(stream)
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed region")
+    total_ms = events[0][0].elapsed_time(events[-1][4])
+    phase_ms = [sum(e[i].elapsed_time(e[i + 1]) for e in events) / steps for i in range(4)]
+    return total_ms, phase_ms, ("fwd",) + names
+
+
+EXTRA_WORKLOADS = ("long_causal_peaked", "wide_head_d256")
+EXTRA_STEPS = 10
+
+
+def time_workload(fa, name: str, device, stream, steps: int, warmup: int) -> dict:
+    """Device-resident timing of one named workload (fa_fwd + the backward
+    phases fa_bwd runs), as a dict of sizes, per-phase ms and TFLOP/s."""
+    import torch
+    p = all_workloads()[name]
+    t, ws = device_buffers(fa, p, host_inputs(p, 0), device)
+    _total, phase_ms, names = time_device_step(fa, p, t, ws, stream, steps, warmup)
+    del t, ws
+    torch.cuda.empty_cache()
+    return {"workload": name, **{kk: p[kk] for kk in ("B", "H", "N", "d", "causal")},
+            **({"peaked_frac": p["peaked_frac"]} if "peaked_frac" in p else {}),
+            "steps": steps, "warmup": warmup, "phase_ms": dict(zip(names, phase_ms)), **workload_rates(p, phase_ms)}
+
+
+def run_sweep(args) -> int:
+    """One JSON line per point of the pages' microbenchmark grid (hidden 2048:
+    d = 64 x 32 heads and d = 128 x 16 heads, N = 512 .. 16k, B = 16384 / N,
+    causal and not), then the long-context and d = 256 configurations."""
+    import torch
+    import exact_softmax_attention_fa_gb300 as fa
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    stream = torch.cuda.current_stream(device)
+    names = [n for n, _ in sweep_points()] + list(EXTRA_WORKLOADS)
+    for name in names:
+        print(json.dumps(time_workload(fa, name, device, stream, args.steps, args.warmup)), flush=True)
+    return 0
+
+
+def workload_rates(p: dict, phase_ms) -> dict:
+    """TFLOP/s by the pages' convention from the per-phase times of one step."""
+    f_fwd, f_bwd, f_step = flops(p, "fwd"), flops(p, "bwd"), flops(p, "fwd_bwd")
+    return {"fwd_tflops": f_fwd / (phase_ms[0] / 1e3) / 1e12,
+            "bwd_tflops": f_bwd / (sum(phase_ms[1:]) / 1e3) / 1e12,
+            "fwd_bwd_tflops": f_step / (sum(phase_ms) / 1e3) / 1e12}
 
 
 def run_reference(args, p: dict, name: str) -> dict:
@@ -284,58 +396,25 @@ def run_ours(args, p: dict, name: str, world: int, rank: int, local: int) -> dic
     scale = float(np.float32(1.0 / np.sqrt(d)))
     x = host_inputs(p, rank)
     pinned = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).pin_memory() for k, v in x.items()}
-    dev = {k: v.to(device) for k, v in pinned.items()}
-    q, k, v, do = dev["q"], dev["k"], dev["v"], dev["do"]
-    o = torch.empty_like(q)
-    lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
-    ws = torch.empty(fa.fa_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=device)
+    t, ws = device_buffers(fa, p, x, device)
+    q, k, v, do = t["q"], t["k"], t["v"], t["do"]
+    o, lse, dq, dk, dv = t["o"], t["lse"], t["dq"], t["dk"], t["dv"]
     stream = torch.cuda.current_stream(device)
 
-    # The backward phases fa_bwd runs for this head dimension (include/fa.h).
-    if d == 128:
-        bwd_names = ("bwd_pre", "bwd_dkdv", "bwd_dq")
-        bwd_calls = (lambda: fa.fa_bwd_preprocess(o, lse, do, ws, stream),
-                     lambda: fa.fa_bwd_dkdv(q, k, v, do, dk, dv, causal, scale, ws, stream),
-                     lambda: fa.fa_bwd_dq(q, k, v, do, dq, causal, scale, ws, stream))
-    else:
-        bwd_names = ("bwd_pre", "bwd_main", "bwd_post")
-        bwd_calls = (lambda: fa.fa_bwd_preprocess(o, lse, do, ws, stream),
-                     lambda: fa.fa_bwd_main(q, k, v, do, dk, dv, causal, scale, ws, stream),
-                     lambda: fa.fa_bwd_postprocess(dq, ws, stream))
-
-    def step(ev=None):
-        if ev is not None:
-            ev[0].record(stream)
-        fa.fa_fwd(q, k, v, o, lse, causal, scale, stream)
-        for i, call in enumerate(bwd_calls):
-            if ev is not None:
-                ev[1 + i].record(stream)
-            call()
-        if ev is not None:
-            ev[4].record(stream)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize(device)
-    if fa.fa_get_device_status(stream) != 0:
-        raise RuntimeError("device status reports a timed-out pipeline wait during warm-up")
-
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     clocks = ClockSampler(local)
-    barrier(device)
-    torch.cuda.synchronize(device)
-    clocks.start()
-    for s in range(args.steps):
-        step(events[s])
-    torch.cuda.synchronize(device)
-    barrier(device)
+
+    def start_timed():
+        barrier(device)
+        torch.cuda.synchronize(device)
+        clocks.start()
+
+    def stop_timed():
+        barrier(device)
+
+    total_ms, phase_ms, phase_names = time_device_step(fa, p, t, ws, stream, args.steps, args.warmup,
+                                                       (start_timed, stop_timed))
     clk = clocks.stop()
-    total_ms = events[0][0].elapsed_time(events[-1][4])
-    phase_ms = [sum(e[i].elapsed_time(e[i + 1]) for e in events) / args.steps for i in range(4)]
-    status = fa.fa_get_device_status(stream)
-    if status != 0:
-        raise RuntimeError(f"device status {status} after the timed region")
+    bwd_names = phase_names[1:]
     max_s = max_over_ranks(total_ms / 1e3, device if world > 1 else None)
 
     # End to end through the C ABI's host-buffer entry point (fa_fwd_bwd_host):
@@ -380,8 +459,20 @@ def run_ours(args, p: dict, name: str, world: int, rank: int, local: int) -> dic
     torch.cuda.synchronize(device)
     e2e_fwd_s = max_over_ranks(e0.elapsed_time(e1) / 1e3 / e2e_steps, device if world > 1 else None)
     del fwd_buf
-    h2d = sum(t.numel() * t.element_size() for t in (q, k, v, do))
-    d2h = sum(t.numel() * t.element_size() for t in (o, lse, dq, dk, dv))
+    h2d = sum(a.numel() * a.element_size() for a in (q, k, v, do))
+    d2h = sum(a.numel() * a.element_size() for a in (o, lse, dq, dk, dv))
+    q_bytes, o_bytes, lse_bytes = (a.numel() * a.element_size() for a in (q, o, lse))
+    del host_buf, out_host
+
+    # The other single-GPU configurations of the pages' workloads (the
+    # longest causal sequence with peaked rows, and the d = 256 head), timed
+    # the same way as the headline step on their own device-resident inputs.
+    extra = {}
+    if world == 1 and not args.no_extra_configs:
+        del t, ws, q, k, v, do, o, lse, dq, dk, dv
+        torch.cuda.empty_cache()
+        for wname in EXTRA_WORKLOADS:
+            extra[wname] = time_workload(fa, wname, device, stream, EXTRA_STEPS, 3)
 
     if rank != 0:
         return None
@@ -394,33 +485,37 @@ def run_ours(args, p: dict, name: str, world: int, rank: int, local: int) -> dic
     num_sms = torch.cuda.get_device_properties(device).multi_processor_count
     pre_bytes = B * H * (2 * N * d * 2 + N * 4 + 2 * n_pad * 4 + (0 if bwd_names[1] == "bwd_dkdv" else n_pad * d * 4))
     value = aggregate_value(f_step * args.steps, world, max_s)
-    fwd_tf = f_fwd / (phase_ms[0] / 1e3) / 1e12
-    bwd_tf = f_bwd / (sum(phase_ms[1:]) / 1e3) / 1e12
-    fwd_bwd_tf = f_step / (sum(phase_ms) / 1e3) / 1e12
-    # Per kernel: its phase time and its own algorithmic FLOPs. The backward's
-    # 10 N^2 d (2.5x forward) are its five 128x128xd products per tile pair;
-    # the dK/dV kernel computes four of them (S, dP, dV, dK), the dQ kernel
-    # three (S, dP, dQ).
+    rates = workload_rates(p, phase_ms)
+    fwd_tf, bwd_tf, fwd_bwd_tf = rates["fwd_tflops"], rates["bwd_tflops"], rates["fwd_bwd_tflops"]
+    # Per kernel: its phase time and its own share of the method's FLOPs. The
+    # backward's 10 N^2 d per head (2.5x forward) are five 128x128xd products
+    # per tile pair: the dK/dV kernel computes four of them (S, dP, dV, dK);
+    # the dQ kernel recomputes S and dP, which the method needs only once, so
+    # it is credited with its dQ product alone.
     if bwd_names[1] == "bwd_dkdv":
         kernels = {"fa_fwd": (phase_ms[0], f_fwd), "fa_bwd_dkdv": (phase_ms[2], 0.8 * f_bwd),
-                   "fa_bwd_dq": (phase_ms[3], 0.6 * f_bwd)}
+                   "fa_bwd_dq": (phase_ms[3], 0.2 * f_bwd)}
     else:
         kernels = {"fa_fwd": (phase_ms[0], f_fwd), "fa_bwd_main": (phase_ms[2], f_bwd)}
-    # The dominant kernel (largest share of the step) gets the roofline entry.
-    ranked = sorted(kernels, key=lambda kk: -kernels[kk][0])
-    dom = ranked[0]
-    dom_ms, dom_flops = kernels[dom]
-    achieved = dom_flops / (dom_ms / 1e3) / 1e12
-    # Each kernel is timed inside a long back-to-back step: sustained peak.
-    roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": sustained, "unit": UNIT,
-                "frac": achieved / sustained, "traffic": profiled_traffic(dom, name),
-                "peak_kind": f"{peak_kind} sustained dense bf16 (MEASURED_PEAKS.json)",
-                "avg_launch_ms": dom_ms}
-    other = ranked[1]
-    o_ms, o_fl = kernels[other]
-    roofline_other = {"bound": "tensor", "kernel": other, "achieved": o_fl / (o_ms / 1e3) / 1e12,
-                      "peak": sustained, "unit": UNIT, "frac": o_fl / (o_ms / 1e3) / 1e12 / sustained,
-                      "traffic": profiled_traffic(other, name), "avg_launch_ms": o_ms}
+    # The denominator: the burst bf16 peak for kernels timed in a short
+    # region that the power cap did not throttle, the sustained one when the
+    # clock sampler saw the power cap active. Both fractions are reported.
+    capped = "sw_power_cap" in (clk.get("reasons") or [])
+    peak = sustained if capped else burst
+    peak_desc = (f"{peak_kind} {'sustained' if capped else 'burst'} dense bf16 (MEASURED_PEAKS.json); "
+                 f"{'sw_power_cap seen' if capped else 'no power cap seen'} during the timed region")
+
+    def roof(name):
+        ms, fl = kernels[name]
+        ach = fl / (ms / 1e3) / 1e12
+        return {"bound": "tensor", "kernel": name, "achieved": ach, "peak": peak, "unit": UNIT,
+                "frac": ach / peak, "frac_vs_burst": ach / burst, "frac_vs_sustained": ach / sustained,
+                "traffic": profiled_traffic(name, name_workload), "avg_launch_ms": ms}
+
+    name_workload = name
+    ranked = sorted(kernels, key=lambda kk: -kernels[kk][0])  # the dominant kernel has the largest share
+    roofline = {**roof(ranked[0]), "peak_kind": peak_desc}
+    roofline_other = roof(ranked[1])
 
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -441,6 +536,10 @@ def run_ours(args, p: dict, name: str, world: int, rank: int, local: int) -> dic
         "phase_ms": {"fwd": phase_ms[0], bwd_names[0]: phase_ms[1], bwd_names[1]: phase_ms[2],
                      bwd_names[2]: phase_ms[3]},
         "roofline": roofline, "roofline_secondary": roofline_other,
+        # The whole backward (all its kernels) against the same peak, with
+        # the method's FLOPs (2.5x forward), not the kernels' executed ones.
+        "bwd_algorithmic_frac": {"value": f_bwd / (sum(phase_ms[1:]) / 1e3) / 1e12 / peak, "peak": peak,
+                                 "bwd_ms": sum(phase_ms[1:])},
         # The preprocess kernel is HBM-bound: it reads O, dO (bf16) and L,
         # writes D and the base-2 L (fp32) per padded row, and on the atomic
         # path zeroes the fp32 dQ accumulator.
@@ -458,22 +557,22 @@ def run_ours(args, p: dict, name: str, world: int, rank: int, local: int) -> dic
         "e2e": {"value": aggregate_value(f_step, world, e2e_s), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "e2e_fwd": {"value": aggregate_value(f_fwd, world, e2e_fwd_s), "unit": UNIT,
-                    "h2d_bytes_per_step": 3 * q.numel() * q.element_size(),
-                    "d2h_bytes_per_step": o.numel() * o.element_size() + lse.numel() * lse.element_size(),
+                    "h2d_bytes_per_step": 3 * q_bytes, "d2h_bytes_per_step": o_bytes + lse_bytes,
                     "steps": e2e_steps, "entry": "fa_fwd_host"},
         "gpu_launches": 4 * args.steps,
         "clocks": clk,
+        "other_configs": extra,
     }
     if not args.no_cpu_baseline and world == 1:
         xs = make_inputs(1, 1, N, d, seed_for(p))
         rows = calibrate_rows(p, xs, 4.0)
         t1, _ = oracle_sample(p, xs, rows, 1)
         calls = max(1, int(round(12.0 / max(t1, 1e-3))))  # about 12 s of CPU work
-        t, fl = oracle_sample(p, xs, rows, calls)
+        t_cpu, fl = oracle_sample(p, xs, rows, calls)
         result["cpu_baseline"] = {
-            "value": fl / t / 1e12, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+            "value": fl / t_cpu / 1e12, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
             "sample": (f"{calls} x float64 oracle forward+backward of {rows} query rows x all {N} keys of one head "
-                       f"({t:.1f} s); FLOPs by the same convention as the GPU number")}
+                       f"({t_cpu:.1f} s); FLOPs by the same convention as the GPU number")}
     return result
 
 
@@ -485,9 +584,16 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(all_workloads()))
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle sample (profiling runs)")
+    ap.add_argument("--no-extra-configs", action="store_true",
+                    help="skip timing the long-context and d = 256 configurations after the headline step")
+    ap.add_argument("--sweep", action="store_true",
+                    help="print one line per point of the microbenchmark grid and the other configurations "
+                         "(1 GPU, device-resident inputs) instead of the benchmark line")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.sweep:
+        return run_sweep(args)
     p = all_workloads()[args.workload]
     world, rank, local = dist_env()
 

@@ -15,8 +15,8 @@ import math
 
 from ._lib import load, check, FAError, header_functions, STATUS_NAMES  # noqa: F401
 
-__all__ = ["fa_fwd", "fa_bwd", "fa_fwd_gqa", "fa_bwd_gqa", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_size", "fa_bwd_deterministic", "fa_bwd_gqa_deterministic", "fa_bwd_workspace_size", "fa_bwd_gqa_workspace_size", "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_postprocess", "fa_bwd_dkdv", "fa_bwd_dq", "fa_bwd_noalloc", "fa_fwd_bwd_host", "fa_fwd_bwd_host_device_bytes", "fa_fwd_host", "fa_fwd_host_device_bytes", "fa_get_device_status", "fa_get_device_status_detail", "fa_set_wait_limit_ns",
-           "fa_debug_timeout_probe", "forward", "backward", "FAError", "flops"]
+__all__ = ["fa_fwd", "fa_bwd", "fa_fwd_gqa", "fa_bwd_gqa", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_size", "fa_bwd_deterministic", "fa_bwd_gqa_deterministic", "fa_bwd_workspace_size", "fa_bwd_gqa_workspace_size", "fa_bwd_preprocess", "fa_bwd_preprocess_stats", "fa_bwd_main", "fa_bwd_postprocess", "fa_bwd_dkdv", "fa_bwd_dq", "fa_bwd_noalloc", "fa_fwd_bwd_host", "fa_fwd_bwd_host_device_bytes", "fa_fwd_host", "fa_fwd_host_device_bytes", "fa_get_device_status", "fa_get_device_status_detail", "fa_set_wait_limit_ns",
+           "fa_debug_timeout_probe", "fa_debug_skip_arrival", "forward", "backward", "FAError", "flops"]
 
 _SUPPORTED_D = (64, 128, 256)
 
@@ -206,6 +206,17 @@ def fa_bwd_preprocess(o, lse, do, workspace, stream=None) -> None:
                                                         *_ws(workspace), _stream_handle(stream)))
 
 
+def fa_bwd_preprocess_stats(o, lse, do, workspace, stream=None) -> None:
+    """First phase of fa_bwd_deterministic: D and base-2 L in `workspace` (no accumulator zeroing)."""
+    shape = _dims(o)
+    _check_bf16("o", o, shape)
+    _check_bf16("do", do, shape)
+    _check_lse(lse, shape)
+    B, H, N, d = shape
+    check("fa_bwd_preprocess_stats", load().fa_bwd_preprocess_stats(o.data_ptr(), lse.data_ptr(), do.data_ptr(), B,
+                                                                    H, N, d, *_ws(workspace), _stream_handle(stream)))
+
+
 def fa_bwd_main(q, k, v, do, dk, dv, causal: bool, scale: float, workspace, stream=None) -> None:
     """Second phase of fa_bwd: dk, dv, and dQ accumulated into `workspace`."""
     shape = _dims(q)
@@ -353,6 +364,13 @@ def fa_set_wait_limit_ns(limit_ns: int) -> None:
 
 def fa_debug_timeout_probe(limit_ns: int, stream=None) -> None:
     check("fa_debug_timeout_probe", load().fa_debug_timeout_probe(int(limit_ns), _stream_handle(stream)))
+
+
+def fa_debug_skip_arrival(role: int) -> None:
+    """Test hook: block 0 of later launches leaves out the first arrival of
+    `role` (a role code of fa_get_device_status_detail), so a bounded wait
+    gives up; 0 turns it off."""
+    check("fa_debug_skip_arrival", load().fa_debug_skip_arrival(int(role)))
 
 
 def forward(q, k, v, causal: bool = False, scale: float | None = None, stream=None):

@@ -45,6 +45,7 @@ _SIGNATURES = {
     "fa_bwd": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int,
                         _c_float, _vp, ctypes.c_size_t, _vp]),
     "fa_bwd_preprocess": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _vp, ctypes.c_size_t, _vp]),
+    "fa_bwd_preprocess_stats": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _vp, ctypes.c_size_t, _vp]),
     "fa_bwd_main": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_float, _vp,
                              ctypes.c_size_t, _vp]),
     "fa_bwd_dkdv": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_float, _vp,
@@ -65,6 +66,7 @@ _SIGNATURES = {
     "fa_get_device_status_detail": (_c_int, [_vp, _vp]),
     "fa_set_wait_limit_ns": (None, [ctypes.c_ulonglong]),
     "fa_debug_timeout_probe": (_c_int, [ctypes.c_ulonglong, _vp]),
+    "fa_debug_skip_arrival": (_c_int, [ctypes.c_uint]),
     "fa_version": (_c_int, []),
 }
 

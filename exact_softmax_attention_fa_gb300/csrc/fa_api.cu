@@ -62,9 +62,13 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr uint64_t kDefaultWaitLimitNs = 4000000000ull;
+constexpr uint64_t kMaxWaitLimitNs = 10000000000ull;
 constexpr double kLog2e = 1.4426950408889634074;
 
 std::atomic<unsigned long long> g_wait_limit_ns{kDefaultWaitLimitNs};
+// Test hook (fa_debug_skip_arrival): role whose first arrival block 0 of the
+// next launches leaves out; 0 = none.
+std::atomic<uint32_t> g_debug_skip{0};
 
 struct DeviceState {
   std::once_flag once;
@@ -264,7 +268,9 @@ const char* fa_status_string(fa_status_t s) {
 }
 
 void fa_set_wait_limit_ns(unsigned long long limit_ns) {
-  g_wait_limit_ns.store(limit_ns == 0 ? kDefaultWaitLimitNs : limit_ns);
+  // 0 restores the default; larger values are capped, so a stalled pipeline
+  // still gives up within kMaxWaitLimitNs instead of holding the GPU.
+  g_wait_limit_ns.store(limit_ns == 0 ? kDefaultWaitLimitNs : std::min<unsigned long long>(limit_ns, kMaxWaitLimitNs));
 }
 
 fa_status_t fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
@@ -331,6 +337,7 @@ fa_status_t fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o,
   a.scale_log2 = static_cast<float>(static_cast<double>(scale) * kLog2e);
   a.wait_limit_ns = g_wait_limit_ns.load();
   a.num_sms = ds->num_sms;
+  a.debug_skip = g_debug_skip.load();
   cudaError_t e = launch_fwd(a, stream);
   if (e == cudaSuccess && splits > 1) e = launch_fwd_combine(a, stream);
   return from_cuda(e);
@@ -435,6 +442,7 @@ fa_status_t prepare_bwd(const BwdTensors& t, int B, int H, int Hkv, int N, int d
   a->scale_log2 = static_cast<float>(static_cast<double>(scale) * kLog2e);
   a->wait_limit_ns = g_wait_limit_ns.load();
   a->num_sms = ds->num_sms;
+  a->debug_skip = g_debug_skip.load();
   return FA_OK;
 }
 
@@ -517,6 +525,21 @@ fa_status_t fa_bwd_preprocess(const void* o, const float* lse, const void* dO, i
   st = prepare_bwd(BwdTensors{nullptr, nullptr, nullptr, o, dO, lse, nullptr, nullptr, nullptr}, B, H, H, N, d, 0, 1.0f,
                    workspace, workspace_bytes, &empty, &a);
   if (st != FA_OK || empty) return st;
+  return from_cuda(launch_bwd_pre(a, stream));
+}
+
+fa_status_t fa_bwd_preprocess_stats(const void* o, const float* lse, const void* dO, int B, int H, int N, int d,
+                                    void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  bool empty = false;
+  fa_status_t st = check_common(B, H, N, d, 0, 1.0f, &empty);
+  if (st != FA_OK) return st;
+  if (empty) return FA_OK;
+  if (!o || !lse || !dO) return FA_ERR_INVALID_ARG;
+  BwdLaunch a;
+  st = prepare_bwd(BwdTensors{nullptr, nullptr, nullptr, o, dO, lse, nullptr, nullptr, nullptr}, B, H, H, N, d, 0, 1.0f,
+                   workspace, workspace_bytes, &empty, &a);
+  if (st != FA_OK || empty) return st;
+  a.deterministic = 1;  // the accumulator is not zeroed: the dQ kernel does not use it
   return from_cuda(launch_bwd_pre(a, stream));
 }
 
@@ -603,11 +626,28 @@ fa_status_t fa_get_device_status(cudaStream_t stream) {
   return fa_get_device_status_detail(word, stream);
 }
 
+fa_status_t fa_debug_skip_arrival(unsigned int role) {
+  switch (role) {
+    case 0:
+    case WHERE_FWD_LOAD:
+    case WHERE_FWD_MMA:
+    case WHERE_FWD_SOFTMAX:
+    case WHERE_BWD_LOAD:
+    case WHERE_BWD_MMA:
+    case WHERE_BWD_SOFTMAX:
+    case WHERE_BWD_DQ:
+      g_debug_skip.store(role);
+      return FA_OK;
+    default:
+      return FA_ERR_INVALID_ARG;
+  }
+}
+
 fa_status_t fa_debug_timeout_probe(unsigned long long limit_ns, cudaStream_t stream) {
   fa_status_t st = FA_OK;
   DeviceState* ds = device_state(&st);
   if (!ds) return st;
-  if (limit_ns == 0 || limit_ns > 10000000000ull) return FA_ERR_INVALID_ARG;
+  if (limit_ns == 0 || limit_ns > kMaxWaitLimitNs) return FA_ERR_INVALID_ARG;
   return from_cuda(launch_timeout_probe(ds->status, limit_ns, stream));
 }
 
@@ -623,10 +663,12 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[FA_BWD_NOALLOC_
 
 namespace {
 
+// Device address of g_noalloc_scratch per device, looked up on the first
+// call that finds the device usable. A failed lookup is not remembered, so a
+// later call tries again.
 struct NoAllocState {
-  std::once_flag once;
-  cudaError_t error = cudaSuccess;
-  void* scratch = nullptr;  // device address of g_noalloc_scratch on this device
+  std::mutex mu;
+  void* scratch = nullptr;
 };
 NoAllocState g_noalloc[kMaxDevices];
 
@@ -641,16 +683,23 @@ extern "C" fa_status_t fa_bwd_noalloc(const void* q, const void* k, const void* 
   if (st != FA_OK) return st;
   if (empty) return FA_OK;
   if (fa_bwd_workspace_size(B, H, N, d) > FA_BWD_NOALLOC_SCRATCH_BYTES) return FA_ERR_WORKSPACE;
+  // The device must be one the kernels run on (sm_103a) before its copy of
+  // the array is looked up.
+  DeviceState* ds = device_state(&st);
+  if (!ds) return st;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
   NoAllocState& ns = g_noalloc[dev];
-  // Once per device, with that device current: the array's device address.
-  // In host code the symbol itself is only a host-side stand-in.
-  std::call_once(ns.once, [&ns] {
-    ns.error = cudaGetSymbolAddress(&ns.scratch, g_noalloc_scratch);
-  });
-  if (ns.error != cudaSuccess || ns.scratch == nullptr) return FA_ERR_CUDA;
-  return fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, causal, scale, ns.scratch,
-                FA_BWD_NOALLOC_SCRATCH_BYTES, stream);
+  void* scratch = nullptr;
+  {
+    // Once per device, with that device current: the array's device address.
+    // In host code the symbol itself is only a host-side stand-in.
+    std::lock_guard<std::mutex> lock(ns.mu);
+    if (!ns.scratch && cudaGetSymbolAddress(&ns.scratch, g_noalloc_scratch) != cudaSuccess) ns.scratch = nullptr;
+    scratch = ns.scratch;
+  }
+  if (!scratch) return FA_ERR_CUDA;
+  return fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, causal, scale, scratch, FA_BWD_NOALLOC_SCRATCH_BYTES,
+                stream);
 }
 

@@ -89,6 +89,7 @@ struct BwdShared {
   uint64_t qdo_full[4], qdo_empty[4];
   uint64_t s_full, dp_full, pa_ready, ds_ready, pv_done, dq_full, dq_free, acc_done;
   uint64_t acc_free;  // dK, dV of the previous item read out of TMEM
+  uint64_t mma_drain;  // the MMA thread's last commit: all its MMAs done before the CTA exits
   // Work-item queue filled by the load thread (item >= BH*T ends the loop).
   uint64_t item_full[4], item_empty[4];
   int item_ring[4];
@@ -298,13 +299,15 @@ __device__ void bwd_load_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sK, ui
       aborted = true;
       break;
     }
-    mbar_arrive_expect_tx(&sh.kv_full, 2 * C::TILE_BYTES);
+    if (!debug_skip_here(p.debug_skip, WHERE_BWD_LOAD, items == 0)) {  // test hook
+      mbar_arrive_expect_tx(&sh.kv_full, 2 * C::TILE_BYTES);
 #pragma unroll
-    for (int c = 0; c < C::CHUNKS; ++c) {
-      tma_load_3d(sK + c * C::CHUNK_BYTES, &p.tmK, &sh.kv_full, c * 64, wk.j * 128, wk.bh);
-      tma_load_3d(sV + c * C::CHUNK_BYTES, &p.tmV, &sh.kv_full, c * 64, wk.j * 128, wk.bh);
+      for (int c = 0; c < C::CHUNKS; ++c) {
+        tma_load_3d(sK + c * C::CHUNK_BYTES, &p.tmK, &sh.kv_full, c * 64, wk.j * 128, wk.bh);
+        tma_load_3d(sV + c * C::CHUNK_BYTES, &p.tmV, &sh.kv_full, c * 64, wk.j * 128, wk.bh);
+      }
+      ++kv_issued;
     }
-    ++kv_issued;
     for (int n = 1; n < n_iter; ++n) {
       wk.advance(pos);
       if (!load_qdo(g + n, pos.i, pos.bh)) {
@@ -317,13 +320,12 @@ __device__ void bwd_load_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sK, ui
     if (!aborted) item = claim_item(p.sched);
   }
   finish_claiming(p.sched);
-  const int zero = 0;
-  if (aborted) {
-    record_timeout(p.status, &sh.abort_flag, WHERE_BWD_LOAD);
-    for (int n = max(0, issued - C::QST); n < issued; ++n)
-      mbar_wait(&sh.qdo_full[n % C::QST], (n / C::QST) & 1, &zero, lim);
-  }
-  if (kv_issued > 0) mbar_wait(&sh.kv_full, (kv_issued - 1) & 1, &zero, lim);
+  if (aborted) record_timeout(p.status, &sh.abort_flag, WHERE_BWD_LOAD);
+  // The copies already issued land before the CTA can exit (after an abort
+  // no consumer may wait for them).
+  for (int n = max(0, issued - C::QST); n < issued; ++n)
+    drain_wait(&sh.qdo_full[n % C::QST], (n / C::QST) & 1, lim);
+  if (kv_issued > 0) drain_wait(&sh.kv_full, (kv_issued - 1) & 1, lim);
 }
 
 // One thread issues every MMA. Per query tile n of an item (global index g;
@@ -357,7 +359,10 @@ __device__ void bwd_mma_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sK, uin
       umma_ss(tmem + d_col, desc_add(ad, off), desc_add(bd, off), kIdescSq, ks > 0 ? 1u : 0u);
     }
   };
-  auto fail = [&]() { record_timeout(p.status, &sh.abort_flag, WHERE_BWD_MMA); };
+  auto fail = [&]() {
+    record_timeout(p.status, &sh.abort_flag, WHERE_BWD_MMA);
+    drain_mmas(&sh.mma_drain, lim);
+  };
 
   int g = 0, items = 0;
   while (true) {
@@ -374,7 +379,7 @@ __device__ void bwd_mma_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sK, uin
     if (g > 0 && !mbar_wait(&sh.pv_done, (g - 1) & 1, &sh.abort_flag, lim)) return fail();
     tc_fence_after_sync();
     issue_sq(C::REG_A, k_addr, q_addr + s0 * C::TILE_BYTES);  // S^T(first)
-    umma_commit(&sh.s_full);
+    if (!debug_skip_here(p.debug_skip, WHERE_BWD_MMA, g == 0)) umma_commit(&sh.s_full);  // test hook
     if (DQ && g > 0 && !mbar_wait(&sh.dq_free, (g - 1) & 1, &sh.abort_flag, lim)) return fail();
     tc_fence_after_sync();
     issue_sq(C::REG_B, v_addr, do_addr + s0 * C::TILE_BYTES);  // dP^T(first)
@@ -439,6 +444,9 @@ __device__ void bwd_mma_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sK, uin
     umma_commit(&sh.acc_done);
     ++items;
   }
+  // Normally the epilogues have waited for the last products; if a softmax
+  // warpgroup gave up, nothing has.
+  drain_mmas(&sh.mma_drain, lim);
 }
 
 // Warpgroup w (w = 0, 1) owns query columns [64w, 64w + 64) of every tile:
@@ -541,7 +549,7 @@ __device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS
     tmem_st32(tA, pk);  // columns [64w, 64w + 32): already read
     tmem_st_wait();
     tc_fence_before_sync();
-    mbar_arrive(&sh.pa_ready);
+    if (!debug_skip_here(p.debug_skip, WHERE_BWD_SOFTMAX, w == 0 && g == 0)) mbar_arrive(&sh.pa_ready);  // test hook
   };
 
   // ---- phase B: dS^T = P^T o (dP^T - D) * scale -> smem (bf16, swizzled)
@@ -602,7 +610,7 @@ __device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS
       tmem_ld32(tB + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
       tmem_ld_wait();
       tc_fence_before_sync();
-      mbar_arrive(&sh.dq_free);
+      if (!debug_skip_here(p.debug_skip, WHERE_BWD_DQ, w == 0 && g == 0)) mbar_arrive(&sh.dq_free);  // test hook
 #pragma unroll
       for (int c = 0; c < 64; ++c) red_add_f32(dst + static_cast<size_t>(c) * HD, __uint_as_float(v[c]));
     } else {
@@ -614,7 +622,7 @@ __device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS
         tmem_ld32(tmem + lane_base + C::REG_B + 32 * w, v);
         tmem_ld_wait();
         tc_fence_before_sync();
-        mbar_arrive(&sh.dq_free);
+        if (!debug_skip_here(p.debug_skip, WHERE_BWD_DQ, w == 0 && g == 0)) mbar_arrive(&sh.dq_free);  // test hook
       }
       if (r == 0) tma_store_wait_read_all();  // the previous reduce has read the chunk
       named_barrier_sync(bar_id, 128);
@@ -772,6 +780,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
     mbar_init(&sh.dq_free, 256);
     mbar_init(&sh.acc_done, 1);
     mbar_init(&sh.acc_free, 256);
+    mbar_init(&sh.mma_drain, 1);
     for (int s = 0; s < kItemSlots; ++s) {
       mbar_init(&sh.item_full[s], 1);
       mbar_init(&sh.item_empty[s], kItemConsumers);

@@ -49,6 +49,7 @@ struct Cfg256 {
 struct Shared256 {
   uint64_t kv_full, q_full, q_empty, do_full, do_empty;
   uint64_t s_full, dp_full, pa_ready, ds_ready, pv_done, dq_full, dq_free, acc_done;
+  uint64_t mma_drain;  // the MMA thread's last commit: all its MMAs done before the CTA exits
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -105,7 +106,6 @@ __device__ void load_role(const BwdLaunch& p, Shared256& sh, uint8_t* sK, uint8_
     tma_load_3d(sK + c * C::KV_CHUNK, &p.tmK, &sh.kv_full, c * 64, wk.j * 128, wk.bh);
     tma_load_3d(sV + c * C::KV_CHUNK, &p.tmV, &sh.kv_full, c * 64, wk.j * 128, wk.bh);
   }
-  const int zero = 0;
   const int n_iter = wk.n_iter();
   int q_issued = 0, do_issued = 0;
   bool aborted = false;
@@ -129,12 +129,11 @@ __device__ void load_role(const BwdLaunch& p, Shared256& sh, uint8_t* sK, uint8_
     for (int c = 0; c < 4; ++c) tma_load_3d(sdO + c * C::Q_CHUNK, &p.tmdO, &sh.do_full, c * 64, i * C::BQ, qbh);
     ++do_issued;
   }
-  if (aborted) {
-    record_timeout(p.status, &sh.abort_flag, WHERE_BWD_LOAD);
-    if (q_issued > 0) mbar_wait(&sh.q_full, (q_issued - 1) & 1, &zero, p.wait_limit_ns);
-    if (do_issued > 0) mbar_wait(&sh.do_full, (do_issued - 1) & 1, &zero, p.wait_limit_ns);
-  }
-  mbar_wait(&sh.kv_full, 0, &zero, p.wait_limit_ns);
+  if (aborted) record_timeout(p.status, &sh.abort_flag, WHERE_BWD_LOAD);
+  // The copies already issued land before the CTA can exit.
+  if (q_issued > 0) drain_wait(&sh.q_full, (q_issued - 1) & 1, p.wait_limit_ns);
+  if (do_issued > 0) drain_wait(&sh.do_full, (do_issued - 1) & 1, p.wait_limit_ns);
+  drain_wait(&sh.kv_full, 0, p.wait_limit_ns);
 }
 
 template <bool CAUSAL>
@@ -148,7 +147,10 @@ __device__ void mma_role(const BwdLaunch& p, Shared256& sh, uint8_t* sK, uint8_t
                  ds_addr = smem_u32(sDS);
   const uint64_t lim = p.wait_limit_ns;
   const int n_iter = wk.n_iter();
-  auto fail = [&]() { record_timeout(p.status, &sh.abort_flag, WHERE_BWD_MMA); };
+  auto fail = [&]() {
+    record_timeout(p.status, &sh.abort_flag, WHERE_BWD_MMA);
+    drain_mmas(&sh.mma_drain, lim);
+  };
 
   // D = A (128 x 256, K-major) * B (64 x 256, K-major)^T
   auto issue_sq = [&](uint32_t d_col, uint32_t a_addr, uint32_t b_addr) {
@@ -202,6 +204,7 @@ __device__ void mma_role(const BwdLaunch& p, Shared256& sh, uint8_t* sK, uint8_t
     umma_commit(&sh.dq_full);
   }
   umma_commit(&sh.acc_done);
+  drain_mmas(&sh.mma_drain, lim);  // if a softmax warpgroup gave up, nothing waits for the last products
 }
 
 template <bool CAUSAL>
@@ -399,6 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd256_kernel(const __grid_con
     mbar_init(&sh.dq_full, 1);
     mbar_init(&sh.dq_free, 256);
     mbar_init(&sh.acc_done, 1);
+    mbar_init(&sh.mma_drain, 1);
     sh.abort_flag = 0;
     fence_mbarrier_init();
   }

@@ -70,6 +70,7 @@ struct DqShared {
   // Tile t+2 needs dP(t+2), issued after the wait, so one barrier per tile
   // parity can be at most one phase ahead of its waiter.
   uint64_t dp_full, dp_free, ds_ready[2], dq_done, acc_done, acc_free;
+  uint64_t mma_drain;  // the MMA thread's last commit: all its MMAs done before the CTA exits
   uint64_t item_full[kItemSlots], item_empty[kItemSlots];
   int item_ring[kItemSlots];
   uint32_t tmem_base;
@@ -110,6 +111,7 @@ __device__ void dq_load_role(const BwdLaunch& p, DqShared& sh, uint8_t* sQ, uint
   const int total = p.BH * T;
   const uint64_t lim = p.wait_limit_ns;
   int u = 0, kv = 0, q_issued = 0;  // kv: K/V tiles loaded
+  bool k_extra = false;              // K of tile kv issued, its V not (abort in between)
   bool aborted = false;
   auto load_kv = [&](int j, int kvh) -> bool {
     const int ks = kv % C::KST, vs = kv % C::VST;
@@ -118,12 +120,14 @@ __device__ void dq_load_role(const BwdLaunch& p, DqShared& sh, uint8_t* sQ, uint
 #pragma unroll
     for (int c = 0; c < C::CHUNKS; ++c)
       tma_load_3d(sK + ks * C::TILE_BYTES + c * C::CHUNK_BYTES, &p.tmK, &sh.k_full[ks], c * 64, j * 128, kvh);
+    k_extra = true;
     if (kv >= C::VST && !mbar_wait(&sh.v_empty[vs], ((kv / C::VST) - 1) & 1, &sh.abort_flag, lim)) return false;
     mbar_arrive_expect_tx(&sh.v_full[vs], C::TILE_BYTES);
 #pragma unroll
     for (int c = 0; c < C::CHUNKS; ++c)
       tma_load_3d(sV + vs * C::TILE_BYTES + c * C::CHUNK_BYTES, &p.tmV, &sh.v_full[vs], c * 64, j * 128, kvh);
     ++kv;
+    k_extra = false;
     return true;
   };
   int item = blockIdx.x;  // the grid never exceeds the item count
@@ -140,26 +144,28 @@ __device__ void dq_load_role(const BwdLaunch& p, DqShared& sh, uint8_t* sQ, uint
       aborted = true;
       break;
     }
-    mbar_arrive_expect_tx(&sh.q_full, 2 * C::TILE_BYTES);
+    if (!debug_skip_here(p.debug_skip, WHERE_BWD_LOAD, u == 0)) {  // test hook
+      mbar_arrive_expect_tx(&sh.q_full, 2 * C::TILE_BYTES);
 #pragma unroll
-    for (int c = 0; c < C::CHUNKS; ++c) {
-      tma_load_3d(sQ + c * C::CHUNK_BYTES, &p.tmQ, &sh.q_full, c * 64, wk.i * 128, wk.bh);
-      tma_load_3d(sdO + c * C::CHUNK_BYTES, &p.tmdO, &sh.q_full, c * 64, wk.i * 128, wk.bh);
+      for (int c = 0; c < C::CHUNKS; ++c) {
+        tma_load_3d(sQ + c * C::CHUNK_BYTES, &p.tmQ, &sh.q_full, c * 64, wk.i * 128, wk.bh);
+        tma_load_3d(sdO + c * C::CHUNK_BYTES, &p.tmdO, &sh.q_full, c * 64, wk.i * 128, wk.bh);
+      }
+      ++q_issued;
     }
-    ++q_issued;
     for (int j = 1; j < wk.nkv && !aborted; ++j) aborted = !load_kv(j, kvh);
     ++u;
     if (!aborted) item = claim_item(p.sched + 2);
   }
   finish_claiming(p.sched + 2);
-  const int zero = 0;
-  if (aborted) {
-    record_timeout(p.status, &sh.abort_flag, WHERE_BWD_LOAD);
-    // the K and V copies of the last tiles may still be in flight
-    for (int n = std::max(0, kv - C::KST); n < kv; ++n) mbar_wait(&sh.k_full[n % C::KST], (n / C::KST) & 1, &zero, lim);
-    for (int n = std::max(0, kv - C::VST); n < kv; ++n) mbar_wait(&sh.v_full[n % C::VST], (n / C::VST) & 1, &zero, lim);
-  }
-  if (q_issued > 0) mbar_wait(&sh.q_full, (q_issued - 1) & 1, &zero, lim);
+  if (aborted) record_timeout(p.status, &sh.abort_flag, WHERE_BWD_LOAD);
+  // The copies already issued land before the CTA can exit (after an abort
+  // no consumer may wait for them). An aborted load_kv may have issued K_j
+  // without V_j: kv counts only tiles whose K and V were both issued.
+  for (int n = std::max(0, kv - C::KST); n < kv; ++n) drain_wait(&sh.k_full[n % C::KST], (n / C::KST) & 1, lim);
+  if (k_extra) drain_wait(&sh.k_full[kv % C::KST], (kv / C::KST) & 1, lim);
+  for (int n = std::max(0, kv - C::VST); n < kv; ++n) drain_wait(&sh.v_full[n % C::VST], (n / C::VST) & 1, lim);
+  if (q_issued > 0) drain_wait(&sh.q_full, (q_issued - 1) & 1, lim);
 }
 
 // One thread issues every MMA. Per key tile j (global tile t):
@@ -187,7 +193,10 @@ __device__ void dq_mma_role(const BwdLaunch& p, DqShared& sh, uint8_t* sQ, uint8
       umma_ss(tmem + d_col, desc_add(ad, off), desc_add(bd, off), kIdescSq, ks > 0 ? 1u : 0u);
     }
   };
-  auto fail = [&]() { record_timeout(p.status, &sh.abort_flag, WHERE_BWD_MMA); };
+  auto fail = [&]() {
+    record_timeout(p.status, &sh.abort_flag, WHERE_BWD_MMA);
+    drain_mmas(&sh.mma_drain, lim);
+  };
 
   // S(t) into buffer t & 1, which tile t - 2 used.
   // done_tile: the latest dQ product issued (tile t - 2 inside an item, t - 1
@@ -199,7 +208,7 @@ __device__ void dq_mma_role(const BwdLaunch& p, DqShared& sh, uint8_t* sQ, uint8
     if (t >= 2 && !mbar_wait(&sh.dq_done, done_tile & 1, &sh.abort_flag, lim)) return false;
     tc_fence_after_sync();
     issue_sq(C::s_col(t & 1), q_addr, k_addr + stage * C::TILE_BYTES);
-    umma_commit(&sh.s_full[t & 1]);
+    if (!debug_skip_here(p.debug_skip, WHERE_BWD_MMA, t == 0)) umma_commit(&sh.s_full[t & 1]);  // test hook
     return true;
   };
   // dP(t) over dP(t - 1): wait until phase B(t - 1) loaded it.
@@ -249,6 +258,9 @@ __device__ void dq_mma_role(const BwdLaunch& p, DqShared& sh, uint8_t* sQ, uint8
     umma_commit(&sh.acc_done);
     ++u;
   }
+  // Normally the epilogues have waited for the last products; if a softmax
+  // warpgroup gave up, nothing has.
+  drain_mmas(&sh.mma_drain, lim);
 }
 
 // Warpgroup w owns key columns [64w, 64w + 64) of every tile; thread r owns
@@ -364,7 +376,8 @@ __device__ void dq_softmax_role(const BwdLaunch& p, DqShared& sh, uint32_t tmem,
         tmem_st32(tS0 + 128u * uint32_t(t & 1), ds);
         tmem_st_wait();
         tc_fence_before_sync();
-        mbar_arrive(&sh.ds_ready[t & 1]);
+        if (!debug_skip_here(p.debug_skip, WHERE_BWD_SOFTMAX, w == 0 && t == 0))  // test hook
+          mbar_arrive(&sh.ds_ready[t & 1]);
       }
     }
     const int item_next = next_item(u + 1);
@@ -428,6 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
     mbar_init(&sh.dq_done, 1);
     mbar_init(&sh.acc_done, 1);
     mbar_init(&sh.acc_free, 256);
+    mbar_init(&sh.mma_drain, 1);
     for (int s = 0; s < kItemSlots; ++s) {
       mbar_init(&sh.item_full[s], 1);
       mbar_init(&sh.item_empty[s], kItemConsumers);

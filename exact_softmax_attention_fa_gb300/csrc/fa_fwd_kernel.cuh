@@ -82,6 +82,7 @@ struct FwdShared {
   uint64_t q_full[2], q_free[2];  // per query-tile slot
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
   uint64_t s_full[2], p_full[2], pv_done[2], o_free[2];
+  uint64_t mma_drain;  // the MMA thread's last commit: all its MMAs done before the CTA exits
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -211,6 +212,7 @@ __device__ void fwd_load_role(const FwdLaunch& p, FwdShared& sh, uint8_t* sQ, ui
           mbar_arrive(&sh.q_full[t]);
           continue;
         }
+        if (debug_skip_here(p.debug_skip, WHERE_FWD_LOAD, items == 0 && t == 0)) continue;  // test hook
         mbar_arrive_expect_tx(&sh.q_full[t], C::TILE_BYTES);
 #pragma unroll
         for (int c = 0; c < C::CHUNKS; ++c)
@@ -269,17 +271,15 @@ __device__ void fwd_load_role(const FwdLaunch& p, FwdShared& sh, uint8_t* sQ, ui
     if (aborted) break;
     ++items;
   }
-  if (aborted) {
-    record_timeout(p.status, &sh.abort_flag, WHERE_FWD_LOAD);
-    // Let the copies already issued land before the CTA can exit.
-    const int zero = 0;
-    for (int jj = max(0, k_issued - C::KST); jj < k_issued; ++jj)
-      mbar_wait(&sh.k_full[jj % C::KST], (jj / C::KST) & 1, &zero, lim);
-    for (int jj = max(0, v_issued - C::VST); jj < v_issued; ++jj)
-      mbar_wait(&sh.v_full[jj % C::VST], (jj / C::VST) & 1, &zero, lim);
-    for (int t = 0; t < C::NT; ++t)
-      if (q_mask >> t & 1) mbar_wait(&sh.q_full[t], q_item & 1, &zero, lim);
-  }
+  if (aborted) record_timeout(p.status, &sh.abort_flag, WHERE_FWD_LOAD);
+  // The copies already issued land before the CTA can exit (after an abort
+  // no consumer may wait for them).
+  for (int jj = max(0, k_issued - C::KST); jj < k_issued; ++jj)
+    drain_wait(&sh.k_full[jj % C::KST], (jj / C::KST) & 1, lim);
+  for (int jj = max(0, v_issued - C::VST); jj < v_issued; ++jj)
+    drain_wait(&sh.v_full[jj % C::VST], (jj / C::VST) & 1, lim);
+  for (int t = 0; t < C::NT; ++t)
+    if (q_mask >> t & 1) drain_wait(&sh.q_full[t], q_item & 1, lim);
 }
 
 // ---------------------------------------------------------------------------
@@ -296,6 +296,7 @@ __device__ void fwd_mma_role(const FwdLaunch& p, FwdShared& sh, uint8_t* sQ, uin
   const int total = total_items<PACK>(p, C::NT);
   const int G = gridDim.x;
 
+  bool first_s = true;
   auto issue_s = [&](int t, int g) {  // g: running K/V tile index
     const uint32_t qa = q_addr + t * C::TILE_BYTES;
     const uint32_t ka = k_addr + (g % C::KST) * C::TILE_BYTES;
@@ -305,7 +306,8 @@ __device__ void fwd_mma_role(const FwdLaunch& p, FwdShared& sh, uint8_t* sQ, uin
       const uint32_t off = (ks >> 2) * C::CHUNK_BYTES + (ks & 3) * 32;
       umma_ss(tmem + C::s_col(t), desc_add(qd, off), desc_add(kd, off), kIdescS, ks > 0 ? 1u : 0u);
     }
-    umma_commit(&sh.s_full[t]);
+    if (!debug_skip_here(p.debug_skip, WHERE_FWD_MMA, first_s)) umma_commit(&sh.s_full[t]);  // test hook
+    first_s = false;
   };
   auto issue_pv = [&](int t, int g, bool first) {
     const uint64_t vd = make_smem_desc_sw128(v_addr + (g % C::VST) * C::TILE_BYTES, C::CHUNK_BYTES, 1024);
@@ -315,7 +317,10 @@ __device__ void fwd_mma_role(const FwdLaunch& p, FwdShared& sh, uint8_t* sQ, uin
               (!first || ks > 0) ? 1u : 0u);
     umma_commit(&sh.pv_done[t]);
   };
-  auto fail = [&]() { record_timeout(p.status, &sh.abort_flag, WHERE_FWD_MMA); };
+  auto fail = [&]() {
+    record_timeout(p.status, &sh.abort_flag, WHERE_FWD_MMA);
+    drain_mmas(&sh.mma_drain, lim);
+  };
 
   int kv = 0;             // running K/V tile index
   int items = 0;          // items processed
@@ -381,6 +386,9 @@ __device__ void fwd_mma_role(const FwdLaunch& p, FwdShared& sh, uint8_t* sQ, uin
     kv += wk.nkv;
     ++items;
   }
+  // Normally the epilogues have waited for the last products; if a softmax
+  // warpgroup gave up, nothing has.
+  drain_mmas(&sh.mma_drain, lim);
 }
 
 // ---------------------------------------------------------------------------
@@ -512,7 +520,7 @@ __device__ void fwd_softmax_role(const FwdLaunch& p, FwdShared& sh, uint8_t* sQ,
       m2 = m_ref;
       tmem_st_wait();
       tc_fence_before_sync();
-      mbar_arrive(&sh.p_full[t]);
+      if (!debug_skip_here(p.debug_skip, WHERE_FWD_SOFTMAX, t == 0 && cnt + j == 0)) mbar_arrive(&sh.p_full[t]);
     }
 
     // Epilogue: wait for the last O~ += P~ V, normalise, store through the
@@ -627,6 +635,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       mbar_init(&sh.o_free[t], 128);
       mbar_init(&sh.q_free[t], 1);
     }
+    mbar_init(&sh.mma_drain, 1);
     sh.abort_flag = 0;
     fence_mbarrier_init();
   }

@@ -43,6 +43,7 @@ struct FwdLaunch {
   float scale_log2;  // scale * log2(e): scores are exponentiated in base 2
   uint64_t wait_limit_ns;
   int num_sms;
+  uint32_t debug_skip;  // test hook: role (WHERE_*) whose first arrival block 0 leaves out; 0 = none
 };
 
 struct BwdLaunch {
@@ -68,6 +69,7 @@ struct BwdLaunch {
   float scale_log2;  // scale * log2(e)
   uint64_t wait_limit_ns;
   int num_sms;
+  uint32_t debug_skip;  // test hook: role (WHERE_*) whose first arrival block 0 leaves out; 0 = none
 };
 
 // Checks of the sizes, flag and scale common to every entry point; *empty is

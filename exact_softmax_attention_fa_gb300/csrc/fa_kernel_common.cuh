@@ -20,6 +20,34 @@ __device__ __forceinline__ void record_timeout(uint32_t* status, int* abort_flag
   *reinterpret_cast<volatile int*>(abort_flag) = 1;
 }
 
+// Waits after an abort for work this CTA has already issued (TMA copies, MMAs
+// committed to a barrier). Such work always completes, so these waits do not
+// use the caller's wait limit, which may be a few milliseconds; they are still
+// bounded, at the larger of that limit and one second.
+constexpr uint64_t kDrainLimitNs = 1000000000ull;
+__device__ __forceinline__ uint64_t drain_limit(uint64_t lim) { return lim > kDrainLimitNs ? lim : kDrainLimitNs; }
+
+// Wait for the latest phase of a barrier whose arrival (a TMA copy's bytes)
+// was issued before an abort. The abort flag is not consulted.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t lim) {
+  const int zero = 0;
+  mbar_wait(bar, parity, &zero, drain_limit(lim));
+}
+
+// MMA issuer leaving early: every tcgen05 MMA it issued must complete before
+// the CTA frees its tensor memory and shared memory. `bar` is a barrier of
+// count 1 used for nothing else (one phase per kernel).
+__device__ __forceinline__ void drain_mmas(uint64_t* bar, uint64_t lim) {
+  umma_commit(bar);
+  drain_wait(bar, 0, lim);
+}
+
+// Test hook: true for the one arrival of `role` in block 0 that a launch with
+// debug_skip == role leaves out (see fa_debug_skip_arrival in fa.h).
+__device__ __forceinline__ bool debug_skip_here(uint32_t debug_skip, uint32_t role, bool first) {
+  return debug_skip == role && first && blockIdx.x == 0;
+}
+
 __device__ __forceinline__ void red_add_f32(float* addr, float a) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(a) : "memory");
 }

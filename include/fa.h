@@ -193,6 +193,10 @@ fa_status_t fa_bwd_gqa(const void* q, const void* k, const void* v, const void* 
  *   L_i * log2(e), a zeroed fp32 dQ accumulator and a zeroed work-item
  *   counter, all in the workspace.
  *   Reads o, lse, dO. HBM-bound.
+ * fa_bwd_preprocess_stats: fa_bwd_preprocess without zeroing the dQ
+ *   accumulator (D, the base-2 logsumexp and the work-item counters only):
+ *   the first phase of fa_bwd_deterministic, whose dQ kernel does not use
+ *   the accumulator. Same arguments.
  * fa_bwd_main: the block loops of reading note 5.3 (key blocks outer): writes
  *   dk and dv, and adds every dS K_j into the workspace's dQ accumulator.
  *   Reads q, k, v, dO and the preprocessed workspace.
@@ -200,13 +204,16 @@ fa_status_t fa_bwd_gqa(const void* q, const void* k, const void* v, const void* 
  */
 fa_status_t fa_bwd_preprocess(const void* o, const float* lse, const void* dO, int B, int H, int N, int d,
                               void* workspace, size_t workspace_bytes, cudaStream_t stream);
+fa_status_t fa_bwd_preprocess_stats(const void* o, const float* lse, const void* dO, int B, int H, int N, int d,
+                                    void* workspace, size_t workspace_bytes, cudaStream_t stream);
 fa_status_t fa_bwd_main(const void* q, const void* k, const void* v, const void* dO, void* dk, void* dv, int B,
                         int H, int N, int d, int causal, float scale, void* workspace, size_t workspace_bytes,
                         cudaStream_t stream);
 /*
  * The phases of the deterministic backward (d = 64, 128; d = 256:
- * FA_ERR_UNSUPPORTED), run after fa_bwd_preprocess on the same workspace:
- * fa_bwd_deterministic == preprocess, dkdv, dq.
+ * FA_ERR_UNSUPPORTED), run after fa_bwd_preprocess_stats (or
+ * fa_bwd_preprocess) on the same workspace:
+ * fa_bwd_deterministic == preprocess_stats, dkdv, dq.
  * fa_bwd_dkdv: the block loops of reading note 5.3 without the dQ products:
  *   writes dk and dv.
  * fa_bwd_dq: per 128-row query tile, recomputes S, P, dP and dS for every key
@@ -236,12 +243,16 @@ fa_status_t fa_bwd_postprocess(void* dq, int B, int H, int N, int d, void* works
  *   Arguments and results are those of fa_bwd, minus the workspace.
  *   Problems whose workspace (fa_bwd_workspace_size) exceeds
  *   FA_BWD_NOALLOC_SCRATCH_BYTES are rejected with FA_ERR_WORKSPACE before
- *   any GPU work; use fa_bwd with your own workspace for those.
+ *   any GPU work; use fa_bwd with your own workspace for those. That size
+ *   always counts the fp32 dQ accumulator (4 d bytes per padded row), also at
+ *   d = 128 where fa_bwd forms dQ without it, so at d = 128 the largest
+ *   accepted problem is about 32k padded rows (B * H * ceil(N / 128) * 128).
+ *   A device that is not sm_103a gives FA_ERR_UNSUPPORTED, as for fa_bwd.
  *   The call allocates nothing: no cudaMalloc/cudaFree and no allocating
  *   library routine.
  *   The first call on a device looks up the scratch array's device address
- *   (once per device, with that device current); make that first call
- *   before any stream capture.
+ *   (once per device, with that device current; a failed lookup is retried
+ *   by the next call); make that first call before any stream capture.
  *   All calls share the one array per device. Each call re-initialises the
  *   parts that must start at zero, so a call never sees the previous call's
  *   values, but calls that overlap on the GPU (different streams or
@@ -334,8 +345,10 @@ fa_status_t fa_get_device_status_detail(unsigned int* word, cudaStream_t stream)
 
 /*
  * Time limit, in nanoseconds, of every device-side pipeline wait in later
- * launches (default 4e9). A wait that exceeds it records FA_ERR_TIMEOUT and
- * the kernel returns early with its outputs undefined.
+ * launches (default 4e9; 0 restores the default; values above 1e10 are
+ * capped at 1e10, so a stalled pipeline always gives up within 10 s). A wait
+ * that exceeds it records FA_ERR_TIMEOUT and the kernel returns early with
+ * its outputs undefined.
  */
 void fa_set_wait_limit_ns(unsigned long long limit_ns);
 
@@ -346,6 +359,22 @@ void fa_set_wait_limit_ns(unsigned long long limit_ns);
  * fa_get_device_status().
  */
 fa_status_t fa_debug_timeout_probe(unsigned long long limit_ns, cudaStream_t stream);
+
+/*
+ * Failure-detection test hook for the real kernels. Off (0) by default. With
+ * a role code of fa_get_device_status_detail (1-3 forward load / MMA /
+ * softmax; 11-14 backward load / MMA / softmax / dQ drain), block 0 of every
+ * later launch of a kernel that has that role leaves out that role's first
+ * arrival on one pipeline barrier (a TMA load it would issue, an MMA
+ * completion it would signal, or a softmax hand-off), so the bounded wait on
+ * that barrier gives up after the wait limit: the launch records
+ * FA_ERR_TIMEOUT, lets every copy and MMA it issued complete, frees its
+ * tensor memory and returns, and its outputs are undefined. Other blocks run
+ * normally. fa_debug_skip_arrival(0) turns the hook off. Process-wide; meant
+ * for tests (set a short limit with fa_set_wait_limit_ns first).
+ * FA_ERR_INVALID_ARG for any other value.
+ */
+fa_status_t fa_debug_skip_arrival(unsigned int role);
 
 /* Library version, major*10000 + minor*100 + patch. */
 int fa_version(void);

@@ -68,12 +68,56 @@ def test_bitwise_reproducible(d, causal):
         assert torch.equal(t1, t2)
 
 
-def test_matches_atomic_backward():
-    x, _ = inputs(1, 4, 777, 128, BASE_SEED + 710)
-    det = run(x, True, scale_f32(128))
-    atomic = run(x, True, scale_f32(128), deterministic=False)
-    for a, b in zip(det, atomic):
-        assert rel_err(to_host64(a), to_host64(b)) <= 1e-2
+def _atomic_phases(x, B, H, N, d, causal, scale):
+    """The exported atomic-dQ phases in order: preprocess, main (dK, dV and
+    the fp32 dQ accumulation with reductions), postprocess (dq = bf16 of the
+    accumulator). At d = 128 fa_bwd itself runs the per-query-tile dQ path, so
+    these phases are reached only through their own entry points."""
+    import exact_softmax_attention_fa_gb300 as fa
+    import torch
+    q, k, v, do = (to_device(x[n]) for n in ("q", "k", "v", "do"))
+    o, lse = fa.forward(q, k, v, causal=causal, scale=scale)
+    ws = torch.empty(fa.fa_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device="cuda")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    fa.fa_bwd_preprocess(o, lse, do, ws)
+    fa.fa_bwd_main(q, k, v, do, dk, dv, causal, scale, ws)
+    fa.fa_bwd_postprocess(dq, ws)
+    assert fa.fa_get_device_status() == 0
+    return dq, dk, dv
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [1, 129, 1000])
+def test_atomic_phases_parity(d, causal, N):
+    # the atomic-dQ main kernel against the oracle, at the head dimension
+    # where fa_bwd does not run it (d = 128) and at d = 64 where it does
+    B, H = 2, 3
+    x, f = inputs(B, H, N, d, BASE_SEED + 710 + N)
+    scale = scale_f32(d)
+    grads = _atomic_phases(x, B, H, N, d, causal, scale)
+    ref = oracle.attention_backward(f["q"], f["k"], f["v"], f["do"], causal, scale)
+    for name, g, r in zip(("dq", "dk", "dv"), grads, ref):
+        e = rel_err(to_host64(g), r)
+        assert e <= TOL_GRAD_REL, (name, e)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_atomic_phases_sweep_point_sampled_heads(causal):
+    # the pages' d = 128 microbenchmark point (B = 2, H = 16, N = 8192); the
+    # oracle computes the sampled heads, whose dq, dk and dv are compared whole
+    from gpu_util import sampled_pairs
+    B, H, N, d = 2, 16, 8192, 128
+    x, f = inputs(B, H, N, d, BASE_SEED + 715)
+    scale = scale_f32(d)
+    heads = sampled_pairs(B, H, BASE_SEED + 716, n_random=1)
+    grads = _atomic_phases(x, B, H, N, d, causal, scale)
+    ref = oracle.attention_backward(f["q"], f["k"], f["v"], f["do"], causal, scale, heads=heads)
+    for name, g, r in zip(("dq", "dk", "dv"), grads, ref):
+        host = to_host64(g)
+        got = np.stack([host[b, h] for b, h in heads])
+        want = np.stack([r[b, h] for b, h in heads])
+        assert rel_err(got, want) <= TOL_GRAD_REL, name
 
 
 def test_several_thousand_rows_sampled_heads():
@@ -100,8 +144,9 @@ def test_head_dim_256_is_unsupported():
     assert fa.fa_get_device_status() == 0
 
 
+@pytest.mark.parametrize("pre", ["fa_bwd_preprocess_stats", "fa_bwd_preprocess"])
 @pytest.mark.parametrize("d", [64, 128])
-def test_phases_compose_to_the_deterministic_backward(d):
+def test_phases_compose_to_the_deterministic_backward(d, pre):
     import exact_softmax_attention_fa_gb300 as fa
     import torch
     x, _ = inputs(1, 3, 700, d, BASE_SEED + 740)
@@ -112,7 +157,7 @@ def test_phases_compose_to_the_deterministic_backward(d):
     a = [torch.empty_like(q) for _ in range(3)]
     b = [torch.empty_like(q) for _ in range(3)]
     fa.fa_bwd_deterministic(q, k, v, o, lse, do, *a, True, scale, ws)
-    fa.fa_bwd_preprocess(o, lse, do, ws)
+    getattr(fa, pre)(o, lse, do, ws)  # the accumulator the full preprocess zeroes is not read
     fa.fa_bwd_dkdv(q, k, v, do, b[1], b[2], True, scale, ws)
     fa.fa_bwd_dq(q, k, v, do, b[0], True, scale, ws)
     assert fa.fa_get_device_status() == 0

@@ -23,7 +23,10 @@ def _rel(a, b):
     return np.abs(a - b).max() / max(np.abs(b).max(), 1e-3)
 
 
-@pytest.mark.parametrize("d,causal", [(64, True), (128, False)])
+# d = 64 and 256 accumulate dQ with reductions (order varies run to run), so
+# they are compared within the gradient tolerance; at d = 128 both entry
+# points run the reproducible dQ kernel and must agree bit for bit.
+@pytest.mark.parametrize("d,causal", [(64, True), (128, False), (128, True), (256, False)])
 def test_noalloc_backward_matches_fa_bwd_twice(cuda_lib, d, causal):
     import torch
     import exact_softmax_attention_fa_gb300 as fa
@@ -44,6 +47,8 @@ def test_noalloc_backward_matches_fa_bwd_twice(cuda_lib, d, causal):
         assert st == 0, lib.fa_status_string(st)
         assert lib.fa_get_device_status(stream) == 0
         for name, got, want in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+            if d == 128:
+                assert torch.equal(got, want), (call, name)
             e = _rel(to_host64(got), to_host64(want))
             assert e <= TOL_GRAD_REL, (call, name, e)
 
