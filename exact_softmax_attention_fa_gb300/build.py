@@ -25,7 +25,8 @@ BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_NAME = "libfa_gb300.so"
 LIB_PATH = os.path.join(PKG_DIR, LIB_NAME)
 
-SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_fwd_pack.cu", "fa_bwd.cu", "fa_bwd256.cu", "fa_bwd_dq.cu", "fa_host.cu"]
+SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_fwd_pack.cu", "fa_bwd.cu", "fa_bwd256.cu", "fa_bwd_dq.cu", "fa_bwd_dq256.cu",
+           "fa_host.cu"]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH_FLAGS + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
                            "--expt-relaxed-constexpr", "-I", INCLUDE]

@@ -483,7 +483,6 @@ fa_status_t fa_bwd_gqa_deterministic(const void* q, const void* k, const void* v
   bool empty = false;
   fa_status_t st = check_common(B, Hq, N, d, causal, scale, &empty);
   if (st != FA_OK) return st;
-  if (d == 256) return FA_ERR_UNSUPPORTED;
   st = check_heads(Hq, Hkv);
   if (st != FA_OK) return st;
   if (empty) return FA_OK;
@@ -564,8 +563,7 @@ fa_status_t fa_bwd_dkdv(const void* q, const void* k, const void* v, const void*
   bool empty = false;
   fa_status_t st = check_common(B, H, N, d, causal, scale, &empty);
   if (st != FA_OK) return st;
-  if (d == 256) return FA_ERR_UNSUPPORTED;
-  if (empty) return FA_OK;
+    if (empty) return FA_OK;
   if (!q || !k || !v || !dO || !dk || !dv) return FA_ERR_INVALID_ARG;
   BwdLaunch a;
   st = prepare_bwd(BwdTensors{q, k, v, nullptr, dO, nullptr, nullptr, dk, dv}, B, H, H, N, d, causal, scale,
@@ -580,8 +578,7 @@ fa_status_t fa_bwd_dq(const void* q, const void* k, const void* v, const void* d
   bool empty = false;
   fa_status_t st = check_common(B, H, N, d, causal, scale, &empty);
   if (st != FA_OK) return st;
-  if (d == 256) return FA_ERR_UNSUPPORTED;
-  if (empty) return FA_OK;
+    if (empty) return FA_OK;
   if (!q || !k || !v || !dO || !dq) return FA_ERR_INVALID_ARG;
   BwdLaunch a;
   st = prepare_bwd(BwdTensors{q, k, v, nullptr, dO, nullptr, dq, nullptr, nullptr}, B, H, H, N, d, causal, scale,

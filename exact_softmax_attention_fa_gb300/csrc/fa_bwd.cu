@@ -379,7 +379,7 @@ __device__ void bwd_mma_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sK, uin
     if (g > 0 && !mbar_wait(&sh.pv_done, (g - 1) & 1, &sh.abort_flag, lim)) return fail();
     tc_fence_after_sync();
     issue_sq(C::REG_A, k_addr, q_addr + s0 * C::TILE_BYTES);  // S^T(first)
-    if (!debug_skip_here(p.debug_skip, WHERE_BWD_MMA, g == 0)) umma_commit(&sh.s_full);  // test hook
+    umma_commit(&sh.s_full);
     if (DQ && g > 0 && !mbar_wait(&sh.dq_free, (g - 1) & 1, &sh.abort_flag, lim)) return fail();
     tc_fence_after_sync();
     issue_sq(C::REG_B, v_addr, do_addr + s0 * C::TILE_BYTES);  // dP^T(first)
@@ -549,7 +549,7 @@ __device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS
     tmem_st32(tA, pk);  // columns [64w, 64w + 32): already read
     tmem_st_wait();
     tc_fence_before_sync();
-    if (!debug_skip_here(p.debug_skip, WHERE_BWD_SOFTMAX, w == 0 && g == 0)) mbar_arrive(&sh.pa_ready);  // test hook
+    mbar_arrive(&sh.pa_ready);
   };
 
   // ---- phase B: dS^T = P^T o (dP^T - D) * scale -> smem (bf16, swizzled)
@@ -610,7 +610,7 @@ __device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS
       tmem_ld32(tB + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
       tmem_ld_wait();
       tc_fence_before_sync();
-      if (!debug_skip_here(p.debug_skip, WHERE_BWD_DQ, w == 0 && g == 0)) mbar_arrive(&sh.dq_free);  // test hook
+      mbar_arrive(&sh.dq_free);
 #pragma unroll
       for (int c = 0; c < 64; ++c) red_add_f32(dst + static_cast<size_t>(c) * HD, __uint_as_float(v[c]));
     } else {
@@ -622,7 +622,7 @@ __device__ void bwd_softmax_role(const BwdLaunch& p, BwdShared& sh, uint8_t* sDS
         tmem_ld32(tmem + lane_base + C::REG_B + 32 * w, v);
         tmem_ld_wait();
         tc_fence_before_sync();
-        if (!debug_skip_here(p.debug_skip, WHERE_BWD_DQ, w == 0 && g == 0)) mbar_arrive(&sh.dq_free);  // test hook
+        mbar_arrive(&sh.dq_free);
       }
       if (r == 0) tma_store_wait_read_all();  // the previous reduce has read the chunk
       named_barrier_sync(bar_id, 128);
@@ -771,13 +771,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
       mbar_init(&sh.qdo_full[s], 1);
       mbar_init(&sh.qdo_empty[s], 1);
     }
-    mbar_init(&sh.s_full, 1);
+    // test hook: the S, P or dQ barrier waits for one arrival too many
+    mbar_init(&sh.s_full, 1 + debug_extra(p.debug_skip, WHERE_BWD_MMA));
     mbar_init(&sh.dp_full, 1);
-    mbar_init(&sh.pa_ready, 256);
+    mbar_init(&sh.pa_ready, 256 + debug_extra(p.debug_skip, WHERE_BWD_SOFTMAX));
     mbar_init(&sh.ds_ready, 256);
     mbar_init(&sh.pv_done, 1);
     mbar_init(&sh.dq_full, 1);
-    mbar_init(&sh.dq_free, 256);
+    mbar_init(&sh.dq_free, 256 + debug_extra(p.debug_skip, WHERE_BWD_DQ));
     mbar_init(&sh.acc_done, 1);
     mbar_init(&sh.acc_free, 256);
     mbar_init(&sh.mma_drain, 1);

@@ -161,9 +161,12 @@ __device__ void dq_load_role(const BwdLaunch& p, DqShared& sh, uint8_t* sQ, uint
   if (aborted) record_timeout(p.status, &sh.abort_flag, WHERE_BWD_LOAD);
   // The copies already issued land before the CTA can exit (after an abort
   // no consumer may wait for them). An aborted load_kv may have issued K_j
-  // without V_j: kv counts only tiles whose K and V were both issued.
-  for (int n = std::max(0, kv - C::KST); n < kv; ++n) drain_wait(&sh.k_full[n % C::KST], (n / C::KST) & 1, lim);
-  if (k_extra) drain_wait(&sh.k_full[kv % C::KST], (kv / C::KST) & 1, lim);
+  // without V_j: kv counts only tiles whose K and V were both issued. Each
+  // slot waits for the latest phase issued into it only (an older phase of a
+  // slot can no longer be told apart once a newer one has completed).
+  const int k_last = k_extra ? kv : kv - 1;
+  for (int n = std::max(0, k_last - C::KST + 1); n <= k_last; ++n)
+    drain_wait(&sh.k_full[n % C::KST], (n / C::KST) & 1, lim);
   for (int n = std::max(0, kv - C::VST); n < kv; ++n) drain_wait(&sh.v_full[n % C::VST], (n / C::VST) & 1, lim);
   if (q_issued > 0) drain_wait(&sh.q_full, (q_issued - 1) & 1, lim);
 }
@@ -208,7 +211,7 @@ __device__ void dq_mma_role(const BwdLaunch& p, DqShared& sh, uint8_t* sQ, uint8
     if (t >= 2 && !mbar_wait(&sh.dq_done, done_tile & 1, &sh.abort_flag, lim)) return false;
     tc_fence_after_sync();
     issue_sq(C::s_col(t & 1), q_addr, k_addr + stage * C::TILE_BYTES);
-    if (!debug_skip_here(p.debug_skip, WHERE_BWD_MMA, t == 0)) umma_commit(&sh.s_full[t & 1]);  // test hook
+    umma_commit(&sh.s_full[t & 1]);
     return true;
   };
   // dP(t) over dP(t - 1): wait until phase B(t - 1) loaded it.
@@ -376,8 +379,7 @@ __device__ void dq_softmax_role(const BwdLaunch& p, DqShared& sh, uint32_t tmem,
         tmem_st32(tS0 + 128u * uint32_t(t & 1), ds);
         tmem_st_wait();
         tc_fence_before_sync();
-        if (!debug_skip_here(p.debug_skip, WHERE_BWD_SOFTMAX, w == 0 && t == 0))  // test hook
-          mbar_arrive(&sh.ds_ready[t & 1]);
+        mbar_arrive(&sh.ds_ready[t & 1]);
       }
     }
     const int item_next = next_item(u + 1);
@@ -434,10 +436,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
       mbar_init(&sh.v_full[s], 1);
       mbar_init(&sh.v_empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) mbar_init(&sh.s_full[b], 1);
+    // test hook: buffer 0's S or dS barrier waits for one arrival too many
+    for (int b = 0; b < 2; ++b) mbar_init(&sh.s_full[b], 1 + (b == 0 ? debug_extra(p.debug_skip, WHERE_BWD_MMA) : 0u));
     mbar_init(&sh.dp_full, 1);
     mbar_init(&sh.dp_free, 256);
-    for (int b = 0; b < 2; ++b) mbar_init(&sh.ds_ready[b], 256);
+    for (int b = 0; b < 2; ++b)
+      mbar_init(&sh.ds_ready[b], 256 + (b == 0 ? debug_extra(p.debug_skip, WHERE_BWD_SOFTMAX) : 0u));
     mbar_init(&sh.dq_done, 1);
     mbar_init(&sh.acc_done, 1);
     mbar_init(&sh.acc_free, 256);
@@ -490,6 +494,7 @@ cudaError_t launch_bwd_dq(const BwdLaunch& a, cudaStream_t stream) {
   switch (a.d) {
     case 64: return a.causal ? launch_t<64, true>(a, stream) : launch_t<64, false>(a, stream);
     case 128: return a.causal ? launch_t<128, true>(a, stream) : launch_t<128, false>(a, stream);
+    case 256: return launch_bwd_dq256(a, stream);
     default: return cudaErrorNotSupported;
   }
 }

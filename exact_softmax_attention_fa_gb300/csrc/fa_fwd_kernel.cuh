@@ -296,7 +296,6 @@ __device__ void fwd_mma_role(const FwdLaunch& p, FwdShared& sh, uint8_t* sQ, uin
   const int total = total_items<PACK>(p, C::NT);
   const int G = gridDim.x;
 
-  bool first_s = true;
   auto issue_s = [&](int t, int g) {  // g: running K/V tile index
     const uint32_t qa = q_addr + t * C::TILE_BYTES;
     const uint32_t ka = k_addr + (g % C::KST) * C::TILE_BYTES;
@@ -306,8 +305,7 @@ __device__ void fwd_mma_role(const FwdLaunch& p, FwdShared& sh, uint8_t* sQ, uin
       const uint32_t off = (ks >> 2) * C::CHUNK_BYTES + (ks & 3) * 32;
       umma_ss(tmem + C::s_col(t), desc_add(qd, off), desc_add(kd, off), kIdescS, ks > 0 ? 1u : 0u);
     }
-    if (!debug_skip_here(p.debug_skip, WHERE_FWD_MMA, first_s)) umma_commit(&sh.s_full[t]);  // test hook
-    first_s = false;
+    umma_commit(&sh.s_full[t]);
   };
   auto issue_pv = [&](int t, int g, bool first) {
     const uint64_t vd = make_smem_desc_sw128(v_addr + (g % C::VST) * C::TILE_BYTES, C::CHUNK_BYTES, 1024);
@@ -520,7 +518,7 @@ __device__ void fwd_softmax_role(const FwdLaunch& p, FwdShared& sh, uint8_t* sQ,
       m2 = m_ref;
       tmem_st_wait();
       tc_fence_before_sync();
-      if (!debug_skip_here(p.debug_skip, WHERE_FWD_SOFTMAX, t == 0 && cnt + j == 0)) mbar_arrive(&sh.p_full[t]);
+      mbar_arrive(&sh.p_full[t]);
     }
 
     // Epilogue: wait for the last O~ += P~ V, normalise, store through the
@@ -629,8 +627,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       mbar_init(&sh.v_empty[i], 1);
     }
     for (int t = 0; t < 2; ++t) {
-      mbar_init(&sh.s_full[t], 1);
-      mbar_init(&sh.p_full[t], 128);
+      // test hook: slot 0's S or P barrier waits for one arrival too many
+      mbar_init(&sh.s_full[t], 1 + (t == 0 ? debug_extra(p.debug_skip, WHERE_FWD_MMA) : 0u));
+      mbar_init(&sh.p_full[t], 128 + (t == 0 ? debug_extra(p.debug_skip, WHERE_FWD_SOFTMAX) : 0u));
       mbar_init(&sh.pv_done[t], 1);
       mbar_init(&sh.o_free[t], 128);
       mbar_init(&sh.q_free[t], 1);

@@ -87,6 +87,7 @@ cudaError_t launch_bwd_main(const BwdLaunch& a, cudaStream_t stream);  // dK, dV
 cudaError_t launch_bwd_post(const BwdLaunch& a, cudaStream_t stream);  // dQ = bf16(accumulator)
 cudaError_t launch_bwd_main_d256(const BwdLaunch& a, cudaStream_t stream);  // fa_bwd256.cu
 cudaError_t launch_bwd_dq(const BwdLaunch& a, cudaStream_t stream);  // fa_bwd_dq.cu: dq without atomics
+cudaError_t launch_bwd_dq256(const BwdLaunch& a, cudaStream_t stream);  // fa_bwd_dq256.cu: the same at d = 256
 cudaError_t launch_timeout_probe(uint32_t* status, uint64_t limit_ns, cudaStream_t stream);
 
 }  // namespace fa

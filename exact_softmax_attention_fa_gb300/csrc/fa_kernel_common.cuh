@@ -27,11 +27,17 @@ __device__ __forceinline__ void record_timeout(uint32_t* status, int* abort_flag
 constexpr uint64_t kDrainLimitNs = 1000000000ull;
 __device__ __forceinline__ uint64_t drain_limit(uint64_t lim) { return lim > kDrainLimitNs ? lim : kDrainLimitNs; }
 
-// Wait for the latest phase of a barrier whose arrival (a TMA copy's bytes)
-// was issued before an abort. The abort flag is not consulted.
+// Wait for the latest phase of a barrier whose arrival (a TMA copy's bytes,
+// an MMA commit) was issued earlier; the abort flag is not consulted. The
+// role is otherwise idle here while other warps of its sub-partition may
+// still be working, so it sleeps between polls instead of spinning.
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t lim) {
-  const int zero = 0;
-  mbar_wait(bar, parity, &zero, drain_limit(lim));
+  if (mbar_try_wait(bar, parity)) return;
+  const uint64_t t0 = global_timer_ns(), limit = drain_limit(lim);
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > limit) return;
+    __nanosleep(256);
+  }
 }
 
 // MMA issuer leaving early: every tcgen05 MMA it issued must complete before
@@ -42,10 +48,16 @@ __device__ __forceinline__ void drain_mmas(uint64_t* bar, uint64_t lim) {
   drain_wait(bar, 0, lim);
 }
 
-// Test hook: true for the one arrival of `role` in block 0 that a launch with
-// debug_skip == role leaves out (see fa_debug_skip_arrival in fa.h).
+// Test hook (fa_debug_skip_arrival in fa.h), in two forms that cost nothing
+// on the kernels' per-tile paths: a load role leaves out one of its copies
+// (debug_skip_here, checked once per item), and an MMA or softmax role's
+// barrier is initialised in block 0 to expect one more arrival than the role
+// makes (debug_extra), so the first wait on it gives up.
 __device__ __forceinline__ bool debug_skip_here(uint32_t debug_skip, uint32_t role, bool first) {
   return debug_skip == role && first && blockIdx.x == 0;
+}
+__device__ __forceinline__ uint32_t debug_extra(uint32_t debug_skip, uint32_t role) {
+  return debug_skip == role && blockIdx.x == 0 ? 1u : 0u;
 }
 
 __device__ __forceinline__ void red_add_f32(float* addr, float a) {

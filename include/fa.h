@@ -169,7 +169,9 @@ size_t fa_bwd_gqa_workspace_size(int B, int Hq, int Hkv, int N, int d);
  * dK and dV. Costs three more 128x128xd products per (query tile, key tile)
  * pair than the atomic version.
  *   Arguments, layouts and workspace as for fa_bwd / fa_bwd_gqa.
- *   d must be 64 or 128 (d = 256: FA_ERR_UNSUPPORTED).
+ *   d = 64, 128 or 256 (at d = 256 the dQ kernel streams K and V in 64-column
+ *   chunks and reads K twice, since Q, dO and a 128-key K tile do not fit in
+ *   shared memory together).
  */
 fa_status_t fa_bwd_deterministic(const void* q, const void* k, const void* v, const void* o, const float* lse,
                                  const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal,
@@ -210,9 +212,8 @@ fa_status_t fa_bwd_main(const void* q, const void* k, const void* v, const void*
                         int H, int N, int d, int causal, float scale, void* workspace, size_t workspace_bytes,
                         cudaStream_t stream);
 /*
- * The phases of the deterministic backward (d = 64, 128; d = 256:
- * FA_ERR_UNSUPPORTED), run after fa_bwd_preprocess_stats (or
- * fa_bwd_preprocess) on the same workspace:
+ * The phases of the deterministic backward (d = 64, 128, 256), run after
+ * fa_bwd_preprocess_stats (or fa_bwd_preprocess) on the same workspace:
  * fa_bwd_deterministic == preprocess_stats, dkdv, dq.
  * fa_bwd_dkdv: the block loops of reading note 5.3 without the dQ products:
  *   writes dk and dv.
@@ -364,10 +365,11 @@ fa_status_t fa_debug_timeout_probe(unsigned long long limit_ns, cudaStream_t str
  * Failure-detection test hook for the real kernels. Off (0) by default. With
  * a role code of fa_get_device_status_detail (1-3 forward load / MMA /
  * softmax; 11-14 backward load / MMA / softmax / dQ drain), block 0 of every
- * later launch of a kernel that has that role leaves out that role's first
- * arrival on one pipeline barrier (a TMA load it would issue, an MMA
- * completion it would signal, or a softmax hand-off), so the bounded wait on
- * that barrier gives up after the wait limit: the launch records
+ * later launch of a kernel that has that role misses one of that role's
+ * hand-offs: a load role leaves out one of its TMA copies; for an MMA,
+ * softmax or dQ-drain role, one barrier it signals is set up to expect one
+ * arrival more than the role makes. Either way the bounded wait on that
+ * barrier gives up after the wait limit: the launch records
  * FA_ERR_TIMEOUT, lets every copy and MMA it issued complete, frees its
  * tensor memory and returns, and its outputs are undefined. Other blocks run
  * normally. fa_debug_skip_arrival(0) turns the hook off. Process-wide; meant

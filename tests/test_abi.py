@@ -99,12 +99,13 @@ def test_deterministic_backward_checks(lib):
     def det(d=64, Hq=4, Hkv=2, ws=P, ws_bytes=1 << 30, ptr=P):
         return lib.fa_bwd_gqa_deterministic(ptr, ptr, ptr, ptr, P, ptr, ptr, ptr, ptr, 1, Hq, Hkv, 128, d, 0, 0.125,
                                             ws, ws_bytes, None)
-    assert det(d=256) == UNSUPPORTED
+    assert det(d=256, ws=0) == WORKSPACE  # d = 256 is supported; the missing workspace is caught
     assert det(d=96) == UNSUPPORTED
     assert det(Hkv=3) == INVALID
     assert det(ptr=0) == INVALID
     assert det(ws=0) == WORKSPACE
-    assert lib.fa_bwd_deterministic(P, P, P, P, P, P, P, P, P, 1, 1, 128, 256, 0, 0.125, P, 1 << 30, None) == UNSUPPORTED
+    assert lib.fa_bwd_deterministic(P, P, P, P, P, P, P, P, P, 1, 1, 128, 256, 0, 0.125, 0, 0, None) == WORKSPACE
+    assert lib.fa_bwd_deterministic(P, P, P, P, P, P, P, P, P, 1, 1, 128, 96, 0, 0.125, P, 1 << 30, None) == UNSUPPORTED
 
 
 def test_split_key_forward_checks(lib):
@@ -130,8 +131,10 @@ def test_split_key_forward_checks(lib):
 
 
 def test_deterministic_phase_checks(lib):
-    assert lib.fa_bwd_dkdv(P, P, P, P, P, P, 1, 1, 128, 256, 0, 0.125, P, 1 << 30, None) == UNSUPPORTED
-    assert lib.fa_bwd_dq(P, P, P, P, P, 1, 1, 128, 256, 0, 0.125, P, 1 << 30, None) == UNSUPPORTED
+    assert lib.fa_bwd_dkdv(P, P, P, P, P, P, 1, 1, 128, 96, 0, 0.125, P, 1 << 30, None) == UNSUPPORTED
+    assert lib.fa_bwd_dq(P, P, P, P, P, 1, 1, 128, 96, 0, 0.125, P, 1 << 30, None) == UNSUPPORTED
+    assert lib.fa_bwd_dkdv(P, P, P, P, 0, P, 1, 1, 128, 256, 0, 0.125, P, 1 << 30, None) == INVALID
+    assert lib.fa_bwd_dq(P, P, P, P, P, 1, 1, 128, 256, 0, 0.125, 0, 0, None) == WORKSPACE
     assert lib.fa_bwd_dkdv(P, P, P, P, 0, P, 1, 1, 128, 64, 0, 0.125, P, 1 << 30, None) == INVALID
     assert lib.fa_bwd_dq(P, P, P, P, P, 1, 1, 128, 64, 0, 0.125, 0, 0, None) == WORKSPACE
     assert lib.fa_bwd_dq(P, P, P, P, P, 1, 1, 128, 64, 2, 0.125, P, 1 << 30, None) == INVALID
@@ -255,3 +258,21 @@ def test_forward_host_entry_checks(lib):
     assert call(nbytes=need - 1) == WORKSPACE
     assert call(buf=P + 64, nbytes=need) == MISALIGNED
     assert call(H=0, ptr=0, lse=0, buf=0, nbytes=0) == OK
+
+
+def test_preprocess_stats_checks(lib):
+    """The stats-only preprocess validates like the full one (no GPU needed)."""
+    assert lib.fa_bwd_preprocess_stats(P, P, P, 1, 1, 128, 96, P, 1 << 30, None) == UNSUPPORTED
+    assert lib.fa_bwd_preprocess_stats(0, P, P, 1, 1, 128, 64, P, 1 << 30, None) == INVALID
+    assert lib.fa_bwd_preprocess_stats(P, P, P, 1, 1, 128, 64, 0, 0, None) == WORKSPACE
+    assert lib.fa_bwd_preprocess_stats(P + 8, P, P, 1, 1, 128, 64, P, 1 << 30, None) == MISALIGNED
+    assert lib.fa_bwd_preprocess_stats(0, 0, 0, 1, 1, 0, 64, 0, 0, None) == OK
+
+
+def test_debug_skip_hook_checks(lib):
+    """Only the role codes of the status word are accepted; 0 turns the hook off."""
+    for bad in (4, 10, 15, 99, 1 << 31):
+        assert lib.fa_debug_skip_arrival(bad) == INVALID
+    for good in (1, 2, 3, 11, 12, 13, 14):
+        assert lib.fa_debug_skip_arrival(good) == OK
+    assert lib.fa_debug_skip_arrival(0) == OK

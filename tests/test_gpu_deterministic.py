@@ -6,7 +6,7 @@ import numpy as np
 import pytest
 
 import oracle
-from attn_inputs import BASE_SEED
+from attn_inputs import BASE_SEED, WORKLOADS, seed_for
 from gpu_util import TOL_GRAD_REL, inputs, scale_f32, to_device, to_host64
 
 pytestmark = pytest.mark.gpu
@@ -41,7 +41,7 @@ def check(x, f, causal, d):
     return grads
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("N", [1, 65, 128, 129, 300, 1000])
 def test_deterministic_parity(d, causal, N):
@@ -49,7 +49,7 @@ def test_deterministic_parity(d, causal, N):
     check(x, f, causal, d)
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("Hq,Hkv", [(4, 2), (6, 1)])
 def test_deterministic_grouped_parity(d, causal, Hq, Hkv):
@@ -57,7 +57,7 @@ def test_deterministic_grouped_parity(d, causal, Hq, Hkv):
     check(x, f, causal, d)
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("causal", [False, True])
 def test_bitwise_reproducible(d, causal):
     import torch
@@ -133,19 +133,24 @@ def test_several_thousand_rows_sampled_heads():
         assert rel_err(got, want) <= TOL_GRAD_REL, name
 
 
-def test_head_dim_256_is_unsupported():
-    import exact_softmax_attention_fa_gb300 as fa
-    import torch
-    x, _ = inputs(1, 1, 64, 256, BASE_SEED + 730)
-    q, k, v, do = (to_device(x[n]) for n in ("q", "k", "v", "do"))
-    o, lse = fa.forward(q, k, v, causal=False)
-    with pytest.raises(fa.FAError):
-        fa.backward(q, k, v, o, lse, do, deterministic=True)
-    assert fa.fa_get_device_status() == 0
+def test_wide_head_d256_sampled_heads():
+    # the d = 256 configuration (B = 1, H = 2, N = 16384), causal and not;
+    # the oracle computes one head, compared whole in every gradient
+    w = WORKLOADS["wide_head_d256"]
+    for causal in (False, True):
+        x, f = inputs(w["B"], w["H"], w["N"], w["d"], seed_for(w))
+        scale = scale_f32(w["d"])
+        heads = [(0, 1)]
+        grads = run(x, causal, scale)
+        ref = oracle.attention_backward(f["q"], f["k"], f["v"], f["do"], causal, scale, heads=heads)
+        for name, g, r in zip(("dq", "dk", "dv"), grads, ref):
+            got = np.stack([to_host64(g)[b, h] for b, h in heads])
+            want = np.stack([r[b, h] for b, h in heads])
+            assert rel_err(got, want) <= TOL_GRAD_REL, (causal, name)
 
 
 @pytest.mark.parametrize("pre", ["fa_bwd_preprocess_stats", "fa_bwd_preprocess"])
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 def test_phases_compose_to_the_deterministic_backward(d, pre):
     import exact_softmax_attention_fa_gb300 as fa
     import torch

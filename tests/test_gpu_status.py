@@ -81,6 +81,8 @@ def _run_phase(fa, kernel, t, causal, scale, ws):
     ("dkdv", 11, 128), ("dkdv", 12, 128), ("dkdv", 13, 128),
     ("dq", 11, 128), ("dq", 12, 128), ("dq", 13, 64),
     ("main", 11, 64), ("main", 12, 128), ("main", 13, 64), ("main", 14, 128), ("main", 14, 64),
+    ("main", 11, 256), ("main", 12, 256), ("main", 13, 256), ("main", 14, 256),
+    ("dkdv", 13, 256), ("dq", 11, 256), ("dq", 12, 256), ("dq", 13, 256),
 ])
 def test_kernel_wait_gives_up_and_next_launch_is_correct(cuda_lib, kernel, role, d):
     import torch
