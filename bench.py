@@ -49,15 +49,18 @@ DEFAULT_WORKLOAD = "sweep_d128_N8192_full"
 PAGES_FWD_BWD_TFLOPS = {"sweep_d128_N8192_full": 201.0}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 NOMINAL_BF16_TFLOPS = 2250.0  # GB300 datasheet dense bf16 (without 2:4 sparsity), for context
+_CSRC = "exact_softmax_attention_fa_gb300/csrc/"
+_COMMON = [_CSRC + "sm103_ptx.cuh", _CSRC + "fa_kernel_common.cuh"]
+# Source files of each kernel: a committed ncu summary carries their hash,
+# and its DRAM traffic is reported only while the hash still matches.
 KERNEL_SOURCES = {
-    "fa_bwd_main": ["exact_softmax_attention_fa_gb300/csrc/fa_bwd.cu",
-                    "exact_softmax_attention_fa_gb300/csrc/sm103_ptx.cuh"],
-    "fa_bwd_dkdv": ["exact_softmax_attention_fa_gb300/csrc/fa_bwd.cu",
-                    "exact_softmax_attention_fa_gb300/csrc/sm103_ptx.cuh"],
-    "fa_bwd_dq": ["exact_softmax_attention_fa_gb300/csrc/fa_bwd_dq.cu",
-                  "exact_softmax_attention_fa_gb300/csrc/sm103_ptx.cuh"],
-    "fa_fwd": ["exact_softmax_attention_fa_gb300/csrc/fa_fwd_kernel.cuh",
-               "exact_softmax_attention_fa_gb300/csrc/sm103_ptx.cuh"],
+    "fa_bwd_main": [_CSRC + "fa_bwd.cu"] + _COMMON,
+    "fa_bwd_dkdv": [_CSRC + "fa_bwd.cu"] + _COMMON,
+    "fa_bwd_dq": [_CSRC + "fa_bwd_dq.cu"] + _COMMON,
+    "fa_fwd": [_CSRC + "fa_fwd_kernel.cuh"] + _COMMON,
+    "fa_bwd256": [_CSRC + "fa_bwd256.cu"] + _COMMON,
+    "fa_bwd_dq256": [_CSRC + "fa_bwd_dq256.cu"] + _COMMON,
+    "bwd_pre": [_CSRC + "fa_bwd.cu"] + _COMMON,
 }
 
 
