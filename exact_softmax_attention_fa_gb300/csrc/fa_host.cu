@@ -351,7 +351,9 @@ fa_status_t fa_fwd_bwd_host(const void* q, const void* k, const void* v, const v
     }
     ok(cudaStreamWaitEvent(bs, cs->ev[EV_DO0 + g], 0));
     uint8_t *q_g = Qd + off, *k_g = Kd + off, *v_g = Vd + off, *do_g = dOd + off;
-    run(fa_bwd_preprocess(Od + off, Ld + g0 * N, do_g, 1, hg, N, d, ws, wsb, bs));
+    // d = 128 runs the dQ kernel, which needs no zeroed accumulator
+    if (d == 128) run(fa_bwd_preprocess_stats(Od + off, Ld + g0 * N, do_g, 1, hg, N, d, ws, wsb, bs));
+    else run(fa_bwd_preprocess(Od + off, Ld + g0 * N, do_g, 1, hg, N, d, ws, wsb, bs));
     if (d == 128) {
       ok(cudaEventRecord(cs->ev[EV_PRE0 + g], bs));
       ok(cudaStreamWaitEvent(qs, cs->ev[EV_PRE0 + g], 0));
