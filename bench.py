@@ -498,8 +498,8 @@ def run_ours(args, p: dict, name: str, world: int, rank: int, local: int) -> dic
     if bwd_names[1] == "bwd_dkdv":
         kernels = {"fa_fwd": (phase_ms[0], f_fwd), "fa_bwd_dkdv": (phase_ms[2], 0.8 * f_bwd),
                    "fa_bwd_dq": (phase_ms[3], 0.2 * f_bwd)}
-    else:
-        kernels = {"fa_fwd": (phase_ms[0], f_fwd), "fa_bwd_main": (phase_ms[2], f_bwd)}
+    else:  # the atomic main kernel: fa_bwd.cu at d = 64, fa_bwd256.cu at d = 256
+        kernels = {"fa_fwd": (phase_ms[0], f_fwd), ("fa_bwd256" if d == 256 else "fa_bwd_main"): (phase_ms[2], f_bwd)}
     # The denominator: the burst bf16 peak for kernels timed in a short
     # region that the power cap did not throttle, the sustained one when the
     # clock sampler saw the power cap active. Both fractions are reported.
