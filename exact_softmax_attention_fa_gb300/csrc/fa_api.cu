@@ -494,7 +494,11 @@ fa_status_t fa_bwd_gqa_deterministic(const void* q, const void* k, const void* v
   a.deterministic = 1;
   cudaError_t e = launch_bwd_pre(a, stream);
   if (e == cudaSuccess) e = launch_bwd_main(a, stream);  // dK, dV only
+  // The dQ kernel reads nothing the dK/dV pass writes: it may take the SMs
+  // that pass leaves idle in its last round.
+  a.overlap_prev = 1;
   if (e == cudaSuccess) e = launch_bwd_dq(a, stream);
+  a.overlap_prev = 0;
   if (e == cudaSuccess) e = launch_bwd_post(a, stream);  // split groups' dK, dV sums, if any
   return from_cuda(e);
 }

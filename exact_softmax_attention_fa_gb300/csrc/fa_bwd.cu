@@ -763,6 +763,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
   float* sLD = reinterpret_cast<float*>(sDS + C::DS_BYTES);
   uint8_t* sDQ = sDS + C::DS_BYTES + C::LD_BYTES;  // 1024-aligned: DS and LD sizes are multiples of 1024
   const int warp = threadIdx.x >> 5;
+  // Without dQ this pass writes nothing the dQ kernel reads, so a dQ kernel
+  // queued behind it may take SMs as soon as this grid's CTAs leave them.
+  if constexpr (!DQ) griddep_launch_dependents();
   const int wg = warp >> 2;
 
   if (threadIdx.x == 0) {

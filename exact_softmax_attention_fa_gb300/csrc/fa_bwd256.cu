@@ -578,6 +578,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd256_kernel(const __grid_con
   uint8_t* sDS = sDOo + C::HALF_BYTES;
   float* sLD = reinterpret_cast<float*>(sDS + C::DS_BYTES);
   const int warp = threadIdx.x >> 5;
+  // Without dQ this pass writes nothing the dQ kernel reads, so a dQ kernel
+  // queued behind it may take SMs as soon as this grid's CTAs leave them.
+  if constexpr (!DQ) griddep_launch_dependents();
 
   if (threadIdx.x == 0) {
     mbar_init(&sh.kv_full, 1);

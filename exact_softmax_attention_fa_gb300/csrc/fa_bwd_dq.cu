@@ -474,6 +474,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
   __syncthreads();
   tc_fence_after_sync();
   if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
+  // Launched to overlap the dK/dV pass (overlap_prev), this grid must not
+  // complete before that pass has: work queued after it may read dK and dV.
+  if (threadIdx.x == 0) griddep_wait();
 }
 
 template <int HD, bool CAUSAL>
@@ -484,8 +487,17 @@ cudaError_t launch_t(const BwdLaunch& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const long long items = static_cast<long long>(a.BH) * ((a.N + 127) / 128);
   const long long grid = items < a.num_sms ? items : a.num_sms;
-  kern<<<static_cast<unsigned>(grid), kThreads, C::SMEM_BYTES, stream>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = a.overlap_prev ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 }  // namespace

@@ -70,6 +70,10 @@ struct BwdLaunch {
   uint64_t wait_limit_ns;
   int num_sms;
   uint32_t debug_skip;  // test hook: role (WHERE_*) whose first arrival block 0 leaves out; 0 = none
+  // 1: the dQ kernel is launched to overlap the kernel before it in the
+  // stream, which must be the dK/dV pass of the same call (it reads nothing
+  // that pass writes); it still completes only after that pass has.
+  int overlap_prev;
 };
 
 // Checks of the sizes, flag and scale common to every entry point; *empty is

@@ -292,6 +292,18 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch. launch_dependents: a kernel launched after
+// this one with programmatic stream serialization may start once every CTA
+// of this grid has executed it (or exited); its CTAs then take SMs as this
+// grid's CTAs leave them. wait: blocks until the grids this one may overlap
+// have completed and their memory is visible (returns at once without them).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
 // numeric helpers
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float ex2_approx(float x) {

@@ -219,6 +219,12 @@ fa_status_t fa_bwd_main(const void* q, const void* k, const void* v, const void*
  *   writes dk and dv.
  * fa_bwd_dq: per 128-row query tile, recomputes S, P, dP and dS for every key
  *   tile it sees and sums dQ on chip in key order; writes dq.
+ * Within fa_bwd_deterministic (and fa_bwd at d = 128) the dQ kernel is
+ * launched to overlap the dK/dV kernel before it on the stream (programmatic
+ * dependent launch: it takes the SMs the dK/dV pass leaves idle in its last
+ * round) and completes only after that kernel has, so work queued after the
+ * call sees dq, dk and dv final. The separate entry points launch without
+ * the overlap; an event recorded between them would serialise it anyway.
  */
 fa_status_t fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* dO, void* dk, void* dv, int B,
                         int H, int N, int d, int causal, float scale, void* workspace, size_t workspace_bytes,
