@@ -600,9 +600,9 @@ def run_ours(args, p: dict, name: str, world: int, rank: int, local: int) -> dic
                         "vs_nominal": {"fwd": fwd_tf / NOMINAL_BF16_TFLOPS, "fwd_bwd": fwd_bwd_tf / NOMINAL_BF16_TFLOPS,
                                        "peak_tflops": NOMINAL_BF16_TFLOPS}},
         "phase_ms": {"fwd": phase_ms[0], bwd_names[0]: phase_ms[1], bwd_names[1]: phase_ms[2],
-                     bwd_names[2]: phase_ms[3],
-                     "note": "second timed pass, events between the phases (no overlap); value, ms_per_step and "
-                             "the fwd/bwd rates come from the fa_fwd + fa_bwd pass"},
+                     bwd_names[2]: phase_ms[3]},
+        "phase_ms_source": "second timed pass, events between the phases (no overlap); value, ms_per_step and "
+                           "the fwd/bwd rates come from the fa_fwd + fa_bwd pass",
         "roofline": roofline, "roofline_secondary": roofline_other,
         # The whole backward (all its kernels) against the same peak, with
         # the method's FLOPs (2.5x forward), not the kernels' executed ones.
