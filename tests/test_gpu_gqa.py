@@ -135,3 +135,39 @@ def test_split_and_unsplit_groups_agree(causal, d):
         outs.append(g)
     for a, b in zip(outs[0][1:], outs[1][1:]):
         assert rel_err(to_host64(a), to_host64(b)) <= 1e-2
+
+
+@pytest.mark.parametrize("Hq,Hkv,N", [(16, 1, 1024), (2, 2, 4096)])
+def test_work_queued_after_the_backward_sees_final_gradients(Hq, Hkv, N):
+    """At d = 128 fa_bwd lets its dQ kernel start on SMs the dK/dV pass leaves
+    idle; the call must still complete only when both have. With one K/V head
+    for 16 query heads the dK/dV pass has a few long work items and the dQ
+    kernel many short ones, so the dQ kernel ends first. dk, dv and dq are
+    zeroed before every call, and a copy queued on the same stream right
+    after the call must equal the final gradients, which match the oracle."""
+    import torch
+    import exact_softmax_attention_fa_gb300 as fa
+    B, d, causal = 1, 128, False
+    scale = scale_f32(d)
+    x, f = gqa_inputs(B, Hq, Hkv, N, d, BASE_SEED + 470 + Hq)
+    q, k, v, do = (to_device(x[n]) for n in ("q", "k", "v", "do"))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
+    fa.fa_fwd_gqa(q, k, v, o, lse, causal, scale)
+    ws = torch.empty(fa.fa_bwd_gqa_workspace_size(B, Hq, Hkv, N, d), dtype=torch.uint8, device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    copies = []
+    for _ in range(4):
+        for g in (dq, dk, dv):
+            g.zero_()
+        fa.fa_bwd_gqa(q, k, v, o, lse, do, dq, dk, dv, causal, scale, ws)
+        copies.append(tuple(g.clone() for g in (dq, dk, dv)))
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == 0
+    for c in copies:
+        for got, final in zip(c, (dq, dk, dv)):
+            assert bool((got.view(torch.int16) == final.view(torch.int16)).all())
+    ref = oracle.attention_backward(f["q"], f["k"], f["v"], f["do"], causal, scale)
+    for name, g, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+        e = rel_err(to_host64(g), r)
+        assert e <= TOL_GRAD_REL, (name, Hq, Hkv, N, e)
