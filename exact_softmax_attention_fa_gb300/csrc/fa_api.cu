@@ -186,20 +186,38 @@ size_t splitkv_bytes(long long BH, int Nq, int d, int splits) {
          align_up(static_cast<size_t>(splits) * BH * Nq * 4, 256);
 }
 
-// Automatic number of key ranges: enough items for about two per SM when the
-// query tiles alone are too few (short query blocks such as decoding), at
-// least one key tile per range, and no more ranges than the workspace holds.
-// units: query-head units (heads, or packed head groups), tq: query tiles per
-// unit; BH, Nq size the partials.
-int auto_splits(long long units, long long tq, int Nk, int d, int sms, long long BH, int Nq, size_t room) {
+// Automatic number of key ranges. Work items are (query-tile pair, key
+// range); the persistent grid runs them in rounds of one per SM, so the
+// busiest CTA processes ceil(items * s / SMs) items of ceil(Tk / s) key tiles
+// each, plus a fixed cost per item (its Q load, first S product and
+// epilogue, about two key tiles' time). The count minimising that estimate
+// is taken (a larger one must win by 1 %), among counts whose fp32 partials
+// fit the workspace and stay below a sixteenth of the K/V bytes the call
+// reads (short query blocks such as decoding; a long query block keeps one
+// range). units: query-head units (heads, or packed head groups), tq: query
+// tiles per unit; BH, Nq size the partials, BHkv the K/V heads.
+int auto_splits(long long units, long long tq, int Nk, int d, int sms, long long BH, int Nq, long long BHkv,
+                size_t room) {
+  constexpr double kItemCost = 2.0;  // key tiles' time
   const long long nt = d <= 128 ? 2 : 1;  // query tiles per CTA
   const long long items = units * ((tq + nt - 1) / nt);
   const int Tk = (Nk + 127) / 128;
-  if (items >= sms || Tk < 2) return 1;
-  long long want = (2LL * sms + items - 1) / items;
-  want = std::min<long long>(want, std::min(Tk, kMaxSplits));
-  while (want > 1 && splitkv_bytes(BH, Nq, d, static_cast<int>(want)) > room) --want;
-  return static_cast<int>(std::max<long long>(want, 1));
+  if (Tk < 2 || sms <= 0 || items <= 0) return 1;
+  const double kv_bytes = static_cast<double>(BHkv) * Nk * d * 2 * 2;
+  int best = 1;
+  double best_t = 1e300;
+  for (int s = 1; s <= std::min(Tk, kMaxSplits); ++s) {
+    const int per = (Tk + s - 1) / s;
+    if ((Tk + per - 1) / per != s) continue;  // the count the call would actually use differs
+    if (s > 1 && (splitkv_bytes(BH, Nq, d, s) > room || splitkv_bytes(BH, Nq, d, s) * 16.0 > kv_bytes)) break;
+    const double rounds = static_cast<double>((items * s + sms - 1) / sms);
+    const double t = rounds * (per + kItemCost);
+    if (t < best_t * 0.99) {
+      best_t = t;
+      best = s;
+    }
+  }
+  return best;
 }
 
 // fp32 partial dK + dV of one chunk of a group, for every K/V head.
@@ -300,7 +318,7 @@ fa_status_t fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o,
   if (splits == 0) {
     DeviceState* ds0 = device_state(&st);
     if (!ds0) return st;
-    splits = auto_splits(BH / pack, (Nq + 128 / pack - 1) / (128 / pack), Nk, d, ds0->num_sms, BH, Nq,
+    splits = auto_splits(BH / pack, (Nq + 128 / pack - 1) / (128 / pack), Nk, d, ds0->num_sms, BH, Nq, BHkv,
                          workspace ? workspace_bytes : 0);
   }
   int per = (Tk + splits - 1) / splits;  // key tiles per range; no range is empty
