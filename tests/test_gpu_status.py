@@ -74,6 +74,8 @@ def _run_phase(fa, kernel, t, causal, scale, ws):
     elif kernel == "main":
         fa.fa_bwd_main(q, k, v, do, dk, dv, causal, scale, ws)
         fa.fa_bwd_postprocess(dq, ws)
+    elif kernel == "bwd":  # the whole call: at d = 128 its dQ kernel overlaps the dK/dV pass
+        fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, causal, scale, ws)
 
 
 @pytest.mark.parametrize("kernel,role,d", [
@@ -83,6 +85,7 @@ def _run_phase(fa, kernel, t, causal, scale, ws):
     ("main", 11, 64), ("main", 12, 128), ("main", 13, 64), ("main", 14, 128), ("main", 14, 64),
     ("main", 11, 256), ("main", 12, 256), ("main", 13, 256), ("main", 14, 256),
     ("dkdv", 13, 256), ("dq", 11, 256), ("dq", 12, 256), ("dq", 13, 256),
+    ("bwd", 11, 128), ("bwd", 12, 128), ("bwd", 13, 128),
 ])
 def test_kernel_wait_gives_up_and_next_launch_is_correct(cuda_lib, kernel, role, d):
     import torch
@@ -118,7 +121,7 @@ def test_kernel_wait_gives_up_and_next_launch_is_correct(cuda_lib, kernel, role,
         assert np.abs(to_host64(t["o"]) - o_ref).max() <= TOL_O
         return
     ref = dict(zip(("dq", "dk", "dv"), oracle.attention_backward(f["q"], f["k"], f["v"], f["do"], causal, scale)))
-    names = {"dkdv": ("dk", "dv"), "dq": ("dq",), "main": ("dq", "dk", "dv")}[kernel]
+    names = {"dkdv": ("dk", "dv"), "dq": ("dq",), "main": ("dq", "dk", "dv"), "bwd": ("dq", "dk", "dv")}[kernel]
     for n in names:
         got = to_host64(t[n])
         assert np.abs(got - ref[n]).max() / np.abs(ref[n]).max() <= TOL_GRAD_REL, n
