@@ -225,18 +225,21 @@ size_t kv_part_bytes(long long BHkv, int N, int d) { return static_cast<size_t>(
 
 // How many work items share one (K/V head, key tile) when g query heads read
 // the same K/V head. One item per group keeps dK, dV on chip; splitting the
-// group adds items (fewer idle SMs in the last round) and, under a causal
-// mask, shortens the longest item, at the price of fp32 partials written to
-// the workspace and summed by a post kernel. The estimate compares, per
-// candidate, the tiles the busiest SM processes (a tile = 5 MMAs of 128x128xd
-// at ~6 TFLOP/s per SM) plus the post kernel's read of the partials at
-// ~6 TB/s (their writes overlap the main kernel's compute); a split must win
-// by 2 %. d = 256 keeps one item per group.
-int choose_kv_chunks(long long BHkv, int g, int N, int d, int causal, int sms, size_t part_room) {
+// group adds items and, under a causal mask, shortens the longest item (key
+// tile 0 meets every query tile of every head of the group), at the price of
+// fp32 partials that the main kernel writes and a post kernel reads. The
+// estimate, in 128x128xd products at ~6 TFLOP/s per SM: the longest item
+// against the average per SM, with the dQ kernel's 3 products per tile pair
+// counted into the average when it runs after the dK/dV pass and takes the
+// SMs that pass leaves idle (dq_separate); without it, non-causal items of
+// equal length run in whole rounds. A split must win by 2 %. d = 256 keeps
+// one item per group.
+int choose_kv_chunks(long long BHkv, int g, int N, int d, int causal, int sms, size_t part_room, bool dq_separate) {
   if (g <= 1 || d == 256 || sms <= 0) return 1;
   const double T = static_cast<double>((N + 127) / 128);
-  const double t_tile = 10.0 * 128 * 128 * d / 6.0e12;
-  const double total = static_cast<double>(BHkv) * g * (causal ? T * (T + 1) / 2 : T * T);
+  const double t_prod = 2.0 * 128 * 128 * d / 6.0e12;
+  const double pairs = static_cast<double>(BHkv) * g * (causal ? T * (T + 1) / 2 : T * T);
+  const double per_pair = dq_separate ? 4.0 : 5.0;  // products per tile pair in the kernel holding dK, dV
   int best = 1;
   double best_t = 1e300;
   for (int chunks = 1; chunks <= g; ++chunks) {
@@ -244,8 +247,13 @@ int choose_kv_chunks(long long BHkv, int g, int N, int d, int causal, int sms, s
     if (chunks > 1 && static_cast<size_t>(chunks) * kv_part_bytes(BHkv, N, d) > part_room) break;
     const double gs = g / chunks;
     const double items = static_cast<double>(BHkv) * chunks * T;
-    const double tiles = causal ? std::max(gs * T, total / sms) : std::ceil(items / sms) * gs * T;
-    const double t = tiles * t_tile + (chunks > 1 ? chunks * kv_part_bytes(BHkv, N, d) / 6.0e12 : 0.0);
+    const double longest = per_pair * gs * T;
+    double work;
+    if (dq_separate)
+      work = std::max(longest, (per_pair + 3.0) * pairs / sms);
+    else
+      work = causal ? std::max(longest, per_pair * pairs / sms) : std::ceil(items / sms) * longest;
+    const double t = work * t_prod + (chunks > 1 ? 2.0 * chunks * kv_part_bytes(BHkv, N, d) / 6.0e12 : 0.0);
     if (t < best_t * 0.98) {
       best_t = t;
       best = chunks;
@@ -405,8 +413,11 @@ struct BwdTensors {
   void *dq, *dk, *dv;
 };
 
+// dq_separate: the call forms dQ with the separate dQ kernel after the dK/dV
+// pass (the deterministic route), which the work-item split takes into account.
 fa_status_t prepare_bwd(const BwdTensors& t, int B, int H, int Hkv, int N, int d, int causal, float scale,
-                        void* workspace, size_t workspace_bytes, bool* empty, BwdLaunch* a) {
+                        void* workspace, size_t workspace_bytes, bool* empty, BwdLaunch* a,
+                        bool dq_separate = false) {
   fa_status_t st = check_common(B, H, N, d, causal, scale, empty);
   if (st != FA_OK) return st;
   st = check_heads(H, Hkv);
@@ -445,7 +456,7 @@ fa_status_t prepare_bwd(const BwdTensors& t, int B, int H, int Hkv, int N, int d
   a->sched = reinterpret_cast<uint32_t*>(ws + wl.sched_off);
   // Room after the fixed layout holds the split groups' dK, dV partials.
   const size_t part_room = workspace_bytes > wl.total ? workspace_bytes - wl.total : 0;
-  a->chunks = choose_kv_chunks(BHkv, H / (Hkv > 0 ? Hkv : 1), N, d, causal, ds->num_sms, part_room);
+  a->chunks = choose_kv_chunks(BHkv, H / (Hkv > 0 ? Hkv : 1), N, d, causal, ds->num_sms, part_room, dq_separate);
   a->kv_part = reinterpret_cast<float*>(ws + wl.total);
   if (!make_map_f32_acc(&a->tmdQacc, a->dq_acc, BH, round_up_128(N), d)) return FA_ERR_CUDA;
   a->status = ds->status;
@@ -507,7 +518,7 @@ fa_status_t fa_bwd_gqa_deterministic(const void* q, const void* k, const void* v
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
   BwdLaunch a;
   st = prepare_bwd(BwdTensors{q, k, v, o, dO, lse, dq, dk, dv}, B, Hq, Hkv, N, d, causal, scale, workspace,
-                   workspace_bytes, &empty, &a);
+                   workspace_bytes, &empty, &a, true);
   if (st != FA_OK || empty) return st;
   a.deterministic = 1;
   cudaError_t e = launch_bwd_pre(a, stream);
