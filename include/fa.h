@@ -225,6 +225,11 @@ fa_status_t fa_bwd_main(const void* q, const void* k, const void* v, const void*
  * round) and completes only after that kernel has, so work queued after the
  * call sees dq, dk and dv final. The separate entry points launch without
  * the overlap; an event recorded between them would serialise it anyway.
+ * The dK/dV kernel signals programmatic launch completion at its start, so a
+ * kernel a caller queues after fa_bwd_dkdv with programmatic stream
+ * serialization must wait for its prerequisite grid (as that launch mode
+ * always requires) before it reads dk or dv; ordinary launches are ordered
+ * as usual.
  */
 fa_status_t fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* dO, void* dk, void* dv, int B,
                         int H, int N, int d, int causal, float scale, void* workspace, size_t workspace_bytes,
