@@ -20,6 +20,9 @@ __global__ void __launch_bounds__(256) fwd_combine_kernel(const float* __restric
                                                           int BH, int Nq, int Nk, int causal, int causal_off,
                                                           int splits, int keys_per_split) {
   constexpr int PER = HD / 32;
+  // Launched to overlap the forward's last round: its partials are final
+  // only once that grid has completed.
+  griddep_wait();
   const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (row >= static_cast<long long>(BH) * Nq) return;
@@ -62,9 +65,21 @@ __global__ void __launch_bounds__(256) fwd_combine_kernel(const float* __restric
 template <int HD>
 cudaError_t launch_combine_t(const FwdLaunch& a, cudaStream_t stream) {
   const long long threads = static_cast<long long>(a.BH) * a.Nq * 32;
-  fwd_combine_kernel<HD><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, stream>>>(
-      a.o_part, a.lse_part, a.o, a.lse, a.BH, a.Nq, a.Nk, a.causal, a.causal_off, a.splits, a.kv_per_split * 128);
-  return cudaGetLastError();
+  // Programmatic dependent launch: the forward (splits > 1) signals at its
+  // start, so these blocks are queued as its CTAs leave SMs and wait in
+  // griddep_wait for its completion instead of for a launch after it.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((threads + 255) / 256));
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fwd_combine_kernel<HD>, static_cast<const float*>(a.o_part),
+                            static_cast<const float*>(a.lse_part), a.o, a.lse, a.BH, a.Nq, a.Nk, a.causal,
+                            a.causal_off, a.splits, a.kv_per_split * 128);
 }
 
 }  // namespace

@@ -617,6 +617,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   uint8_t* sK = sQ + C::NT * C::TILE_BYTES;
   uint8_t* sV = sK + C::KST * C::TILE_BYTES;
   const int warp = threadIdx.x >> 5;
+  // Split key ranges: the combine kernel queued next may take SMs as this
+  // grid's CTAs leave them (it waits for this grid before it reads).
+  if (p.splits > 1) griddep_launch_dependents();
 
   if (threadIdx.x == 0) {
     for (int t = 0; t < 2; ++t) mbar_init(&sh.q_full[t], 1);
